@@ -1,0 +1,169 @@
+/*
+ * vp.h -- C ABI of libvp: vocab-parallel cross-entropy over a tied,
+ * vocab-sharded LM head, and the vocab-sharded embedding gather, on one
+ * B300 (sm_103a).
+ *
+ * Notation: N tokens, H hidden size, V vocabulary size, T vocab shards.
+ * X is [N,H] row-major, W is [V,H] row-major and tied between the embedding
+ * and the LM head.  Shard t owns vocab ids [t*V/T, (t+1)*V/T)  (MiniMind-tron
+ * book, ch. 5 "Vocab Parallelism", sec. 5.1 and 5.2.1); V % T must be 0.
+ * On one GPU the T shards are a tiling of the vocab dimension inside the
+ * kernels and every cross-shard reduction the pages do with a collective is
+ * an on-device reduction; nothing here talks to another GPU.
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers owned by the caller (the library keeps no
+ *     reference after the call returns); the library never allocates device
+ *     memory -- scratch comes from the caller's `workspace`.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream).  A returned VP_OK means "arguments
+ *     accepted and kernels launched"; results are ready when the stream is.
+ *   - dtype applies to X, W, the embedding output and dX.  VP_BF16 runs on the
+ *     tcgen05 tensor cores with fp32 accumulation; VP_F32 runs on CUDA-core
+ *     FMAs (no TF32) for full fp32 accuracy.
+ *   - Arguments are checked before any launch: N, H, V, T <= 0 or V % T != 0
+ *     -> VP_ERR_INVALID_ARG; a NULL required pointer -> VP_ERR_INVALID_ARG;
+ *     a pointer not 16-byte aligned or H*sizeof(dtype) not a multiple of 16
+ *     -> VP_ERR_UNSUPPORTED; a workspace smaller than the minimum
+ *     -> VP_ERR_WORKSPACE; a CUDA launch error -> VP_ERR_CUDA.  On any error
+ *     nothing has been launched or written, except for VP_ERR_CUDA.
+ *   - Every wait inside a kernel is bounded in time.  A wait that runs out
+ *     sets a bit in the workspace's device status word (vp_read_device_status)
+ *     and the kernel returns early; outputs are then undefined.
+ */
+#ifndef VP_H
+#define VP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { VP_F32 = 0, VP_BF16 = 1 } vp_dtype;
+
+typedef enum {
+  VP_OK = 0,
+  VP_ERR_INVALID_ARG = 1,
+  VP_ERR_UNSUPPORTED = 2,
+  VP_ERR_WORKSPACE = 3,
+  VP_ERR_CUDA = 4
+} vp_status;
+
+/* Device status bits written into the workspace header by the kernels. */
+#define VP_DEV_TIMEOUT_PRODUCER 0x1u /* TMA producer gave up waiting for a free stage  */
+#define VP_DEV_TIMEOUT_MMA      0x2u /* MMA issuer gave up waiting for data / TMEM      */
+#define VP_DEV_TIMEOUT_EPILOGUE 0x4u /* epilogue gave up waiting for an accumulator     */
+
+/* Human-readable name of a status code (static storage). */
+const char* vp_status_string(vp_status s);
+
+/* Library version string, e.g. "libvp 0.1 sm_103a". */
+const char* vp_version(void);
+
+/*
+ * vp_embed_fwd -- vocab-parallel embedding lookup, the shard outputs summed.
+ *
+ * "Vocab Parallelism" sec. 5.2.1 (masked local lookup; the V=8 worked table)
+ * and "Vocab parallelism: how to split embedding and LM head", figure 1:
+ * shard t maps an id outside [t*V/T,(t+1)*V/T) to local row 0, looks it up
+ * and zeroes the row; the T shard outputs are summed.  Exactly one shard
+ * contributes, so
+ *     out[n,:] = +0.0 + W[ids[n],:]   if 0 <= ids[n] < V
+ *     out[n,:] = 0                    otherwise,
+ * bit-exact (a -0.0 weight comes out +0.0, as a sum from +0.0 gives).
+ *
+ *   ids  int64 [N]        token ids (any value; out-of-range ids give zero rows)
+ *   W    dtype [V,H]      tied weight, row-major
+ *   out  dtype [N,H]      written, row-major
+ * Requires H*sizeof(dtype) % 16 == 0 and 16-byte aligned W and out.
+ */
+vp_status vp_embed_fwd(const int64_t* ids, const void* W, void* out,
+                       int64_t N, int64_t H, int64_t V, int T, vp_dtype dtype,
+                       void* stream);
+
+/*
+ * vp_lmhead_ce_workspace_size -- bytes of device workspace for a call.
+ *   pass 0: vp_lmhead_ce_fwd (exact size needed).
+ *   pass 1: vp_lmhead_ce_bwd with the vocab processed in chunks of
+ *           `vocab_chunk` ids (<= 0 or >= V: one chunk, the fastest).  Any
+ *           workspace at least this large for some chunk works; the backward
+ *           derives its chunk from the bytes it is given.
+ * Returns 0 for invalid arguments.
+ */
+size_t vp_lmhead_ce_workspace_size(int64_t N, int64_t H, int64_t V, int T,
+                                   vp_dtype dtype, int pass, int64_t vocab_chunk);
+
+/*
+ * vp_lmhead_ce_fwd -- fused LM head + vocab-parallel cross-entropy, forward.
+ *
+ * "Vocab Parallelism" sec. 5.3.1 and the interview note's figure 2 / key
+ * formulas: Z = X W^T is produced tile by tile and never stored.  For every
+ * shard t and token n the kernel reduces its logits slice to the local max
+ * m_t, the local sum S_t = sum exp(z - m_t) and the local target logit
+ * z_y^(t) (0 off-shard); an on-device merge gives
+ *     m = max_t m_t,  S = sum_t S_t e^(m_t - m),  lse = m + log S,
+ *     loss[n] = lse - z_y                      (0 for ignored targets),
+ *     loss_mean = sum_n loss[n] / max(1, N_valid)   (sec. 5.3.3).
+ * A target equal to ignore_index, or outside [0,V), is ignored; the latter
+ * kind is counted in n_bad.
+ *
+ *   X         dtype [N,H]    hidden states
+ *   W         dtype [V,H]    tied weight
+ *   targets   int64 [N]
+ *   loss      f32 [N]        written
+ *   lse       f32 [N]        written (log-sum-exp of every row, ignored or not;
+ *                            the backward consumes it)
+ *   loss_mean f32 [1]        written, or NULL
+ *   shard_stats f32 [T][3][N] written as (m_t, S_t, z_y^(t)), or NULL
+ *   n_bad     int32 [1]      written, or NULL
+ *   workspace device bytes >= vp_lmhead_ce_workspace_size(..., pass 0, 0),
+ *             16-byte aligned; overwritten.
+ */
+vp_status vp_lmhead_ce_fwd(const void* X, const void* W, const int64_t* targets,
+                           int64_t N, int64_t H, int64_t V, int T,
+                           int64_t ignore_index, vp_dtype dtype,
+                           float* loss, float* lse, float* loss_mean,
+                           float* shard_stats, int32_t* n_bad,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * vp_lmhead_ce_bwd -- backward of vp_lmhead_ce_fwd.
+ *
+ * "Vocab Parallelism" sec. 5.3.2 and the interview note's key formulas: the
+ * logit gradient is local to each shard, dZ[n,j] = g_n (softmax_j - 1[j=y_n]),
+ * with g_n = dloss[n] (or 1/max(1,N_valid) when dloss is NULL, the gradient of
+ * the mean) on valid tokens and 0 on ignored ones.  Each logit tile is
+ * recomputed from X and W, dZ is formed in the epilogue and stored in bf16
+ * (f32 for VP_F32) scratch for one vocab chunk, then
+ *     dW[chunk] = dZ_chunk^T X,     dX += dZ_chunk W[chunk]
+ * run on the tensor cores; the sum of dX over chunks is the on-device form of
+ * the column-parallel LM head's dX all-reduce.
+ *
+ *   lse    f32 [N]           from vp_lmhead_ce_fwd
+ *   dloss  f32 [N] or NULL
+ *   dX     dtype [N,H]       overwritten
+ *   dW     f32 [V,H]         overwritten (fp32 so that a caller can add the
+ *                            tied embedding's gradient)
+ *   workspace  >= vp_lmhead_ce_workspace_size(..., pass 1, c) for some chunk c
+ */
+vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t* targets,
+                           const float* lse, const float* dloss,
+                           int64_t N, int64_t H, int64_t V, int T,
+                           int64_t ignore_index, vp_dtype dtype,
+                           void* dX, float* dW,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * vp_read_device_status -- synchronise `stream` and copy the device status
+ * word of `workspace` (VP_DEV_* bits; 0 = no kernel gave up waiting) into
+ * *flags.  The word is cleared at the start of every fwd/bwd call.
+ */
+vp_status vp_read_device_status(const void* workspace, uint32_t* flags, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VP_H */

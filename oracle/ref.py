@@ -88,10 +88,12 @@ def logits(X: np.ndarray, W: np.ndarray) -> np.ndarray:
 
 
 def target_masks(y: np.ndarray, V: int, ignore_index: int = IGNORE_INDEX):
-    """(valid, bad): valid = target in [0, V); bad = neither valid nor ignored."""
+    """(valid, bad): valid = target in [0, V) and not ignore_index (an
+    ignore_index inside [0, V) still marks the position as ignored);
+    bad = out of range and not ignore_index."""
     y = np.asarray(y, dtype=np.int64)
     in_range = (y >= 0) & (y < V)
-    return in_range, (~in_range) & (y != ignore_index)
+    return in_range & (y != ignore_index), (~in_range) & (y != ignore_index)
 
 
 # --------------------------------------------------------------------------
@@ -144,10 +146,11 @@ def cross_entropy_three_reductions(Z: np.ndarray, y: np.ndarray, V: int, T: int,
             "n_valid": n_valid, "n_bad": int(bad.sum())}
 
 
-def shard_local_stats(Z: np.ndarray, y: np.ndarray, V: int, T: int) -> np.ndarray:
+def shard_local_stats(Z: np.ndarray, y: np.ndarray, V: int, T: int,
+                      ignore_index: int = IGNORE_INDEX) -> np.ndarray:
     """Per shard t and token n the triple (m_t, S_t, z_y^(t)): local max, sum of
-    exp(z - m_t) over the shard, and the target logit if the target is in the
-    shard (else 0).  Returns an array [T, 3, N]."""
+    exp(z - m_t) over the shard, and the target logit if the (non-ignored)
+    target is in the shard, else 0.  Returns an array [T, 3, N]."""
     Z = np.asarray(Z, dtype=np.float64)
     y = np.asarray(y, dtype=np.int64)
     n = Z.shape[0]
@@ -157,7 +160,7 @@ def shard_local_stats(Z: np.ndarray, y: np.ndarray, V: int, T: int) -> np.ndarra
         mt = zt.max(axis=1)
         out[t, 0] = mt
         out[t, 1] = np.exp(zt - mt[:, None]).sum(axis=1)
-        own = (y >= a) & (y < b)
+        own = (y >= a) & (y < b) & (y != ignore_index)
         out[t, 2] = np.where(own, zt[np.arange(n), np.where(own, y - a, 0)], 0.0)
     return out
 
@@ -191,9 +194,10 @@ def grad_logits(Z: np.ndarray, y: np.ndarray, lse: np.ndarray, g: np.ndarray) ->
     n, V = Z.shape
     p = np.exp(Z - np.asarray(lse, dtype=np.float64)[:, None])
     onehot = np.zeros_like(p)
-    valid = (np.asarray(y) >= 0) & (np.asarray(y) < V)
-    rows = np.nonzero(valid)[0]
+    in_range = (np.asarray(y) >= 0) & (np.asarray(y) < V)
+    rows = np.nonzero(in_range)[0]
     onehot[rows, np.asarray(y)[rows]] = 1.0
+    # ignored rows carry g_n = 0, so their onehot term vanishes with them
     return np.asarray(g, dtype=np.float64)[:, None] * (p - onehot)
 
 
@@ -212,7 +216,7 @@ def lmhead_ce_forward(X, W, y, V: int, T: int, ignore_index: int = IGNORE_INDEX)
     per-shard triples (for checking the shard statistics output)."""
     Z = logits(X, W)
     out = cross_entropy(Z, y, ignore_index)
-    out["shard_stats"] = shard_local_stats(Z, y, V, T)
+    out["shard_stats"] = shard_local_stats(Z, y, V, T, ignore_index)
     return out
 
 

@@ -124,6 +124,15 @@ def pin_ce_ignore_and_bad(o):
     np.testing.assert_allclose(r["mean"], ref.mean(), rtol=1e-12)
     r0 = o.cross_entropy(Z, np.full(6, IGN), IGN)
     assert r0["mean"] == 0.0 and r0["n_valid"] == 0
+    # an ignore_index inside [0, V) marks its positions ignored, as torch does
+    y3 = np.array([3, 3, 1, 9, 0, 3])
+    r3 = o.cross_entropy(Z, y3, 3)
+    t3 = torch.nn.functional.cross_entropy(torch.from_numpy(Z), torch.from_numpy(y3), ignore_index=3,
+                                           reduction="none").numpy()
+    np.testing.assert_allclose(r3["loss"], t3, rtol=1e-12)
+    assert r3["n_valid"] == 3 and r3["n_bad"] == 0
+    g3 = o.upstream_scale(y3, 10, 3)
+    np.testing.assert_allclose(g3, [0, 0, 1 / 3, 1 / 3, 1 / 3, 0])
 
 
 def pin_shard_invariance(o):

@@ -1,0 +1,92 @@
+"""libvp on the host, without a GPU: it loads, exports every function that
+include/*.h declares, and rejects bad arguments before launching anything."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import vocab_lm_head_vp_b300 as vp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(vp_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from vocab_lm_head_vp_b300 import build
+    build.build()
+    return vp._load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"vp_embed_fwd", "vp_lmhead_ce_fwd", "vp_lmhead_ce_bwd", "vp_lmhead_ce_workspace_size"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"libvp.so does not export {n}"
+
+
+def test_status_strings(lib):
+    for code, name in vp._STATUS.items():
+        assert lib.vp_status_string(code).decode() == name
+    assert b"sm_103a" in lib.vp_version()
+
+
+P = ctypes.c_void_p
+
+
+def test_embed_rejects_bad_arguments(lib):
+    ids, W, out = P(0x1000), P(0x2000), P(0x3000)
+    f = lib.vp_embed_fwd
+    assert f(ids, W, out, 4, 8, 10, 3, vp.VP_BF16, None) == 1       # V % T != 0
+    assert f(None, W, out, 4, 8, 10, 2, vp.VP_BF16, None) == 1      # null ids
+    assert f(ids, W, out, 0, 8, 10, 2, vp.VP_BF16, None) == 1       # N = 0
+    assert f(ids, W, out, 4, 8, 10, 2, 7, None) == 1                # unknown dtype
+    assert f(ids, P(0x2008), out, 4, 8, 10, 2, vp.VP_BF16, None) == 2  # W not 16-byte aligned
+    assert f(ids, W, out, 4, 6, 10, 2, vp.VP_BF16, None) == 2       # H*2 not a multiple of 16
+    assert f(ids, W, out, 4, 3, 10, 2, vp.VP_F32, None) == 2        # H*4 not a multiple of 16
+
+
+def test_ce_rejects_bad_arguments(lib):
+    X, W, y, ws = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
+    loss, lse = P(0x50000), P(0x60000)
+    fwd = lib.vp_lmhead_ce_fwd
+    args = lambda **k: dict(dict(X=X, W=W, y=y, N=6, H=64, V=16, T=4, dt=vp.VP_F32, loss=loss, lse=lse, ws=ws,
+                                 wsb=1 << 20), **k)
+
+    def call(a):
+        return fwd(a["X"], a["W"], a["y"], a["N"], a["H"], a["V"], a["T"], -100, a["dt"], a["loss"], a["lse"],
+                   None, None, None, a["ws"], a["wsb"], None)
+    assert call(args(T=5)) == 1
+    assert call(args(loss=None)) == 1
+    assert call(args(X=None)) == 1
+    assert call(args(V=-16)) == 1
+    assert call(args(X=P(0x10004))) == 2
+    assert call(args(H=63)) == 2
+    assert call(args(wsb=16)) == 3                                   # workspace too small
+    bwd = lib.vp_lmhead_ce_bwd
+    assert bwd(X, W, y, lse, None, 6, 64, 16, 3, -100, vp.VP_F32, P(0x70000), P(0x80000), ws, 1 << 20, None) == 1
+    assert bwd(X, W, y, None, None, 6, 64, 16, 4, -100, vp.VP_F32, P(0x70000), P(0x80000), ws, 1 << 20, None) == 1
+    assert bwd(X, W, y, lse, None, 6, 64, 16, 4, -100, vp.VP_F32, P(0x70008), P(0x80000), ws, 1 << 20, None) == 2
+    assert bwd(X, W, y, lse, None, 6, 64, 16, 4, -100, vp.VP_F32, P(0x70000), P(0x80000), ws, 64, None) == 3
+
+
+def test_workspace_sizes(lib):
+    N, H, V, T = 16384, 4096, 128256, 8
+    fwd = vp.workspace_size(N, H, V, T, vp.VP_BF16, 0)
+    # records: ceil(V/256) tiles x 2 segment slots x N tokens x (m, S) fp32, plus z_y
+    assert fwd >= 501 * 2 * N * 8 + N * 4 and fwd < 501 * 2 * N * 8 + N * 4 + 4096
+    one = vp.workspace_size(N, H, V, T, vp.VP_BF16, 1)
+    assert one >= N * V * 2 and one < N * V * 2 + N * 4 + 4096       # one chunk: bf16 dZ, no fp32 dX partial
+    c = vp.workspace_size(N, H, V, T, vp.VP_BF16, 1, 16032)
+    assert c >= N * 15872 * 2 + N * H * 4                              # chunk rounded to 256, + fp32 dX partial
+    assert vp.workspace_size(N, H, V, 7, vp.VP_BF16, 1) == 0           # V % T != 0
+    assert vp.workspace_size(6, 64, 16, 4, vp.VP_F32, 2) == 0          # unknown pass

@@ -1,0 +1,240 @@
+"""GPU parity of the vocab-parallel embedding and the fused LM head + CE
+(forward and backward) against the float64 oracle, element by element, on
+seeded inputs spanning several tiles with ragged tails, plus edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.ref as ref
+import synth
+import vocab_lm_head_vp_b300 as vp
+from golden_io import read
+from gpu_util import assert_loss_close, dev_inputs, grad_tol, np64, rel_fro
+
+pytestmark = pytest.mark.gpu
+IGN = -100
+
+
+def _bits(t):
+    return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32).cpu().numpy()
+
+
+def _oracle_embed_bits(ids, W_np, V, T, dtype):
+    o = ref.embed(ids, W_np.astype(np.float64), V, T)
+    if dtype == "bf16":
+        return torch.from_numpy(o.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    return o.astype(np.float32).view(np.int32)
+
+
+# ------------------------------------------------------------------ embedding
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_embed_worked_example(dtype):
+    """The V=8, T=2, ids [1,6] table of sec. 5.2.1 and figure 1's id 5."""
+    for name in ("embed_v8_t2_ids_1_6.txt", "embed_v8_t2_id5.txt"):
+        g = read(name)
+        V, T = int(g["V"][0]), int(g["T"][0])
+        ids = np.array([int(v) for v in g["ids"]])
+        H = 8
+        Wn = (np.arange(V * H, dtype=np.float32).reshape(V, H) + 1.0)
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        W = torch.from_numpy(Wn).to(tdt).cuda()
+        out = vp.embed_fwd(torch.from_numpy(ids).cuda(), W, T)
+        want = np.stack([Wn[int(s[1:])] if s != "0" else np.zeros(H, np.float32) for s in g["sum"]])
+        assert np.array_equal(out.float().cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("name", ["tiny", "minimind"])
+def test_embed_workload_bit_exact(name):
+    inp = synth.make_inputs(name)
+    wl = inp.wl
+    X, W, y = dev_inputs(inp)
+    ids = inp.targets
+    out = vp.embed_fwd(y, W, wl.T)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(out), _oracle_embed_bits(ids, inp.W, wl.V, wl.T, wl.dtype))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_embed_edge_ids_and_negative_zero(dtype):
+    rng = np.random.default_rng(9)
+    V, H, T = 1000, 136, 8
+    Wn = rng.standard_normal((V, H)).astype(np.float32)
+    Wn[7, 5] = -0.0
+    Wn[7, 6] = 0.0
+    ids = rng.integers(0, V, 333)
+    ids[:8] = [7, -1, V, -100, 0, V - 1, 7, 2 ** 40]
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    Wt = torch.from_numpy(Wn).to(tdt)
+    out = vp.embed_fwd(torch.from_numpy(ids).cuda(), Wt.cuda(), T)
+    Wexact = Wt.float().numpy()
+    want = _oracle_embed_bits(ids, Wexact, V, T, dtype)
+    assert np.array_equal(_bits(out), want)
+    assert _bits(out)[0, 5] == 0                      # -0.0 came out +0.0
+
+
+def test_embed_large_uniform_and_zipf():
+    """Full V128k shapes of the gather (N=16384, H=4096, V=128256), bit-exact
+    on sampled rows: uniform and Zipf ids."""
+    wl = synth.WORKLOADS["v128k"]
+    g = torch.Generator(device="cuda").manual_seed(5)
+    W = torch.randn(wl.V, wl.H, generator=g, device="cuda").to(torch.bfloat16)
+    rng = np.random.default_rng(17)
+    for ids in (rng.integers(0, wl.V, wl.N), synth.zipf_ids(rng, wl.N, wl.V, 1.1)):
+        idt = torch.from_numpy(ids).cuda()
+        out = vp.embed_fwd(idt, W, wl.T)
+        rows = rng.choice(wl.N, 64, replace=False)
+        got = out[torch.from_numpy(rows).cuda()].view(torch.int16).cpu()
+        want = W[idt[torch.from_numpy(rows).cuda()]].view(torch.int16).cpu()
+        assert torch.equal(got, want)
+
+
+# ------------------------------------------------------------------ forward + backward
+def _run(inp, T, ignore_index=IGN, dloss=None, vocab_chunk=None, shard_stats=True):
+    X, W, y = dev_inputs(inp)
+    f = vp.lmhead_ce_fwd(X, W, y, T, ignore_index, shard_stats=shard_stats)
+    dl = None if dloss is None else torch.from_numpy(dloss.astype(np.float32)).cuda()
+    dX, dW = vp.lmhead_ce_bwd(X, W, y, f["lse"], T, ignore_index, dloss=dl, vocab_chunk=vocab_chunk)
+    torch.cuda.synchronize()
+    assert vp.read_device_status(f["workspace"]) == 0
+    return f, dX, dW
+
+
+def _check(inp, T, f, dX, dW, ignore_index=IGN, dloss=None, check_stats=True):
+    wl = inp.wl
+    o = ref.lmhead_ce_forward(inp.X, inp.W, inp.targets, wl.V, T, ignore_index)
+    lse_ref = o["lse"]
+    assert_loss_close(np64(f["lse"]), lse_ref, wl.dtype, what="lse")
+    assert_loss_close(np64(f["loss"]), o["loss"], wl.dtype, scale=lse_ref, what="loss")
+    assert_loss_close(np64(f["mean"]), [o["mean"]], wl.dtype, scale=[np.abs(lse_ref).max()], what="mean")
+    assert int(f["n_bad"].item()) == o["n_bad"]
+    if check_stats:
+        st = np64(f["shard_stats"])
+        so = o["shard_stats"]
+        assert_loss_close(st[:, 0], so[:, 0], wl.dtype, what="m_t")
+        assert_loss_close(st[:, 2], so[:, 2], wl.dtype, what="z_y^(t)")
+        # S_t >= 1 (the max term); compare its log, the quantity the loss uses
+        assert_loss_close(np.log(st[:, 1]), np.log(so[:, 1]), wl.dtype, scale=so[:, 0], what="log S_t")
+    b = ref.lmhead_ce_backward(inp.X, inp.W, inp.targets, wl.V, ignore_index, dloss)
+    ex, ew = rel_fro(np64(dX), b["dX"]), rel_fro(np64(dW), b["dW"])
+    tol = grad_tol(wl.dtype)
+    assert ex <= tol and ew <= tol, f"rel Frobenius dX {ex:.2e} dW {ew:.2e} (tol {tol})"
+    return ex, ew
+
+
+def test_tiny_config_f32():
+    inp = synth.make_inputs("tiny")
+    f, dX, dW = _run(inp, inp.wl.T)
+    _check(inp, inp.wl.T, f, dX, dW)
+
+
+def test_page_t4_simulation_f32():
+    """The interview note's t=4 NumPy setup through the GPU: X = z, W = I
+    (H = V = 16), so the kernel's logits are exactly the page's z."""
+    z, y = synth.page_t4_simulation()
+    X = z.astype(np.float32)
+    W = np.eye(16, dtype=np.float32)
+    inp = synth.Inputs(synth.Workload("page_t4", 6, 16, 16, 4, "f32", 0.0, "uniform"), X, W, y, None, None)
+    f, dX, dW = _run(inp, 4)
+    _check(inp, 4, f, dX, dW)
+    dense = ref.cross_entropy(X.astype(np.float64), y)
+    assert np.allclose(np64(f["loss"]), dense["loss"])          # the page's printed True
+
+
+CASES = [  # N, H, V, T, dtype: several tiles, ragged tails, shard edges inside tiles
+    (300, 200, 1000, 4, "bf16"),
+    (130, 64, 520, 2, "bf16"),
+    (1, 64, 256, 1, "bf16"),
+    (257, 136, 770, 7, "bf16"),     # V/T = 110 < 256: one tile spans up to 4 shards
+    (64, 512, 6400, 16, "bf16"),
+    (77, 40, 99, 3, "f32"),
+    (200, 96, 640, 10, "f32"),
+]
+
+
+@pytest.mark.parametrize("N,H,V,T,dtype", CASES)
+def test_small_cases(N, H, V, T, dtype):
+    inp = synth.small_case(N, H, V, T, dtype, seed=N + H + V + T, ignore_frac=0.1)
+    f, dX, dW = _run(inp, T)
+    _check(inp, T, f, dX, dW)
+
+
+def test_shard_count_invariance_bf16():
+    """Loss, dX and dW agree with the oracle for every T dividing V."""
+    inp = synth.small_case(384, 256, 2048, 1, "bf16", seed=3)
+    losses = []
+    for T in (1, 2, 4, 8, 16):
+        f, dX, dW = _run(inp, T)
+        _check(inp, T, f, dX, dW)
+        losses.append(np64(f["loss"]))
+    for l in losses[1:]:
+        np.testing.assert_allclose(l, losses[0], rtol=0, atol=1e-4)
+
+
+@pytest.mark.parametrize("chunk", [256, 768, 1536])
+def test_chunked_backward(chunk):
+    inp = synth.small_case(520, 192, 2000, 4, "bf16", seed=11)
+    f, dX, dW = _run(inp, 4, vocab_chunk=chunk)
+    _check(inp, 4, f, dX, dW)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ignore_index_in_range_and_bad_targets(dtype):
+    inp = synth.small_case(150, 64, 300, 3, dtype, seed=21)
+    y = inp.targets
+    y[:10] = 5                     # ignore_index inside [0, V)
+    y[10:14] = [300, 1000, -1, -7]  # out of range: ignored and counted
+    f, dX, dW = _run(inp, 3, ignore_index=5)
+    _check(inp, 3, f, dX, dW, ignore_index=5)
+    loss = np64(f["loss"])
+    assert np.all(loss[:14] == 0.0)
+    assert np.all(np64(dX)[:14] == 0.0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_all_ignored(dtype):
+    inp = synth.small_case(70, 64, 300, 3, dtype, seed=5)
+    inp.targets[:] = IGN
+    f, dX, dW = _run(inp, 3)
+    assert float(f["mean"].item()) == 0.0 and int(f["n_bad"].item()) == 0
+    assert np.all(np64(f["loss"]) == 0.0)
+    assert np.all(np64(dX) == 0.0) and np.all(np64(dW) == 0.0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_upstream_gradient_vector(dtype):
+    inp = synth.small_case(200, 128, 900, 3, dtype, seed=8)
+    dloss = np.random.default_rng(1).standard_normal(200)
+    f, dX, dW = _run(inp, 3, dloss=dloss)
+    _check(inp, 3, f, dX, dW, dloss=dloss)
+
+
+def test_minimind_config():
+    """Full MiniMind-scale workload (N=4096, H=512, V=6400, T=2, bf16) against
+    the dense float64 oracle, every token and every gradient entry."""
+    inp = synth.make_inputs("minimind")
+    f, dX, dW = _run(inp, inp.wl.T)
+    ex, ew = _check(inp, inp.wl.T, f, dX, dW)
+    print(f"minimind rel Frobenius dX {ex:.3e} dW {ew:.3e}")
+
+
+def test_autograd_wrapper():
+    inp = synth.small_case(96, 64, 512, 2, "bf16", seed=4)
+    X, W, y = dev_inputs(inp)
+    X.requires_grad_(True)
+    W.requires_grad_(True)
+    loss = vp.lmhead_ce(X, W, y, 2)
+    loss.backward()
+    b = ref.lmhead_ce_backward(inp.X, inp.W, inp.targets, inp.wl.V)
+    assert rel_fro(np64(X.grad), b["dX"]) <= 2e-2
+    assert rel_fro(np64(W.grad), b["dW"]) <= 2e-2
+    o = ref.lmhead_ce_forward(inp.X, inp.W, inp.targets, inp.wl.V, 2)
+    assert abs(loss.item() - o["mean"]) <= 2e-2 + 1e-2 * abs(o["mean"])
+
+
+def test_results_repeatable():
+    """Two calls on the same inputs give bit-identical results (no atomics in
+    any reduction)."""
+    inp = synth.small_case(300, 256, 1500, 3, "bf16", seed=2)
+    a = _run(inp, 3)
+    b = _run(inp, 3)
+    assert torch.equal(a[0]["loss"], b[0]["loss"]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])

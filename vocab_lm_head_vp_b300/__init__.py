@@ -1,0 +1,236 @@
+"""Python binding of libvp: vocab-parallel embedding and fused LM head +
+vocab-parallel cross-entropy on one B300.
+
+Argument marshalling only: every step of the path runs in libvp's CUDA
+kernels; torch tensors supply device memory and the current stream.  There is
+no fallback: without the built ``libvp.so`` every call raises.
+
+    out = embed_fwd(ids, W, T)
+    fwd = lmhead_ce_fwd(X, W, targets, T, ignore_index=-100)   # loss, lse, mean ...
+    dX, dW = lmhead_ce_bwd(X, W, targets, fwd["lse"], T)
+    loss = lmhead_ce(X, W, targets, T)                          # autograd wrapper
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["embed_fwd", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce", "workspace_size", "read_device_status",
+           "test_gemm_bf16", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
+
+VP_F32, VP_BF16 = 0, 1
+IGNORE_INDEX = -100
+_STATUS = {0: "VP_OK", 1: "VP_ERR_INVALID_ARG", 2: "VP_ERR_UNSUPPORTED", 3: "VP_ERR_WORKSPACE", 4: "VP_ERR_CUDA"}
+DEV_STATUS_BITS = {0x1: "producer wait timed out", 0x2: "MMA wait timed out", 0x4: "epilogue wait timed out"}
+
+_lib = None
+
+
+class VpError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {_STATUS.get(code, code)}")
+        self.code = code
+
+
+def library_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvp.so")
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libvp.so is not built ({path}); run `python -m vocab_lm_head_vp_b300.build`")
+    L = ctypes.CDLL(path)
+    P, I64, I32, SZ, U = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_int
+    L.vp_status_string.restype = ctypes.c_char_p
+    L.vp_status_string.argtypes = [I32]
+    L.vp_version.restype = ctypes.c_char_p
+    L.vp_embed_fwd.restype = I32
+    L.vp_embed_fwd.argtypes = [P, P, P, I64, I64, I64, I32, I32, P]
+    L.vp_lmhead_ce_workspace_size.restype = SZ
+    L.vp_lmhead_ce_workspace_size.argtypes = [I64, I64, I64, I32, I32, I32, I64]
+    L.vp_lmhead_ce_fwd.restype = I32
+    L.vp_lmhead_ce_fwd.argtypes = [P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, P, P, P, SZ, P]
+    L.vp_lmhead_ce_bwd.restype = I32
+    L.vp_lmhead_ce_bwd.argtypes = [P, P, P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, SZ, P]
+    L.vp_read_device_status.restype = I32
+    L.vp_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
+    L.vp_test_gemm_bf16.restype = I32
+    L.vp_test_gemm_bf16.argtypes = [P, P, P, I64, I64, I64, U, U, P, P]
+    _lib = L
+    return L
+
+
+def _check(fn, code):
+    if code != 0:
+        raise VpError(fn, code)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return VP_BF16
+    if t.dtype == torch.float32:
+        return VP_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or f32)")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def workspace_size(N, H, V, T, dtype, pass_, vocab_chunk=0) -> int:
+    code = dtype if isinstance(dtype, int) else (VP_BF16 if dtype == torch.bfloat16 else VP_F32)
+    return int(_load().vp_lmhead_ce_workspace_size(N, H, V, T, code, pass_, int(vocab_chunk or 0)))
+
+
+def _workspace(nbytes, device, workspace):
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+def embed_fwd(ids: torch.Tensor, W: torch.Tensor, T: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """out[n] = W[ids[n]] (zero row for ids outside [0, V)), gathered shard-wise."""
+    _need(W, "W")
+    _need(ids, "ids", torch.int64, W.device)
+    V, H = W.shape
+    N = ids.numel()
+    if out is None:
+        out = torch.empty((N, H), dtype=W.dtype, device=W.device)
+    _need(out, "out", W.dtype, W.device)
+    _check("vp_embed_fwd", _load().vp_embed_fwd(_ptr(ids), _ptr(W), _ptr(out), N, H, V, T, _dtype_code(W),
+                                                _stream(W.device)))
+    return out
+
+
+def lmhead_ce_fwd(X, W, targets, T, ignore_index=IGNORE_INDEX, shard_stats=False, workspace=None,
+                  out=None) -> dict:
+    """Fused LM head + vocab-parallel CE forward.  Returns loss [N], lse [N],
+    mean [1], n_bad [1] (int32) and, if asked, shard_stats [T,3,N]."""
+    _need(X, "X")
+    _need(W, "W", X.dtype, X.device)
+    _need(targets, "targets", torch.int64, X.device)
+    N, H = X.shape
+    V = W.shape[0]
+    dev = X.device
+    if out is None:
+        out = {"loss": torch.empty(N, dtype=torch.float32, device=dev),
+               "lse": torch.empty(N, dtype=torch.float32, device=dev),
+               "mean": torch.empty(1, dtype=torch.float32, device=dev),
+               "n_bad": torch.empty(1, dtype=torch.int32, device=dev)}
+        if shard_stats:
+            out["shard_stats"] = torch.empty((T, 3, N), dtype=torch.float32, device=dev)
+    ws_bytes = workspace_size(N, H, V, T, _dtype_code(X), 0)
+    if ws_bytes == 0:
+        raise VpError("vp_lmhead_ce_workspace_size", 1)
+    ws = _workspace(ws_bytes, dev, workspace)
+    code = _load().vp_lmhead_ce_fwd(
+        _ptr(X), _ptr(W), _ptr(targets), N, H, V, T, ignore_index, _dtype_code(X), _ptr(out["loss"]),
+        _ptr(out["lse"]), _ptr(out.get("mean")), _ptr(out.get("shard_stats")), _ptr(out.get("n_bad")),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(dev))
+    _check("vp_lmhead_ce_fwd", code)
+    out["workspace"] = ws
+    return out
+
+
+def lmhead_ce_bwd(X, W, targets, lse, T, ignore_index=IGNORE_INDEX, dloss=None, vocab_chunk=None,
+                  workspace=None, dX=None, dW=None):
+    """Backward of the mean loss (or of sum_n dloss[n] * loss[n]): (dX in X's
+    dtype, dW in fp32)."""
+    _need(X, "X")
+    _need(W, "W", X.dtype, X.device)
+    _need(targets, "targets", torch.int64, X.device)
+    _need(lse, "lse", torch.float32, X.device)
+    if dloss is not None:
+        _need(dloss, "dloss", torch.float32, X.device)
+    N, H = X.shape
+    V = W.shape[0]
+    dev = X.device
+    if dX is None:
+        dX = torch.empty_like(X)
+    if dW is None:
+        dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    _need(dX, "dX", X.dtype, dev)
+    _need(dW, "dW", torch.float32, dev)
+    ws_bytes = workspace_size(N, H, V, T, _dtype_code(X), 1, vocab_chunk or 0)
+    if ws_bytes == 0:
+        raise VpError("vp_lmhead_ce_workspace_size", 1)
+    ws = _workspace(ws_bytes, dev, workspace)
+    code = _load().vp_lmhead_ce_bwd(
+        _ptr(X), _ptr(W), _ptr(targets), _ptr(lse), _ptr(dloss), N, H, V, T, ignore_index, _dtype_code(X),
+        _ptr(dX), _ptr(dW), _ptr(ws), ws_bytes if workspace is None else ws.numel() * ws.element_size(),
+        _stream(dev))
+    _check("vp_lmhead_ce_bwd", code)
+    return dX, dW
+
+
+def read_device_status(workspace: torch.Tensor) -> int:
+    """Synchronise the current stream and return the workspace's device status
+    word (0 = no kernel gave up waiting)."""
+    flags = ctypes.c_uint32(0)
+    _check("vp_read_device_status", _load().vp_read_device_status(_ptr(workspace), ctypes.byref(flags),
+                                                                  _stream(workspace.device)))
+    return int(flags.value)
+
+
+def test_gemm_bf16(A, B, a_mn_major=False, b_mn_major=False):
+    """D = A * B^T (fp32) through the tcgen05 GEMM core.  A is [M,K] (or [K,M]
+    when a_mn_major), B is [N,K] (or [K,N] when b_mn_major)."""
+    _need(A, "A", torch.bfloat16)
+    _need(B, "B", torch.bfloat16, A.device)
+    M = A.shape[1] if a_mn_major else A.shape[0]
+    K = A.shape[0] if a_mn_major else A.shape[1]
+    N = B.shape[1] if b_mn_major else B.shape[0]
+    D = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    ws = torch.zeros(256, dtype=torch.uint8, device=A.device)
+    _check("vp_test_gemm_bf16", _load().vp_test_gemm_bf16(_ptr(A), _ptr(B), _ptr(D), M, N, K, int(a_mn_major),
+                                                          int(b_mn_major), _ptr(ws), _stream(A.device)))
+    return D, ws
+
+
+class _LMHeadCE(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, X, W, targets, T, ignore_index):
+        out = lmhead_ce_fwd(X, W, targets, T, ignore_index)
+        ctx.save_for_backward(X, W, targets, out["lse"])
+        ctx.T, ctx.ignore_index = T, ignore_index
+        return out["mean"][0]
+
+    @staticmethod
+    def backward(ctx, grad):
+        X, W, targets, lse = ctx.saved_tensors
+        # d(g * mean)/dl_n = g / N_valid: pass the per-token upstream gradient
+        valid = (targets >= 0) & (targets < W.shape[0]) & (targets != ctx.ignore_index)
+        dloss = (valid.float() * (grad.float() / valid.sum().clamp(min=1))).contiguous()
+        dX, dW = lmhead_ce_bwd(X, W, targets, lse, ctx.T, ctx.ignore_index, dloss=dloss)
+        return dX, dW.to(W.dtype), None, None, None
+
+
+def lmhead_ce(X, W, targets, T, ignore_index=IGNORE_INDEX):
+    """Mean cross-entropy of the tied LM head over valid tokens, differentiable
+    in X and W (autograd wrapper of lmhead_ce_fwd / lmhead_ce_bwd)."""
+    return _LMHeadCE.apply(X, W, targets, T, ignore_index)

@@ -1,0 +1,150 @@
+// Per-token merge of the forward statistics and the small per-batch kernels.
+//
+// lse_merge: the on-device form of the pages' cross-shard reductions ("Vocab
+// Parallelism" sec. 5.3.1; "Vocab parallelism: how to split embedding and LM
+// head", figure 2 and key formulas).  For token n, the per-tile records
+// (m, S) of shard t are merged into the shard's (m_t, S_t); the shards then
+// merge into m = max_t m_t, S = sum_t S_t e^(m_t - m), lse = m + log S, and
+// loss = lse - z_y for a valid target (0 otherwise).
+//
+// loss_mean_and_bad: L = sum_n loss_n / max(1, N_valid) (sec. 5.3.3) and the
+// count of targets that are neither ignore_index nor inside [0, V).
+//
+// upstream_scale: g_n = dloss_n (or 1/max(1, N_valid)) on valid tokens, 0 on
+// ignored ones -- the per-row factor of the logit gradient (sec. 5.3.2-5.3.3).
+#include <cuda_runtime.h>
+
+#include "vp_internal.h"
+
+namespace vp {
+namespace {
+
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
+  if (m2 > m) {
+    s = s * expf(m - m2) + s2;
+    m = m2;
+  } else {
+    s += s2 * expf(m2 - m);
+  }
+}
+
+__global__ void lse_merge_kernel(const float2* __restrict__ partial, const float* __restrict__ zy,
+                                 const int64_t* __restrict__ targets, int64_t N, int64_t V, int64_t Vs, int T,
+                                 int tile_v, int maxseg, int64_t ignore_index, float* __restrict__ loss,
+                                 float* __restrict__ lse, float* __restrict__ shard_stats) {
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  const int64_t y = targets[n];
+  const bool valid = y >= 0 && y < V && y != ignore_index;
+  const float zyn = valid ? zy[n] : 0.f;
+  float m = -INFINITY, s = 0.f;
+  for (int t = 0; t < T; ++t) {
+    const int64_t a = static_cast<int64_t>(t) * Vs;
+    const int64_t b = a + Vs;
+    float mt = -INFINITY, st = 0.f;
+    for (int64_t nb = a / tile_v; nb <= (b - 1) / tile_v; ++nb) {
+      const int k = t - static_cast<int>((nb * tile_v) / Vs);   // slot of shard t inside tile nb
+      const float2 r = partial[(nb * maxseg + k) * N + n];
+      merge_ms(mt, st, r.x, r.y);
+    }
+    if (shard_stats) {
+      shard_stats[(static_cast<int64_t>(t) * 3 + 0) * N + n] = mt;
+      shard_stats[(static_cast<int64_t>(t) * 3 + 1) * N + n] = st;
+      shard_stats[(static_cast<int64_t>(t) * 3 + 2) * N + n] = (valid && y >= a && y < b) ? zyn : 0.f;
+    }
+    merge_ms(m, s, mt, st);
+  }
+  const float l = m + logf(s);
+  lse[n] = l;
+  loss[n] = valid ? l - zyn : 0.f;
+}
+
+constexpr int kRedThreads = 1024;
+
+// One CTA: fixed-order (deterministic) sums over the batch.
+__global__ void __launch_bounds__(kRedThreads) loss_mean_kernel(const float* __restrict__ loss,
+                                                                const int64_t* __restrict__ targets, int64_t N,
+                                                                int64_t V, int64_t ignore_index,
+                                                                float* __restrict__ loss_mean,
+                                                                int32_t* __restrict__ n_bad) {
+  __shared__ double s_sum[kRedThreads];
+  __shared__ int s_valid[kRedThreads];
+  __shared__ int s_bad[kRedThreads];
+  double sum = 0.0;
+  int nv = 0, nbad = 0;
+  for (int64_t n = threadIdx.x; n < N; n += kRedThreads) {
+    const int64_t y = targets[n];
+    const bool valid = y >= 0 && y < V && y != ignore_index;
+    const bool in_range = y >= 0 && y < V;
+    sum += valid ? static_cast<double>(loss[n]) : 0.0;
+    nv += valid;
+    nbad += (!in_range && y != ignore_index);
+  }
+  s_sum[threadIdx.x] = sum;
+  s_valid[threadIdx.x] = nv;
+  s_bad[threadIdx.x] = nbad;
+  __syncthreads();
+  for (int w = kRedThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      s_sum[threadIdx.x] += s_sum[threadIdx.x + w];
+      s_valid[threadIdx.x] += s_valid[threadIdx.x + w];
+      s_bad[threadIdx.x] += s_bad[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const int denom = s_valid[0] > 1 ? s_valid[0] : 1;
+    if (loss_mean) *loss_mean = static_cast<float>(s_sum[0] / denom);
+    if (n_bad) *n_bad = s_bad[0];
+  }
+}
+
+__global__ void __launch_bounds__(kRedThreads) upstream_scale_kernel(const int64_t* __restrict__ targets,
+                                                                     const float* __restrict__ dloss, int64_t N,
+                                                                     int64_t V, int64_t ignore_index,
+                                                                     float* __restrict__ g) {
+  __shared__ int s_valid[kRedThreads];
+  int nv = 0;
+  for (int64_t n = threadIdx.x; n < N; n += kRedThreads) {
+    const int64_t y = targets[n];
+    nv += (y >= 0 && y < V && y != ignore_index);
+  }
+  s_valid[threadIdx.x] = nv;
+  __syncthreads();
+  for (int w = kRedThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) s_valid[threadIdx.x] += s_valid[threadIdx.x + w];
+    __syncthreads();
+  }
+  const float inv = 1.0f / static_cast<float>(s_valid[0] > 1 ? s_valid[0] : 1);
+  for (int64_t n = threadIdx.x; n < N; n += kRedThreads) {
+    const int64_t y = targets[n];
+    const bool valid = y >= 0 && y < V && y != ignore_index;
+    g[n] = valid ? (dloss ? dloss[n] : inv) : 0.f;
+  }
+}
+
+}  // namespace
+
+cudaError_t lse_merge(const float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
+                      int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
+                      float* shard_stats, cudaStream_t stream) {
+  const int threads = 256;
+  const int64_t blocks = (N + threads - 1) / threads;
+  lse_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(partial, zy, targets, N, V, Vs, T, tile_v,
+                                                                          maxseg, ignore_index, loss, lse, shard_stats);
+  return cudaGetLastError();
+}
+
+cudaError_t loss_mean_and_bad(const float* loss, const int64_t* targets, int64_t N, int64_t V, int64_t ignore_index,
+                              float* loss_mean, int32_t* n_bad, cudaStream_t stream) {
+  loss_mean_kernel<<<1, kRedThreads, 0, stream>>>(loss, targets, N, V, ignore_index, loss_mean, n_bad);
+  return cudaGetLastError();
+}
+
+cudaError_t upstream_scale(const int64_t* targets, const float* dloss, int64_t N, int64_t V, int64_t ignore_index,
+                           float* g, cudaStream_t stream) {
+  upstream_scale_kernel<<<1, kRedThreads, 0, stream>>>(targets, dloss, N, V, ignore_index, g);
+  return cudaGetLastError();
+}
+
+}  // namespace vp

@@ -1,0 +1,241 @@
+// Persistent tcgen05 GEMM core for sm_103a: D[128 x 256] tiles of A * B^T with
+// bf16 operands staged by TMA into 128-byte-swizzled shared memory and fp32
+// accumulators in tensor memory.  The epilogue is a template parameter, so
+// the same main loop serves the forward log-sum-exp statistics, the backward
+// logit-gradient recompute and the dX / dW contractions.
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 0      one lane issues TMA loads into a kStages-deep ring
+//   warp 1      allocates 512 TMEM columns; one lane issues tcgen05.mma
+//   warps 2..5  epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, i.e. one
+//               accumulator row (token / vocab row) per thread
+// Two 128x256 fp32 accumulators (2 x 256 TMEM columns) let the epilogue of
+// tile i overlap the MMAs of tile i+1.
+//
+// Operand layouts (A is M x K, B is N x K; "MN-major" = M (or N) contiguous):
+//   K-major : one TMA box {64 K, rows} per stage; swizzle atoms of 8 rows x
+//             128 B stacked along the rows (stride 1024 B); the k-th 16-wide
+//             slice starts 32 B further.
+//   MN-major: boxes {64 MN, 64 K}; each box is 64 K-rows of 128 B, i.e. 8
+//             swizzle atoms of 8 K-rows stacked along K (stride 1024 B);
+//             consecutive 64-wide MN blocks are 8 KB apart; the k-th
+//             16-deep slice starts 2 KB further.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include "ptx.cuh"
+
+namespace vp {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
+constexpr uint32_t kBBytes = kBN * kBK * 2;  // 32 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = 2 * kBN;
+constexpr uint32_t kMnBoxBytes = 64 * kBK * 2;  // one {64 MN, 64 K} box: 8 KB
+constexpr size_t kGemmSmemBytes = 1024 + kStages * kStageBytes + 256;
+
+struct TileSched {
+  int num_m, num_n, group_m;
+  // Tile id -> (m block, n block): ids run down groups of `group_m` m-blocks
+  // first so that CTAs working at the same time share operand tiles in L2.
+  __device__ __forceinline__ void tile(int id, int& mb, int& nb) const {
+    const int per_group = group_m * num_n;
+    const int g = id / per_group;
+    const int first_m = g * group_m;
+    const int gsz = min(num_m - first_m, group_m);
+    const int r = id - g * per_group;
+    mb = first_m + r % gsz;
+    nb = r / gsz;
+  }
+};
+
+struct GemmArgs {
+  TileSched sched;
+  int num_k;           // number of 64-wide K blocks
+  uint32_t* status;    // device status word (VP_DEV_* bits)
+};
+
+__device__ __forceinline__ void record_failure(uint32_t* status, volatile int* abort, uint32_t bit) {
+  *abort = 1;
+  if (status) atomicOr(status, bit);
+}
+
+template <bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmArgs args, const typename Epi::Params ep) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  uint8_t* sA = smem;                         // kStages x 16 KB
+  uint8_t* sB = smem + kStages * kABytes;     // kStages x 32 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = bars;                      // TMA -> MMA
+  uint64_t* empty = bars + kStages;           // MMA -> TMA
+  uint64_t* tfull = bars + 2 * kStages;       // MMA -> epilogue (2 accumulators)
+  uint64_t* tempty = tfull + 2;               // epilogue -> MMA
+  uint64_t* drain = tempty + 2;               // MMA completion at exit
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  __shared__ int never_abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4 * 32);
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    never_abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = args.sched.num_m * args.sched.num_n;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;   // bit s: stage s has a load in flight / its parity
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        int mb, nb;
+        args.sched.tile(tile, mb, nb);
+        bool ok = true;
+        for (int kb = 0; kb < args.num_k; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
+            record_failure(args.status, abort, 0x1u);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          uint8_t* a = sA + stage * kABytes;
+          uint8_t* b = sB + stage * kBBytes;
+          const int k0 = kb * kBK;
+          if (!A_MN) {
+            tma_load_2d(a, &tmA, &full[stage], k0, mb * kBM);
+          } else {
+            tma_load_2d(a, &tmA, &full[stage], mb * kBM, k0);
+            tma_load_2d(a + kMnBoxBytes, &tmA, &full[stage], mb * kBM + 64, k0);
+          }
+          if (!B_MN) {
+            tma_load_2d(b, &tmB, &full[stage], k0, nb * kBN);
+          } else {
+#pragma unroll
+            for (int i = 0; i < kBN / 64; ++i)
+              tma_load_2d(b + i * kMnBoxBytes, &tmB, &full[stage], nb * kBN + 64 * i, k0);
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      // Every load this thread issued must land before the CTA can exit.
+      for (int s = 0; s < kStages; ++s)
+        if (armed & (1u << s)) mbar_wait(&full[s], (armed_parity >> s) & 1u, &never_abort);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort)) {
+          record_failure(args.status, abort, 0x2u);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        bool ok = true;
+        for (int kb = 0; kb < args.num_k; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort)) {
+            record_failure(args.status, abort, 0x2u);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(sA + stage * kABytes);
+          const uint32_t b0 = smem_addr(sB + stage * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, kMnBoxBytes, 1024)
+                                     : sdesc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, kMnBoxBytes, 1024)
+                                     : sdesc_sw128(b0 + kk * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // All MMAs issued above must finish before TMEM is released.
+      umma_commit(drain);
+      mbar_wait(drain, 0, &never_abort);
+    }
+  } else {
+    // -------------------------------------------------- epilogue warps
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int mb, nb;
+      args.sched.tile(tile, mb, nb);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort));
+      if (!ok) {
+        if (lane == 0) record_failure(args.status, abort, 0x4u);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * kBN) + (static_cast<uint32_t>(quad * 32) << 16);
+      Epi::run(ep, taddr, static_cast<int64_t>(mb) * kBM + row, mb, nb);
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace vp

@@ -1,0 +1,245 @@
+// libvp C ABI: argument validation, workspace layout and kernel dispatch for
+// the vocab-parallel embedding and the fused LM head + cross-entropy.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/vp.h"
+#include "../../include/vp_testing.h"
+#include "vp_internal.h"
+
+#define VP_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace vp {
+
+EncodeTiledFn tensor_map_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kHeader = 256;  // device status word + reserved
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int esize_of(vp_dtype dt) { return dt == VP_BF16 ? 2 : 4; }
+bool dtype_ok(int dt) { return dt == VP_F32 || dt == VP_BF16; }
+
+bool shape_ok(int64_t N, int64_t H, int64_t V, int T) {
+  return N > 0 && H > 0 && V > 0 && T > 0 && V % T == 0 && N < (int64_t(1) << 31) && V < (int64_t(1) << 31) &&
+         H < (int64_t(1) << 31);
+}
+
+// ---------------- forward workspace: header | partial records | z_y
+struct FwdLayout {
+  int tile_v, maxseg;
+  int64_t ntiles;
+  size_t off_partial, off_zy, total;
+};
+FwdLayout fwd_layout(int64_t N, int64_t V, int T, vp_dtype dt) {
+  FwdLayout L;
+  const int64_t Vs = V / T;
+  L.tile_v = dt == VP_BF16 ? kBf16TileV : kF32TileV;
+  L.maxseg = dt == VP_BF16 ? lse_maxseg(V, Vs, T) : f32_maxseg(V, Vs, T);
+  L.ntiles = (V + L.tile_v - 1) / L.tile_v;
+  L.off_partial = kHeader;
+  L.off_zy = align_up(L.off_partial + size_t(L.ntiles) * L.maxseg * N * sizeof(float2), kAlign);
+  L.total = align_up(L.off_zy + size_t(N) * sizeof(float), kAlign);
+  return L;
+}
+
+// ---------------- backward workspace: header | g | dZ chunk | dX fp32 partial (bf16, >1 chunk)
+struct BwdLayout {
+  int64_t Vc, ldz;
+  size_t off_g, off_dz, off_acc, total;
+};
+int bwd_tile(vp_dtype dt) { return dt == VP_BF16 ? kBf16TileV : kF32TileV; }
+BwdLayout bwd_layout_for_chunk(int64_t N, int64_t H, int64_t V, vp_dtype dt, int64_t Vc) {
+  BwdLayout L;
+  L.Vc = Vc;
+  L.ldz = (Vc + 7) / 8 * 8;
+  L.off_g = kHeader;
+  L.off_dz = align_up(L.off_g + size_t(N) * sizeof(float), kAlign);
+  L.off_acc = align_up(L.off_dz + size_t(N) * L.ldz * esize_of(dt), kAlign);
+  const bool need_acc = dt == VP_BF16 && Vc < V;
+  L.total = align_up(L.off_acc + (need_acc ? size_t(N) * H * sizeof(float) : 0), kAlign);
+  return L;
+}
+// Largest chunk that fits in ws bytes (0 if none does).
+int64_t bwd_chunk_from_ws(int64_t N, int64_t H, int64_t V, vp_dtype dt, size_t ws) {
+  if (bwd_layout_for_chunk(N, H, V, dt, V).total <= ws) return V;
+  const int64_t tile = bwd_tile(dt);
+  const size_t fixed = bwd_layout_for_chunk(N, H, V, dt, tile).total - size_t(N) * tile * esize_of(dt);
+  if (ws < fixed) return 0;
+  int64_t vc = int64_t((ws - fixed) / (size_t(N) * esize_of(dt))) / tile * tile;
+  while (vc >= tile && bwd_layout_for_chunk(N, H, V, dt, vc).total > ws) vc -= tile;
+  if (vc >= V) vc = V;
+  return vc >= tile || vc == V ? vc : 0;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+}  // namespace vp
+
+using namespace vp;
+
+VP_EXPORT const char* vp_status_string(vp_status s) {
+  switch (s) {
+    case VP_OK: return "VP_OK";
+    case VP_ERR_INVALID_ARG: return "VP_ERR_INVALID_ARG";
+    case VP_ERR_UNSUPPORTED: return "VP_ERR_UNSUPPORTED";
+    case VP_ERR_WORKSPACE: return "VP_ERR_WORKSPACE";
+    case VP_ERR_CUDA: return "VP_ERR_CUDA";
+  }
+  return "VP_ERR_UNKNOWN";
+}
+
+VP_EXPORT const char* vp_version(void) { return "libvp 0.1 sm_103a"; }
+
+VP_EXPORT vp_status vp_embed_fwd(const int64_t* ids, const void* W, void* out, int64_t N, int64_t H, int64_t V, int T,
+                                 vp_dtype dtype, void* stream) {
+  if (!ids || !W || !out || !dtype_ok(dtype) || !shape_ok(N, H, V, T)) return VP_ERR_INVALID_ARG;
+  const int es = esize_of(dtype);
+  if (!aligned16(W) || !aligned16(out) || (H * es) % 16 != 0) return VP_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(ids) & 7u) != 0) return VP_ERR_UNSUPPORTED;
+  cudaError_t e = embed_gather(ids, W, out, N, H, V, V / T, T, es, as_stream(stream));
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+VP_EXPORT size_t vp_lmhead_ce_workspace_size(int64_t N, int64_t H, int64_t V, int T, vp_dtype dtype, int pass,
+                                             int64_t vocab_chunk) {
+  if (!dtype_ok(dtype) || !shape_ok(N, H, V, T)) return 0;
+  if (pass == 0) return fwd_layout(N, V, T, dtype).total;
+  if (pass != 1) return 0;
+  int64_t vc = V;
+  if (vocab_chunk > 0 && vocab_chunk < V) {
+    const int64_t tile = bwd_tile(dtype);
+    vc = vocab_chunk / tile * tile;
+    if (vc < tile) vc = tile;
+    if (vc > V) vc = V;
+  }
+  return bwd_layout_for_chunk(N, H, V, dtype, vc).total;
+}
+
+static vp_status check_common(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H, int64_t V,
+                              int T, vp_dtype dtype, const void* ws) {
+  if (!X || !W || !targets || !ws || !dtype_ok(dtype) || !shape_ok(N, H, V, T)) return VP_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(ws) || (H * esize_of(dtype)) % 16 != 0) return VP_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(targets) & 7u) != 0) return VP_ERR_UNSUPPORTED;
+  if (dtype == VP_BF16 && !tensor_map_encoder()) return VP_ERR_CUDA;
+  return VP_OK;
+}
+
+VP_EXPORT vp_status vp_lmhead_ce_fwd(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H,
+                                     int64_t V, int T, int64_t ignore_index, vp_dtype dtype, float* loss, float* lse,
+                                     float* loss_mean, float* shard_stats, int32_t* n_bad, void* workspace,
+                                     size_t ws_bytes, void* stream) {
+  if (!loss || !lse) return VP_ERR_INVALID_ARG;
+  vp_status st = check_common(X, W, targets, N, H, V, T, dtype, workspace);
+  if (st != VP_OK) return st;
+  const FwdLayout L = fwd_layout(N, V, T, dtype);
+  if (ws_bytes < L.total) return VP_ERR_WORKSPACE;
+  cudaStream_t s = as_stream(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  float2* partial = reinterpret_cast<float2*>(ws + L.off_partial);
+  float* zy = reinterpret_cast<float*>(ws + L.off_zy);
+  const int64_t Vs = V / T;
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) {
+    if (dtype == VP_BF16)
+      e = bf16_lse_stats(X, W, targets, N, H, V, Vs, partial, L.maxseg, zy, status, s);
+    else
+      e = f32_lse_stats(static_cast<const float*>(X), static_cast<const float*>(W), targets, N, H, V, Vs, partial,
+                        L.maxseg, zy, s);
+  }
+  if (e == cudaSuccess)
+    e = lse_merge(partial, zy, targets, N, V, Vs, T, L.tile_v, L.maxseg, ignore_index, loss, lse, shard_stats, s);
+  if (e == cudaSuccess && (loss_mean || n_bad)) e = loss_mean_and_bad(loss, targets, N, V, ignore_index, loss_mean, n_bad, s);
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+VP_EXPORT vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t* targets, const float* lse,
+                                     const float* dloss, int64_t N, int64_t H, int64_t V, int T,
+                                     int64_t ignore_index, vp_dtype dtype, void* dX, float* dW, void* workspace,
+                                     size_t ws_bytes, void* stream) {
+  if (!lse || !dX || !dW) return VP_ERR_INVALID_ARG;
+  vp_status st = check_common(X, W, targets, N, H, V, T, dtype, workspace);
+  if (st != VP_OK) return st;
+  if (!aligned16(dX) || !aligned16(dW)) return VP_ERR_UNSUPPORTED;
+  const int64_t Vc = bwd_chunk_from_ws(N, H, V, dtype, ws_bytes);
+  if (Vc <= 0) return VP_ERR_WORKSPACE;
+  const BwdLayout L = bwd_layout_for_chunk(N, H, V, dtype, Vc);
+  cudaStream_t s = as_stream(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  float* g = reinterpret_cast<float*>(ws + L.off_g);
+  void* dz = ws + L.off_dz;
+  float* acc = reinterpret_cast<float*>(ws + L.off_acc);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = upstream_scale(targets, dloss, N, V, ignore_index, g, s);
+  const bool single = Vc >= V;
+  for (int64_t c0 = 0; c0 < V && e == cudaSuccess; c0 += Vc) {
+    const int64_t vc = (V - c0) < Vc ? (V - c0) : Vc;
+    const bool first = c0 == 0, last = c0 + vc >= V;
+    if (dtype == VP_BF16) {
+      e = bf16_dz_chunk(X, W, targets, lse, g, N, H, c0, vc, dz, L.ldz, status, s);
+      if (e == cudaSuccess) e = bf16_dw_chunk(dz, L.ldz, X, N, H, c0, vc, dW, status, s);
+      if (e == cudaSuccess) {
+        if (single)
+          e = bf16_dx_chunk(dz, L.ldz, W, N, H, c0, vc, dX, nullptr, 3 /*bf16 store*/, status, s);
+        else if (first)
+          e = bf16_dx_chunk(dz, L.ldz, W, N, H, c0, vc, acc, nullptr, 0 /*f32 store*/, status, s);
+        else if (!last)
+          e = bf16_dx_chunk(dz, L.ldz, W, N, H, c0, vc, acc, nullptr, 1 /*f32 add*/, status, s);
+        else
+          e = bf16_dx_chunk(dz, L.ldz, W, N, H, c0, vc, dX, acc, 2 /*bf16 = partial + acc*/, status, s);
+      }
+    } else {
+      const float* Xf = static_cast<const float*>(X);
+      const float* Wf = static_cast<const float*>(W);
+      float* dzf = static_cast<float*>(dz);
+      e = f32_dz_chunk(Xf, Wf, targets, lse, g, N, H, c0, vc, dzf, L.ldz, s);
+      // dW[c0+v, h] = sum_n dZ[n, v] X[n, h]
+      if (e == cudaSuccess) e = f32_gemm(dzf, 1, L.ldz, Xf, H, 1, dW + c0 * H, H, vc, H, N, false, s);
+      // dX[n, h] (+)= sum_v dZ[n, v] W[c0+v, h]
+      if (e == cudaSuccess)
+        e = f32_gemm(dzf, L.ldz, 1, Wf + c0 * H, H, 1, static_cast<float*>(dX), H, N, H, vc, !first, s);
+    }
+  }
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+VP_EXPORT vp_status vp_read_device_status(const void* workspace, uint32_t* flags, void* stream) {
+  if (!workspace || !flags) return VP_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  if (e == cudaSuccess) e = cudaMemcpy(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+VP_EXPORT vp_status vp_test_gemm_bf16(const void* A, const void* B, float* D, int64_t M, int64_t N, int64_t K,
+                                      int a_mn_major, int b_mn_major, void* workspace, void* stream) {
+  if (!A || !B || !D || !workspace || M <= 0 || N <= 0 || K <= 0) return VP_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned16(workspace)) return VP_ERR_UNSUPPORTED;
+  if ((a_mn_major ? M : K) % 8 != 0 || (b_mn_major ? N : K) % 8 != 0 || N % 4 != 0) return VP_ERR_UNSUPPORTED;
+  if (!tensor_map_encoder()) return VP_ERR_CUDA;
+  cudaStream_t s = as_stream(stream);
+  uint32_t* status = static_cast<uint32_t*>(workspace);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = bf16_gemm_test(A, B, D, M, N, K, a_mn_major, b_mn_major, status, s);
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
