@@ -1,0 +1,343 @@
+#!/usr/bin/env python
+"""Benchmark: one step = the whole hot path of the vocab-parallel LM head on
+one batch -- embedding gather of the batch's ids, fused LM head + CE forward,
+and its backward (dX, dW) -- on seeded synthetic inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload v128k] [--no-cpu-baseline]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs the same
+step on its own seeded batch (weak scaling, no collective on the data path;
+the only collectives are the timing barrier and the max over ranks).
+
+``--impl reference`` times the float64 CPU oracle on the host cores on a
+bounded sample of the same workload (the baseline these pages give no faster
+implementation of); only rank 0 runs it.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused LM-head+CE fwd+bwd tokens/s and % of bf16 tensor peak at V=128256"
+UNIT = "tokens/s"
+GEMM_STAGES = ("lse_stats_gemm", "dz_recompute_gemm", "dw_gemm", "dx_gemm")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=40)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="v128k")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU work budget of the oracle baseline")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd[1:1] = ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        sm, smax, power, reasons = [], [], [], set()
+        for line in self.out.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, v in zip(self.REASONS, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.out.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+# ------------------------------------------------------------------ oracle timing (host cores)
+def oracle_tokens_per_s(inp, budget_s):
+    """Time the float64 oracle (fwd + bwd, exactly as it stands) on a leading
+    sample of the batch's tokens sized to about budget_s seconds."""
+    import oracle.ref as ref
+    wl = inp.wl
+    W64 = np.asarray(inp.W, dtype=np.float64)   # input preparation, not timed
+    X64 = np.asarray(inp.X, dtype=np.float64)
+
+    def run(n):
+        t0 = time.perf_counter()
+        ref.lmhead_ce_backward(X64[:n], W64, inp.targets[:n], wl.V)
+        return time.perf_counter() - t0
+
+    n = 2
+    t = run(n)
+    while t < budget_s / 8 and n < wl.N:
+        n = min(wl.N, n * 4)
+        t = run(n)
+    if t < budget_s / 2 and n < wl.N:
+        n = min(wl.N, max(n + 1, int(n * budget_s / max(t, 1e-3) * 0.7)))
+        t = run(n)
+    return n / t, n, t
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    import synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(wl)
+    # each step: the oracle on a bounded sample sized so that the run ends in a few minutes
+    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    _, n, _ = oracle_tokens_per_s(inp, per_step)
+    import oracle.ref as ref
+    W64 = np.asarray(inp.W, dtype=np.float64)
+    X64 = np.asarray(inp.X[:n], dtype=np.float64)
+    for _ in range(args.warmup):
+        ref.lmhead_ce_backward(X64, W64, inp.targets[:n], wl.V)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ref.lmhead_ce_backward(X64, W64, inp.targets[:n], wl.V)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    sample = f"first {n} of {wl.N} tokens per step, full H={wl.H} and V={wl.V}, float64 NumPy fwd+bwd"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores_used(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
+def workload_config(wl):
+    return {"workload": f"{wl.name}: N={wl.N} H={wl.H} V={wl.V} T={wl.T} {wl.dtype}, targets {wl.targets}"
+                        + (f", {int(wl.ignore_frac * 100)}% ignore_index" if wl.ignore_frac else ""),
+            "N": wl.N, "H": wl.H, "V": wl.V, "T": wl.T, "dtype": wl.dtype,
+            "l2": ("no flush: inputs larger than L2 (W %.2f GB, X %.0f MB; L2 126 MB)" if wl.V * wl.H * 2 > 126e6
+                   else "inputs fit in L2 (W %.2f GB, X %.0f MB); no flush") % (wl.V * wl.H * 2 / 1e9,
+                                                                                 wl.N * wl.H * 2 / 1e6)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    import vocab_lm_head_vp_b300 as vp
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    wl = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(wl, seed=wl.seed + rank)
+    N, H, V, T = wl.N, wl.H, wl.V, wl.T
+    to = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    X = to(inp.X_bits).to(dev)
+    W = to(inp.W_bits).to(dev)
+    y = torch.from_numpy(inp.targets).to(dev)
+    emb = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+    fo = {"loss": torch.empty(N, dtype=torch.float32, device=dev),
+          "lse": torch.empty(N, dtype=torch.float32, device=dev),
+          "mean": torch.empty(1, dtype=torch.float32, device=dev),
+          "n_bad": torch.empty(1, dtype=torch.int32, device=dev)}
+    dX = torch.empty_like(X)
+    dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    wsf = torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 0), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 1), dtype=torch.uint8, device=dev)
+
+    def step(Xs, ys):
+        vp.embed_fwd(ys, W, T, out=emb)
+        vp.lmhead_ce_fwd(Xs, W, ys, T, workspace=wsf, out=fo)
+        vp.lmhead_ce_bwd(Xs, W, ys, fo["lse"], T, workspace=wsb, dX=dX, dW=dW)
+
+    for _ in range(args.warmup):
+        step(X, y)
+    torch.cuda.synchronize()
+    assert vp.read_device_status(wsf) == 0 and vp.read_device_status(wsb) == 0
+
+    # ---------------- timed region
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else None)
+    vp.stage_timing_enable(16 * args.steps + 64)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        step(X, y)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    stages = vp.stage_timing_read()
+    vp.stage_timing_enable(0)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---------------- end to end through host buffers (X, targets in; loss out)
+    Xh = to(inp.X_bits).pin_memory()
+    yh = torch.from_numpy(inp.targets).pin_memory()
+    loss_h = torch.empty(N, dtype=torch.float32).pin_memory()
+    mean_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    Xd, yd = torch.empty_like(X), torch.empty_like(y)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        Xd.copy_(Xh, non_blocking=True)
+        yd.copy_(yh, non_blocking=True)
+        step(Xd, yd)
+        loss_h.copy_(fo["loss"], non_blocking=True)
+        mean_h.copy_(fo["mean"], non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = Xh.numel() * 2 + yh.numel() * 8
+    d2h = loss_h.numel() * 4 + 4
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks = load_peaks()
+    sec = ms / 1e3
+    value = world * N * args.steps / sec
+    alg = 6.0 * N * H * V          # fwd 2NHV + dX 2NHV + dW 2NHV
+    exe = 8.0 * N * H * V          # + the logit recompute in the backward
+    gemm_ms = sum(stages[s][0] for s in GEMM_STAGES)
+    gemm_n = sum(stages[s][1] for s in GEMM_STAGES)
+    per_launch_flops = 2.0 * N * H * V          # every GEMM launch: one vocab chunk = all of V
+    avg_launch_s = gemm_ms / max(1, gemm_n) / 1e3
+    achieved = per_launch_flops / avg_launch_s / 1e12
+    emb_ms, emb_n = stages["embed_gather"]
+    emb_bytes = 2.0 * N * H * 2 + 8.0 * N
+    emb_gbs = emb_bytes / (emb_ms / max(1, emb_n) / 1e3) / 1e9
+    launches = sum(c for _, c in stages.values())
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) X, N(0,0.02^2) W, Zipf targets)",
+        "config": dict(workload_config(wl), parallelism=f"replicas x{world}, no data-path collective",
+                       vocab_chunks=1),
+        "tflops_algorithmic": alg * args.steps / sec / 1e12,
+        "tflops_executed": exe * args.steps / sec / 1e12,
+        "pct_bf16_peak_algorithmic": 100.0 * alg * args.steps / sec / 1e12 / peaks["bf16_tflops"],
+        "pct_bf16_peak_executed": 100.0 * exe * args.steps / sec / 1e12 / peaks["bf16_tflops"],
+        "roofline": {"kernel": "umma_gemm_kernel (tcgen05; 4 launches/step: lse stats, dZ recompute, dW, dX)",
+                     "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops_sustained"],
+                     "peak_kind": f"bf16 sustained ({peaks['source']})",
+                     "frac_of_burst": achieved / peaks["bf16_tflops"], "traffic": None},
+        "roofline_embed": {"kernel": "embed_gather_kernel", "bound": "hbm", "achieved": emb_gbs,
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": emb_gbs / peaks["hbm_gbs"],
+                           "note": "Zipf ids repeat rows (L2 hits)"},
+        "stages_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in stages.items() if v[1]},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": {"value": world * N * args.e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "note": "X and targets copied from pinned host memory and loss read back every step; "
+                        "the weight W is model state resident in HBM"},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        v, n, t = oracle_tokens_per_s(inp, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                                  "sample": f"first {n} of {N} tokens, full H and V, float64 NumPy fwd+bwd, "
+                                            f"{t:.1f} s"}
+    print(json.dumps(result))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -29,6 +29,25 @@ extern "C" {
 vp_status vp_test_gemm_bf16(const void* A, const void* B, float* D, int64_t M, int64_t N, int64_t K,
                             int a_mn_major, int b_mn_major, void* workspace, void* stream);
 
+/*
+ * Stage timing for measurement harnesses.  While enabled, every libvp call
+ * records a CUDA event on its stream before and after each kernel it
+ * launches, so a harness can attribute device time to kernels inside its
+ * own timed region.  Process-global, not thread-safe; meant for one
+ * benchmarking thread.
+ *
+ * vp_stage_timing_enable(max_launches): max_launches > 0 creates the events
+ *   (2 per launch) and starts recording from empty; 0 stops and frees them.
+ *   Launches beyond max_launches are not recorded (see the count returned).
+ * vp_stage_timing_read(ms, counts, n): waits for the recorded events and
+ *   writes, for stage s < n, the summed milliseconds and the number of
+ *   launches; returns the number of stages, or -1 on a CUDA error.
+ * vp_stage_name(s): the stage's name (static storage), NULL past the end.
+ */
+vp_status vp_stage_timing_enable(int max_launches);
+int vp_stage_timing_read(float* ms, int32_t* counts, int n);
+const char* vp_stage_name(int stage);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,7 +18,7 @@ import os
 import torch
 
 __all__ = ["embed_fwd", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce", "workspace_size", "read_device_status",
-           "test_gemm_bf16", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
+           "test_gemm_bf16", "stage_timing_enable", "stage_timing_read", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
 
 VP_F32, VP_BF16 = 0, 1
 IGNORE_INDEX = -100
@@ -62,6 +62,12 @@ def _load():
     L.vp_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     L.vp_test_gemm_bf16.restype = I32
     L.vp_test_gemm_bf16.argtypes = [P, P, P, I64, I64, I64, U, U, P, P]
+    L.vp_stage_timing_enable.restype = I32
+    L.vp_stage_timing_enable.argtypes = [I32]
+    L.vp_stage_timing_read.restype = I32
+    L.vp_stage_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32), I32]
+    L.vp_stage_name.restype = ctypes.c_char_p
+    L.vp_stage_name.argtypes = [I32]
     _lib = L
     return L
 
@@ -210,6 +216,23 @@ def test_gemm_bf16(A, B, a_mn_major=False, b_mn_major=False):
     _check("vp_test_gemm_bf16", _load().vp_test_gemm_bf16(_ptr(A), _ptr(B), _ptr(D), M, N, K, int(a_mn_major),
                                                           int(b_mn_major), _ptr(ws), _stream(A.device)))
     return D, ws
+
+
+def stage_timing_enable(max_launches: int) -> None:
+    """Record CUDA events around every kernel libvp launches (0 = stop)."""
+    _check("vp_stage_timing_enable", _load().vp_stage_timing_enable(int(max_launches)))
+
+
+def stage_timing_read() -> dict:
+    """{stage name: (milliseconds, launches)} accumulated since enabling."""
+    L = _load()
+    n = 16
+    ms = (ctypes.c_float * n)()
+    cnt = (ctypes.c_int32 * n)()
+    k = L.vp_stage_timing_read(ms, cnt, n)
+    if k < 0:
+        raise VpError("vp_stage_timing_read", 4)
+    return {L.vp_stage_name(i).decode(): (float(ms[i]), int(cnt[i])) for i in range(k)}
 
 
 class _LMHeadCE(torch.autograd.Function):

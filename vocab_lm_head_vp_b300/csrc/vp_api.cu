@@ -92,6 +92,29 @@ int64_t bwd_chunk_from_ws(int64_t N, int64_t H, int64_t V, vp_dtype dt, size_t w
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+// ---------------- optional per-launch event timing (vp_stage_timing_enable)
+enum Stage { kEmbed, kLseGemm, kMerge, kMean, kScale, kDzGemm, kDwGemm, kDxGemm, kNumStages };
+const char* const kStageNames[kNumStages] = {"embed_gather", "lse_stats_gemm", "lse_merge",  "loss_mean",
+                                             "upstream_scale", "dz_recompute_gemm", "dw_gemm", "dx_gemm"};
+struct StageTimer {
+  int cap = 0, used = 0;
+  cudaEvent_t* ev = nullptr;  // 2 per launch
+  int* stage = nullptr;
+} g_timer;
+
+template <class F>
+cudaError_t timed(Stage st, cudaStream_t s, F&& launch) {
+  int slot = -1;
+  if (g_timer.cap > 0 && g_timer.used < g_timer.cap) {
+    slot = g_timer.used++;
+    g_timer.stage[slot] = st;
+    cudaEventRecord(g_timer.ev[2 * slot], s);
+  }
+  cudaError_t e = launch();
+  if (slot >= 0) cudaEventRecord(g_timer.ev[2 * slot + 1], s);
+  return e;
+}
+
 }  // namespace
 }  // namespace vp
 
@@ -116,7 +139,8 @@ VP_EXPORT vp_status vp_embed_fwd(const int64_t* ids, const void* W, void* out, i
   const int es = esize_of(dtype);
   if (!aligned16(W) || !aligned16(out) || (H * es) % 16 != 0) return VP_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(ids) & 7u) != 0) return VP_ERR_UNSUPPORTED;
-  cudaError_t e = embed_gather(ids, W, out, N, H, V, V / T, T, es, as_stream(stream));
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e = timed(kEmbed, s, [&] { return embed_gather(ids, W, out, N, H, V, V / T, T, es, s); });
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
 }
 
@@ -161,15 +185,19 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd(const void* X, const void* W, const int64_t
   const int64_t Vs = V / T;
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess) {
-    if (dtype == VP_BF16)
-      e = bf16_lse_stats(X, W, targets, N, H, V, Vs, partial, L.maxseg, zy, status, s);
-    else
-      e = f32_lse_stats(static_cast<const float*>(X), static_cast<const float*>(W), targets, N, H, V, Vs, partial,
-                        L.maxseg, zy, s);
+    e = timed(kLseGemm, s, [&] {
+      if (dtype == VP_BF16) return bf16_lse_stats(X, W, targets, N, H, V, Vs, partial, L.maxseg, zy, status, s);
+      return f32_lse_stats(static_cast<const float*>(X), static_cast<const float*>(W), targets, N, H, V, Vs,
+                           partial, L.maxseg, zy, s);
+    });
   }
   if (e == cudaSuccess)
-    e = lse_merge(partial, zy, targets, N, V, Vs, T, L.tile_v, L.maxseg, ignore_index, loss, lse, shard_stats, s);
-  if (e == cudaSuccess && (loss_mean || n_bad)) e = loss_mean_and_bad(loss, targets, N, V, ignore_index, loss_mean, n_bad, s);
+    e = timed(kMerge, s, [&] {
+      return lse_merge(partial, zy, targets, N, V, Vs, T, L.tile_v, L.maxseg, ignore_index, loss, lse, shard_stats,
+                       s);
+    });
+  if (e == cudaSuccess && (loss_mean || n_bad))
+    e = timed(kMean, s, [&] { return loss_mean_and_bad(loss, targets, N, V, ignore_index, loss_mean, n_bad, s); });
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
 }
 
@@ -191,34 +219,36 @@ VP_EXPORT vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t
   void* dz = ws + L.off_dz;
   float* acc = reinterpret_cast<float*>(ws + L.off_acc);
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
-  if (e == cudaSuccess) e = upstream_scale(targets, dloss, N, V, ignore_index, g, s);
+  if (e == cudaSuccess) e = timed(kScale, s, [&] { return upstream_scale(targets, dloss, N, V, ignore_index, g, s); });
   const bool single = Vc >= V;
   for (int64_t c0 = 0; c0 < V && e == cudaSuccess; c0 += Vc) {
     const int64_t vc = (V - c0) < Vc ? (V - c0) : Vc;
     const bool first = c0 == 0, last = c0 + vc >= V;
     if (dtype == VP_BF16) {
-      e = bf16_dz_chunk(X, W, targets, lse, g, N, H, c0, vc, dz, L.ldz, status, s);
-      if (e == cudaSuccess) e = bf16_dw_chunk(dz, L.ldz, X, N, H, c0, vc, dW, status, s);
+      e = timed(kDzGemm, s, [&] { return bf16_dz_chunk(X, W, targets, lse, g, N, H, c0, vc, dz, L.ldz, status, s); });
+      if (e == cudaSuccess)
+        e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(dz, L.ldz, X, N, H, c0, vc, dW, status, s); });
       if (e == cudaSuccess) {
-        if (single)
-          e = bf16_dx_chunk(dz, L.ldz, W, N, H, c0, vc, dX, nullptr, 3 /*bf16 store*/, status, s);
-        else if (first)
-          e = bf16_dx_chunk(dz, L.ldz, W, N, H, c0, vc, acc, nullptr, 0 /*f32 store*/, status, s);
-        else if (!last)
-          e = bf16_dx_chunk(dz, L.ldz, W, N, H, c0, vc, acc, nullptr, 1 /*f32 add*/, status, s);
-        else
-          e = bf16_dx_chunk(dz, L.ldz, W, N, H, c0, vc, dX, acc, 2 /*bf16 = partial + acc*/, status, s);
+        // dX over chunks: bf16 store (one chunk), else fp32 store / fp32 add / bf16 = fp32 partial + last
+        void* out = (single || last) ? dX : static_cast<void*>(acc);
+        const int mode = single ? 3 : first ? 0 : !last ? 1 : 2;
+        e = timed(kDxGemm, s, [&] {
+          return bf16_dx_chunk(dz, L.ldz, W, N, H, c0, vc, out, mode == 2 ? acc : nullptr, mode, status, s);
+        });
       }
     } else {
       const float* Xf = static_cast<const float*>(X);
       const float* Wf = static_cast<const float*>(W);
       float* dzf = static_cast<float*>(dz);
-      e = f32_dz_chunk(Xf, Wf, targets, lse, g, N, H, c0, vc, dzf, L.ldz, s);
+      e = timed(kDzGemm, s, [&] { return f32_dz_chunk(Xf, Wf, targets, lse, g, N, H, c0, vc, dzf, L.ldz, s); });
       // dW[c0+v, h] = sum_n dZ[n, v] X[n, h]
-      if (e == cudaSuccess) e = f32_gemm(dzf, 1, L.ldz, Xf, H, 1, dW + c0 * H, H, vc, H, N, false, s);
+      if (e == cudaSuccess)
+        e = timed(kDwGemm, s, [&] { return f32_gemm(dzf, 1, L.ldz, Xf, H, 1, dW + c0 * H, H, vc, H, N, false, s); });
       // dX[n, h] (+)= sum_v dZ[n, v] W[c0+v, h]
       if (e == cudaSuccess)
-        e = f32_gemm(dzf, L.ldz, 1, Wf + c0 * H, H, 1, static_cast<float*>(dX), H, N, H, vc, !first, s);
+        e = timed(kDxGemm, s, [&] {
+          return f32_gemm(dzf, L.ldz, 1, Wf + c0 * H, H, 1, static_cast<float*>(dX), H, N, H, vc, !first, s);
+        });
     }
   }
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
@@ -242,4 +272,55 @@ VP_EXPORT vp_status vp_test_gemm_bf16(const void* A, const void* B, float* D, in
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess) e = bf16_gemm_test(A, B, D, M, N, K, a_mn_major, b_mn_major, status, s);
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+VP_EXPORT vp_status vp_stage_timing_enable(int max_launches) {
+  StageTimer& t = g_timer;
+  if (t.ev) {
+    for (int i = 0; i < 2 * t.cap; ++i) cudaEventDestroy(t.ev[i]);
+    delete[] t.ev;
+    delete[] t.stage;
+    t.ev = nullptr;
+    t.stage = nullptr;
+  }
+  t.cap = 0;
+  t.used = 0;
+  if (max_launches <= 0) return VP_OK;
+  t.ev = new cudaEvent_t[2 * max_launches];
+  t.stage = new int[max_launches];
+  for (int i = 0; i < 2 * max_launches; ++i) {
+    if (cudaEventCreate(&t.ev[i]) != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(t.ev[j]);
+      delete[] t.ev;
+      delete[] t.stage;
+      t.ev = nullptr;
+      t.stage = nullptr;
+      return VP_ERR_CUDA;
+    }
+  }
+  t.cap = max_launches;
+  return VP_OK;
+}
+
+VP_EXPORT int vp_stage_timing_read(float* ms, int32_t* counts, int n) {
+  for (int s = 0; s < n && s < kNumStages; ++s) {
+    if (ms) ms[s] = 0.f;
+    if (counts) counts[s] = 0;
+  }
+  const StageTimer& t = g_timer;
+  for (int i = 0; i < t.used; ++i) {
+    float x = 0.f;
+    if (cudaEventSynchronize(t.ev[2 * i + 1]) != cudaSuccess) return -1;
+    if (cudaEventElapsedTime(&x, t.ev[2 * i], t.ev[2 * i + 1]) != cudaSuccess) return -1;
+    const int s = t.stage[i];
+    if (s < n) {
+      if (ms) ms[s] += x;
+      if (counts) counts[s] += 1;
+    }
+  }
+  return kNumStages;
+}
+
+VP_EXPORT const char* vp_stage_name(int stage) {
+  return (stage >= 0 && stage < kNumStages) ? kStageNames[stage] : nullptr;
 }
