@@ -129,6 +129,39 @@ vp_status vp_lmhead_ce_fwd(const void* X, const void* W, const int64_t* targets,
                            void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * vp_lmhead_ce_fwd_noalloc -- vp_lmhead_ce_fwd for callers that cannot
+ * allocate device memory.  The source pages have no counterpart to this call;
+ * it exists for users of this library.
+ *
+ * Some callers have no device allocator to draw a workspace from: a plugin
+ * whose host hands it only input and output buffers, or a latency-bound loop
+ * that must never call cudaMalloc (which can synchronise the device and has
+ * no time bound).  This call takes the same inputs and outputs as
+ * vp_lmhead_ce_fwd and computes the same results, but keeps its scratch in a
+ * fixed 32 MiB device array inside libvp instead of a caller workspace.
+ *
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - Every GPU that loads libvp holds the 32 MiB array until the process exits.
+ *   - Size limit: 256 + ceil(V/tile)*slots*N*8 + N*4 bytes (rounded up to 256)
+ *     must fit in 32 MiB, where tile = 256 (bf16) or 64 (f32) and slots is the
+ *     number of shard segments one tile can touch (2 when V/T >= tile, at most
+ *     T).  Larger sizes return VP_ERR_WORKSPACE and launch nothing.  Example:
+ *     N=4096, V=6400, T=2, bf16 needs 1.6 MiB; N=16384, V=128256 does not fit.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Calls whose executions overlap on the GPU (different streams, or
+ *     different host threads on one device) race on it: serialise them.
+ *   - The device status word lives in the shared array and is not readable
+ *     through vp_read_device_status.
+ */
+vp_status vp_lmhead_ce_fwd_noalloc(const void* X, const void* W, const int64_t* targets,
+                                   int64_t N, int64_t H, int64_t V, int T,
+                                   int64_t ignore_index, vp_dtype dtype,
+                                   float* loss, float* lse, float* loss_mean,
+                                   float* shard_stats, int32_t* n_bad, void* stream);
+
+/*
  * vp_lmhead_ce_bwd -- backward of vp_lmhead_ce_fwd.
  *
  * "Vocab Parallelism" sec. 5.3.2 and the interview note's key formulas: the
