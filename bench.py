@@ -109,6 +109,34 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power)}
 
 
+# ------------------------------------------------------------------ ranks
+def rank_env():
+    """(rank, world size, local rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(wl, rank):
+    """Each rank draws its own batch: weak scaling over independent batches."""
+    return wl.seed + rank
+
+
+def max_over_ranks(x, world, device=None):
+    """The slowest rank's time (the job's time); a no-op on one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, steps, seconds):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / seconds
+
+
 # ------------------------------------------------------------------ oracle timing (host cores)
 def oracle_tokens_per_s(inp, budget_s):
     """Time the float64 oracle (fwd + bwd, exactly as it stands) on a leading
@@ -144,7 +172,7 @@ def cores_used():
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
     import synth
-    rank = int(os.environ.get("RANK", "0"))
+    rank, _, _ = rank_env()
     if rank != 0:
         return
     wl = synth.WORKLOADS[args.workload]
@@ -189,9 +217,7 @@ def run_ours(args):
     import synth
     import vocab_lm_head_vp_b300 as vp
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = rank_env()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     if world > 1:
@@ -202,7 +228,7 @@ def run_ours(args):
             dist.barrier()
 
     wl = synth.WORKLOADS[args.workload]
-    inp = synth.make_inputs(wl, seed=wl.seed + rank)
+    inp = synth.make_inputs(wl, seed=rank_seed(wl, rank))
     N, H, V, T = wl.N, wl.H, wl.V, wl.T
     to = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
     X = to(inp.X_bits).to(dev)
@@ -247,10 +273,7 @@ def run_ours(args):
     ms = e0.elapsed_time(e1)
     stages = vp.stage_timing_read()
     vp.stage_timing_enable(0)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # ---------------- end to end through host buffers (X, targets in; loss out)
     Xh = to(inp.X_bits).pin_memory()
@@ -269,10 +292,7 @@ def run_ours(args):
         mean_h.copy_(fo["mean"], non_blocking=True)
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, world, dev)
     h2d = Xh.numel() * 2 + yh.numel() * 8
     d2h = loss_h.numel() * 4 + 4
 
@@ -283,7 +303,7 @@ def run_ours(args):
 
     peaks = load_peaks()
     sec = ms / 1e3
-    value = world * N * args.steps / sec
+    value = job_tokens_per_s(N, world, args.steps, sec)
     alg = 6.0 * N * H * V          # fwd 2NHV + dX 2NHV + dW 2NHV
     exe = 8.0 * N * H * V          # + the logit recompute in the backward
     gemm_ms = sum(stages[s][0] for s in GEMM_STAGES)
@@ -316,7 +336,7 @@ def run_ours(args):
         "stages_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in stages.items() if v[1]},
         "gpu_launches": launches,
         "clocks": clk,
-        "e2e": {"value": world * N * args.e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_tokens_per_s(N, world, args.e2e_steps, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "note": "X and targets copied from pinned host memory and loss read back every step; "
                         "the weight W is model state resident in HBM"},

@@ -110,7 +110,7 @@ def _check(inp, T, f, dX, dW, ignore_index=IGN, dloss=None, check_stats=True):
     if check_stats:
         st = np64(f["shard_stats"])
         so = o["shard_stats"]
-        # single logits carry the rounding of an H-term dot product: judge them on
+        # single logits carry the rounding of an H-term dot product: measure them on
         # the scale of the row's logits (|lse|), as the loss lse - z_y is
         row_scale = np.broadcast_to(np.abs(lse_ref)[None, :], so[:, 0].shape)
         assert_loss_close(st[:, 0], so[:, 0], wl.dtype, scale=row_scale, what="m_t")
