@@ -43,6 +43,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU work budget of the oracle baseline")
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--gemm-variant", choices=["pair", "single"], default="single",
+                   help="tcgen05 GEMM form: 256x256 tiles on SM pairs, or 128x256 tiles on one SM")
     return p.parse_args()
 
 
@@ -220,6 +222,7 @@ def run_ours(args):
     rank, world, local = rank_env()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    vp.set_gemm_variant(args.gemm_variant == "pair")
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
@@ -320,7 +323,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) X, N(0,0.02^2) W, Zipf targets)",
         "config": dict(workload_config(wl), parallelism=f"replicas x{world}, no data-path collective",
-                       vocab_chunks=1),
+                       vocab_chunks=1, gemm_variant=args.gemm_variant),
         "tflops_algorithmic": alg * args.steps / sec / 1e12,
         "tflops_executed": exe * args.steps / sec / 1e12,
         "pct_bf16_peak_algorithmic": 100.0 * alg * args.steps / sec / 1e12 / peaks["bf16_tflops"],

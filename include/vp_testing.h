@@ -30,6 +30,15 @@ vp_status vp_test_gemm_bf16(const void* A, const void* B, float* D, int64_t M, i
                             int a_mn_major, int b_mn_major, void* workspace, void* stream);
 
 /*
+ * vp_test_set_gemm_variant -- select the tcgen05 GEMM form used by every
+ * later bf16 call in this process: 1 runs each 256 x 256 tile on a pair of
+ * SMs (cta_group::2, a cluster of 2 CTAs), 0 (default) runs each 128 x 256
+ * tile on one SM.  Both compute the same results; this exists to compare them
+ * (under a sustained power cap the one-SM form has measured faster).
+ */
+vp_status vp_test_set_gemm_variant(int pair);
+
+/*
  * Stage timing for measurement harnesses.  While enabled, every libvp call
  * records a CUDA event on its stream before and after each kernel it
  * launches, so a harness can attribute device time to kernels inside its

@@ -1,6 +1,7 @@
 """The tcgen05 GEMM core alone against a float64 matmul of the same bf16
 operands, for every operand major-ness the path uses, on sizes with several
-tiles and ragged tails.  Collected first: a core fault stops the GPU run."""
+tiles and ragged tails, in both forms (one 256x256 tile per SM pair, one
+128x256 tile per SM).  Collected first: a core fault stops the GPU run."""
 import numpy as np
 import pytest
 import torch
@@ -9,12 +10,19 @@ import vocab_lm_head_vp_b300 as vp
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(128, 256, 64), (304, 520, 200), (1024, 768, 1024), (136, 264, 4104)]
+SHAPES = [(128, 256, 64), (304, 520, 200), (1024, 768, 1024), (136, 264, 4104), (8, 8, 8)]
+
+
+@pytest.fixture(params=["pair", "single"])
+def variant(request):
+    vp.set_gemm_variant(request.param == "pair")
+    yield request.param
+    vp.set_gemm_variant(False)
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_gemm_core(M, N, K, a_mn, b_mn):
+def test_gemm_core(M, N, K, a_mn, b_mn, variant):
     g = torch.Generator(device="cpu").manual_seed(M * 7 + N * 3 + K)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
     B = torch.randn(N, K, generator=g).to(torch.bfloat16)

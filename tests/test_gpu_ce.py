@@ -241,3 +241,16 @@ def test_results_repeatable():
     a = _run(inp, 3)
     b = _run(inp, 3)
     assert torch.equal(a[0]["loss"], b[0]["loss"]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+@pytest.mark.parametrize("pair", [True, False])
+def test_gemm_forms_agree_on_the_path(pair):
+    """The fused fwd/bwd with the SM-pair GEMMs and with one-SM GEMMs both match
+    the oracle (ragged N and V, a shard edge inside tiles, two vocab chunks)."""
+    vp.set_gemm_variant(pair)
+    try:
+        inp = synth.small_case(333, 264, 1800, 6, "bf16", seed=77, ignore_frac=0.1)
+        f, dX, dW = _run(inp, 6, vocab_chunk=1024)
+        _check(inp, 6, f, dX, dW)
+    finally:
+        vp.set_gemm_variant(False)

@@ -18,7 +18,7 @@ import os
 import torch
 
 __all__ = ["embed_fwd", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce", "workspace_size", "read_device_status",
-           "test_gemm_bf16", "stage_timing_enable", "stage_timing_read", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
+           "test_gemm_bf16", "set_gemm_variant", "stage_timing_enable", "stage_timing_read", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
 
 VP_F32, VP_BF16 = 0, 1
 IGNORE_INDEX = -100
@@ -62,6 +62,8 @@ def _load():
     L.vp_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     L.vp_test_gemm_bf16.restype = I32
     L.vp_test_gemm_bf16.argtypes = [P, P, P, I64, I64, I64, U, U, P, P]
+    L.vp_test_set_gemm_variant.restype = I32
+    L.vp_test_set_gemm_variant.argtypes = [I32]
     L.vp_stage_timing_enable.restype = I32
     L.vp_stage_timing_enable.argtypes = [I32]
     L.vp_stage_timing_read.restype = I32
@@ -216,6 +218,11 @@ def test_gemm_bf16(A, B, a_mn_major=False, b_mn_major=False):
     _check("vp_test_gemm_bf16", _load().vp_test_gemm_bf16(_ptr(A), _ptr(B), _ptr(D), M, N, K, int(a_mn_major),
                                                           int(b_mn_major), _ptr(ws), _stream(A.device)))
     return D, ws
+
+
+def set_gemm_variant(pair: bool) -> None:
+    """Run the tcgen05 GEMMs on SM pairs (True) or one SM per tile (False, default)."""
+    _check("vp_test_set_gemm_variant", _load().vp_test_set_gemm_variant(int(bool(pair))))
 
 
 def stage_timing_enable(max_launches: int) -> None:

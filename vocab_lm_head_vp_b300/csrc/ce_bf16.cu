@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include "umma_gemm.cuh"
+#include "umma_gemm_2sm.cuh"
 #include "vp_internal.h"
 
 namespace vp {
@@ -28,6 +29,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // ------------------------------------------------------------------ forward
 struct EpiLseStats {
+  static constexpr uint32_t kStagingBytes = 0;
   struct Params {
     float2* partial;          // [num_vtiles * maxseg][N] (m, S)
     float* zy;                // [N] target logit, written by the owning tile
@@ -35,7 +37,7 @@ struct EpiLseStats {
     int64_t N, V, Vs;         // tokens, vocab, shard width V/T
     int maxseg;               // record slots per vocab tile
   };
-  __device__ static void run(const Params& p, uint32_t taddr, int64_t n, int /*mb*/, int nb) {
+  __device__ static void run(const Params& p, const CUtensorMap*, uint32_t taddr, int64_t n, int nb, EpiCtx&) {
     const int64_t v0 = static_cast<int64_t>(nb) * kBN;
     const int64_t vend = min(v0 + kBN, p.V);
     const bool row_ok = n < p.N;
@@ -114,53 +116,48 @@ struct EpiLseStats {
 };
 
 // ------------------------------------------------------------------ backward dZ
+// dZ boxes of 32 rows x 64 bf16 columns go out through TMA (the tensor map
+// clips rows >= N and columns >= Vc).
 struct EpiDZ {
+  static constexpr uint32_t kStagingBytes = kStoreStagingBytes;
   struct Params {
-    __nv_bfloat16* dz;        // [N][ldz], chunk-local columns
-    int64_t ldz;
     const float* lse;         // [N]
     const float* g;           // [N] upstream scale (0 for ignored rows)
     const int64_t* targets;   // [N]
     int64_t N;
     int64_t c0, Vc;           // chunk start (global vocab id) and width
   };
-  __device__ static void run(const Params& p, uint32_t taddr, int64_t n, int /*mb*/, int nb) {
+  __device__ static void run(const Params& p, const CUtensorMap* tm, uint32_t taddr, int64_t n, int nb,
+                             EpiCtx& ctx) {
     const int64_t v0 = static_cast<int64_t>(nb) * kBN;   // chunk-local
     const int64_t vend = min(v0 + kBN, p.Vc);
     const bool row_ok = n < p.N;
+    const bool warp_live = ctx.row0 < p.N;
     const float g = row_ok ? p.g[n] : 0.f;
     const float nl = row_ok ? -p.lse[n] * kLog2e : 0.f;
     const int64_t yl = (row_ok ? p.targets[n] : -1) - p.c0 - v0;
-    __nv_bfloat16* out = p.dz + (row_ok ? n : 0) * p.ldz;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      const int64_t col0 = v0 + c * 32;
+    for (int b = 0; b < kBN / 64; ++b) {
+      const int64_t col0 = v0 + b * 64;
       if (col0 >= vend) break;
-      uint32_t r[32];
-      __syncwarp();
-      tmem_ld32(taddr + c * 32, r);
-      tmem_ld_wait();
-      const int64_t j = yl - c * 32;
-      uint32_t w[16];
+      uint32_t w[32];
 #pragma unroll
-      for (int q = 0; q < 32; q += 2) {
-        float d0 = g * ex2_approx(fmaf(as_f(r[q]), kLog2e, nl));
-        float d1 = g * ex2_approx(fmaf(as_f(r[q + 1]), kLog2e, nl));
-        if (q == j) d0 -= g;
-        if (q + 1 == j) d1 -= g;
-        w[q / 2] = pack_bf16x2(d0, d1);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(taddr + b * 64 + h * 32, r);
+        tmem_ld_wait();
+        const int64_t j = yl - (b * 64 + h * 32);
+#pragma unroll
+        for (int q = 0; q < 32; q += 2) {
+          float d0 = g * ex2_approx(fmaf(as_f(r[q]), kLog2e, nl));
+          float d1 = g * ex2_approx(fmaf(as_f(r[q + 1]), kLog2e, nl));
+          if (q == j) d0 -= g;
+          if (q + 1 == j) d1 -= g;
+          w[h * 16 + q / 2] = pack_bf16x2(d0, d1);
+        }
       }
-      if (!row_ok) continue;
-      if (col0 + 32 <= vend) {
-        uint4* dst = reinterpret_cast<uint4*>(out + col0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-      } else {
-        uint16_t* dst = reinterpret_cast<uint16_t*>(out + col0);
-#pragma unroll
-        for (int q = 0; q < 32; ++q)
-          if (col0 + q < vend) dst[q] = static_cast<uint16_t>(w[q / 2] >> (16 * (q & 1)));
-      }
+      if (warp_live) stage_and_store(ctx, tm, w, static_cast<int32_t>(col0));
     }
   }
 };
@@ -168,76 +165,70 @@ struct EpiDZ {
 // ------------------------------------------------------------------ store
 enum StoreMode : int { kStoreF32 = 0, kAddF32 = 1, kStoreBf16AddPartial = 2, kStoreBf16 = 3 };
 
+// fp32 modes store 32-column boxes, bf16 modes 64-column boxes, through TMA.
 struct EpiStore {
+  static constexpr uint32_t kStagingBytes = kStoreStagingBytes;
   struct Params {
-    void* out;              // f32 or bf16 [M][ld_out]
-    const float* partial;   // f32 [M][ld_out] (mode kStoreBf16AddPartial)
-    int64_t ld_out;
+    const float* partial;   // f32 [M][ld] read and added first (modes kAddF32, kStoreBf16AddPartial)
+    int64_t ld;             // leading dimension of `partial`
     int64_t M, N;           // valid rows / cols of the output
     int mode;
   };
-  __device__ static void run(const Params& p, uint32_t taddr, int64_t row, int /*mb*/, int nb) {
+  __device__ static void run(const Params& p, const CUtensorMap* tm, uint32_t taddr, int64_t row, int nb,
+                             EpiCtx& ctx) {
     const int64_t n0 = static_cast<int64_t>(nb) * kBN;
     const int64_t nend = min(n0 + kBN, p.N);
     const bool row_ok = row < p.M;
-    const int64_t roff = (row_ok ? row : 0) * p.ld_out;
+    const bool warp_live = ctx.row0 < p.M;
+    const bool add = p.mode == kAddF32 || p.mode == kStoreBf16AddPartial;
+    const float* src = add && row_ok ? p.partial + row * p.ld : nullptr;
+    if (p.mode == kStoreF32 || p.mode == kAddF32) {
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      const int64_t col0 = n0 + c * 32;
-      if (col0 >= nend) break;
-      uint32_t r[32];
-      __syncwarp();
-      tmem_ld32(taddr + c * 32, r);
-      tmem_ld_wait();
-      if (!row_ok) continue;
-      const bool full = col0 + 32 <= nend;
-      float v[32];
-#pragma unroll
-      for (int q = 0; q < 32; ++q) v[q] = as_f(r[q]);
-      if (p.mode == kAddF32 || p.mode == kStoreBf16AddPartial) {
-        const float* src = (p.mode == kAddF32 ? static_cast<const float*>(p.out) : p.partial) + roff + col0;
-        if (full) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 a = reinterpret_cast<const float4*>(src)[q];
-            v[4 * q] += a.x;
-            v[4 * q + 1] += a.y;
-            v[4 * q + 2] += a.z;
-            v[4 * q + 3] += a.w;
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 32; ++q)
-            if (col0 + q < nend) v[q] += src[q];
-        }
+      for (int b = 0; b < kBN / 32; ++b) {
+        const int64_t col0 = n0 + b * 32;
+        if (col0 >= nend) break;
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(taddr + b * 32, r);
+        tmem_ld_wait();
+        if (src) add_partial(r, src + col0, nend - col0);
+        if (warp_live) stage_and_store(ctx, tm, r, static_cast<int32_t>(col0));
       }
-      if (p.mode == kStoreF32 || p.mode == kAddF32) {
-        float* dst = static_cast<float*>(p.out) + roff + col0;
-        if (full) {
+    } else {
+#pragma unroll 1
+      for (int b = 0; b < kBN / 64; ++b) {
+        const int64_t col0 = n0 + b * 64;
+        if (col0 >= nend) break;
+        uint32_t w[32];
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else {
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld32(taddr + b * 64 + h * 32, r);
+          tmem_ld_wait();
+          if (src) add_partial(r, src + col0 + h * 32, nend - col0 - h * 32);
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            if (col0 + q < nend) dst[q] = v[q];
+          for (int q = 0; q < 16; ++q) w[h * 16 + q] = pack_bf16x2(as_f(r[2 * q]), as_f(r[2 * q + 1]));
         }
-      } else {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + roff + col0;
-        uint32_t w[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) w[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
-        if (full) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            reinterpret_cast<uint4*>(dst)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 32; ++q)
-            if (col0 + q < nend)
-              reinterpret_cast<uint16_t*>(dst)[q] = static_cast<uint16_t>(w[q / 2] >> (16 * (q & 1)));
-        }
+        if (warp_live) stage_and_store(ctx, tm, w, static_cast<int32_t>(col0));
       }
+    }
+  }
+  // r[q] += src[q] for the q < valid columns of this 32-column slice
+  __device__ static void add_partial(uint32_t (&r)[32], const float* src, int64_t valid) {
+    if (valid >= 32) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 a = reinterpret_cast<const float4*>(src)[q];
+        r[4 * q] = __float_as_uint(as_f(r[4 * q]) + a.x);
+        r[4 * q + 1] = __float_as_uint(as_f(r[4 * q + 1]) + a.y);
+        r[4 * q + 2] = __float_as_uint(as_f(r[4 * q + 2]) + a.z);
+        r[4 * q + 3] = __float_as_uint(as_f(r[4 * q + 3]) + a.w);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 32; ++q)
+        if (q < valid) r[q] = __float_as_uint(as_f(r[q]) + src[q]);
     }
   }
 };
@@ -248,18 +239,26 @@ namespace {
 // 2-D bf16 tensor map over a row-major [rows][cols] matrix with leading
 // dimension `ld` elements; box = {box_cols (inner), box_rows}, 128B swizzle,
 // out-of-bounds elements read as zero.
-bool make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
-                    int box_rows) {
+bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, int64_t rows, int64_t cols,
+               int64_t ld, int box_cols, int box_rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                    int box_rows) {
+  return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, cols, ld, box_cols, box_rows);
+}
+// Output maps of the TMA-storing epilogues: boxes of 32 rows x 128 bytes.
+bool make_store_tmap(CUtensorMap* m, bool bf16, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+  return bf16 ? make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, cols, ld, 64, 32)
+              : make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, cols, ld, 32, 32);
 }
 
 int sm_count() {
@@ -274,13 +273,14 @@ int sm_count() {
 }
 
 template <bool A_MN, bool B_MN, class Epi>
-cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int64_t M, int64_t Ncols, int64_t K,
-                        const typename Epi::Params& ep, uint32_t* status, cudaStream_t stream, int group_m) {
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, int64_t M,
+                        int64_t Ncols, int64_t K, const typename Epi::Params& ep, uint32_t* status,
+                        cudaStream_t stream, int group_m) {
   auto kern = umma_gemm_kernel<A_MN, B_MN, Epi>;
+  constexpr size_t smem = kGemmSmemBytes + Epi::kStagingBytes;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kGemmSmemBytes));
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -292,11 +292,70 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int64_t M,
   a.status = status;
   const int total = a.sched.num_m * a.sched.num_n;
   const int grid = total < sm_count() ? total : sm_count();
-  kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(ta, tb, a, ep);
+  kern<<<grid, kGemmThreads, smem, stream>>>(ta, tb, tc, a, ep);
   return cudaGetLastError();
 }
 
+// One 256 x 256 tile per CTA pair (cluster of 2) on the persistent grid of
+// as many pairs as can be resident at once.
+template <bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_gemm_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, int64_t M,
+                            int64_t Ncols, int64_t K, const typename Epi::Params& ep, uint32_t* status,
+                            cudaStream_t stream, int group_m) {
+  auto kern = umma_gemm_2sm_kernel<A_MN, B_MN, Epi>;
+  constexpr size_t smem = kGemm2SmemBytes + Epi::kStagingBytes;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_pairs = 0;
+  if (max_pairs == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = sm_count() / 2;
+    }
+    max_pairs = n;
+  }
+  GemmArgs a;
+  a.sched.num_m = static_cast<int>((M + kPairBM - 1) / kPairBM);
+  a.sched.num_n = static_cast<int>((Ncols + kBN - 1) / kBN);
+  a.sched.group_m = group_m < 1 ? 1 : group_m;
+  a.num_k = static_cast<int>((K + kBK - 1) / kBK);
+  a.status = status;
+  const int total = a.sched.num_m * a.sched.num_n;
+  const int pairs = total < max_pairs ? total : max_pairs;
+  cfg.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, a, ep);
+}
+
+bool g_pair_kernels = false;  // one SM per tile by default (faster under the power cap); vp_test_set_gemm_variant switches
+
+// B operand K-major box rows: 256 for one SM, 128 (its half) for a CTA pair.
+int kmajor_b_box_rows() { return g_pair_kernels ? 128 : kBN; }
+
+template <bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_any(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, int64_t M,
+                       int64_t Ncols, int64_t K, const typename Epi::Params& ep, uint32_t* status,
+                       cudaStream_t stream, int group_m_rows) {
+  if (g_pair_kernels)
+    return launch_gemm_2sm<A_MN, B_MN, Epi>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows / kPairBM);
+  return launch_gemm<A_MN, B_MN, Epi>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows / kBM);
+}
+
 }  // namespace
+
+void set_gemm_variant(int pair) { g_pair_kernels = pair != 0; }
 
 int lse_maxseg(int64_t V, int64_t Vs, int T) {
   // shard segments one 256-wide tile can touch: at most floor(255 / Vs) + 2, and at most T
@@ -313,20 +372,21 @@ cudaError_t bf16_lse_stats(const void* X, const void* W, const int64_t* targets,
                            cudaStream_t stream) {
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, X, N, H, H, kBK, kBM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tb, W, V, H, H, kBK, kBN)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, W, V, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
   EpiLseStats::Params p{partial, zy, targets, N, V, Vs, maxseg};
-  return launch_gemm<false, false, EpiLseStats>(ta, tb, N, V, H, p, status, stream, 16);
+  return launch_any<false, false, EpiLseStats>(ta, tb, ta, N, V, H, p, status, stream, 2048);
 }
 
 cudaError_t bf16_dz_chunk(const void* X, const void* W, const int64_t* targets, const float* lse, const float* g,
                           int64_t N, int64_t H, int64_t c0, int64_t Vc, void* dz, int64_t ldz, uint32_t* status,
                           cudaStream_t stream) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   const uint8_t* Wc = static_cast<const uint8_t*>(W) + c0 * H * 2;
   if (!make_tmap_bf16(&ta, X, N, H, H, kBK, kBM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tb, Wc, Vc, H, H, kBK, kBN)) return cudaErrorInvalidValue;
-  EpiDZ::Params p{static_cast<__nv_bfloat16*>(dz), ldz, lse, g, targets, N, c0, Vc};
-  return launch_gemm<false, false, EpiDZ>(ta, tb, N, Vc, H, p, status, stream, 16);
+  if (!make_tmap_bf16(&tb, Wc, Vc, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
+  if (!make_store_tmap(&tc, true, dz, N, Vc, ldz)) return cudaErrorInvalidValue;
+  EpiDZ::Params p{lse, g, targets, N, c0, Vc};
+  return launch_any<false, false, EpiDZ>(ta, tb, tc, N, Vc, H, p, status, stream, 2048);
 }
 
 cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N, int64_t H, int64_t c0,
@@ -334,39 +394,42 @@ cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N,
                           cudaStream_t stream) {
   // dX[N,H] (+)= dZ_c[N,Vc] * W_c[Vc,H]: A = dZ_c (K-major), B = W_c viewed as
   // [K=Vc rows][N=H cols] (MN-major).
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   const uint8_t* Wc = static_cast<const uint8_t*>(W) + c0 * H * 2;
   if (!make_tmap_bf16(&ta, dz, N, Vc, ldz, kBK, kBM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, Wc, Vc, H, H, 64, kBK)) return cudaErrorInvalidValue;
-  EpiStore::Params p{out, partial, H, N, H, mode};
-  return launch_gemm<false, true, EpiStore>(ta, tb, N, H, Vc, p, status, stream, 8);
+  if (!make_store_tmap(&tc, mode >= kStoreBf16AddPartial, out, N, H, H)) return cudaErrorInvalidValue;
+  EpiStore::Params p{mode == kAddF32 ? static_cast<const float*>(out) : partial, H, N, H, mode};
+  return launch_any<false, true, EpiStore>(ta, tb, tc, N, H, Vc, p, status, stream, 1024);
 }
 
 cudaError_t bf16_dw_chunk(const void* dz, int64_t ldz, const void* X, int64_t N, int64_t H, int64_t c0,
                           int64_t Vc, float* dW, uint32_t* status, cudaStream_t stream) {
   // dW_c[Vc,H] = dZ_c^T[Vc,N] * X[N,H]: A = dZ_c viewed as [K=N rows][M=Vc cols]
   // (MN-major), B = X viewed as [K=N rows][N=H cols] (MN-major).
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if (!make_tmap_bf16(&ta, dz, N, Vc, ldz, 64, kBK)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, X, N, H, H, 64, kBK)) return cudaErrorInvalidValue;
-  EpiStore::Params p{dW + c0 * H, nullptr, H, Vc, H, kStoreF32};
-  return launch_gemm<true, true, EpiStore>(ta, tb, Vc, H, N, p, status, stream, 8);
+  if (!make_store_tmap(&tc, false, dW + c0 * H, Vc, H, H)) return cudaErrorInvalidValue;
+  EpiStore::Params p{nullptr, H, Vc, H, kStoreF32};
+  return launch_any<true, true, EpiStore>(ta, tb, tc, Vc, H, N, p, status, stream, 1024);
 }
 
 // Plain GEMM entry used by the unit tests of the core: D[M,N] = A * B^T with
 // A/B K-major or MN-major, fp32 output.
 cudaError_t bf16_gemm_test(const void* A, const void* B, float* D, int64_t M, int64_t Ncols, int64_t K,
                            int a_mn, int b_mn, uint32_t* status, cudaStream_t stream) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   bool ok = a_mn ? make_tmap_bf16(&ta, A, K, M, M, 64, kBK) : make_tmap_bf16(&ta, A, M, K, K, kBK, kBM);
   ok = ok && (b_mn ? make_tmap_bf16(&tb, B, K, Ncols, Ncols, 64, kBK)
-                   : make_tmap_bf16(&tb, B, Ncols, K, K, kBK, kBN));
+                   : make_tmap_bf16(&tb, B, Ncols, K, K, kBK, kmajor_b_box_rows()));
+  ok = ok && make_store_tmap(&tc, false, D, M, Ncols, Ncols);
   if (!ok) return cudaErrorInvalidValue;
-  EpiStore::Params p{D, nullptr, Ncols, M, Ncols, kStoreF32};
-  if (!a_mn && !b_mn) return launch_gemm<false, false, EpiStore>(ta, tb, M, Ncols, K, p, status, stream, 8);
-  if (!a_mn && b_mn) return launch_gemm<false, true, EpiStore>(ta, tb, M, Ncols, K, p, status, stream, 8);
-  if (a_mn && b_mn) return launch_gemm<true, true, EpiStore>(ta, tb, M, Ncols, K, p, status, stream, 8);
-  return launch_gemm<true, false, EpiStore>(ta, tb, M, Ncols, K, p, status, stream, 8);
+  EpiStore::Params p{nullptr, Ncols, M, Ncols, kStoreF32};
+  if (!a_mn && !b_mn) return launch_any<false, false, EpiStore>(ta, tb, tc, M, Ncols, K, p, status, stream, 1024);
+  if (!a_mn && b_mn) return launch_any<false, true, EpiStore>(ta, tb, tc, M, Ncols, K, p, status, stream, 1024);
+  if (a_mn && b_mn) return launch_any<true, true, EpiStore>(ta, tb, tc, M, Ncols, K, p, status, stream, 1024);
+  return launch_any<true, false, EpiStore>(ta, tb, tc, M, Ncols, K, p, status, stream, 1024);
 }
 
 }  // namespace vp

@@ -38,6 +38,38 @@ constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr uint32_t kMnBoxBytes = 64 * kBK * 2;  // one {64 MN, 64 K} box: 8 KB
 constexpr size_t kGemmSmemBytes = 1024 + kStages * kStageBytes + 256;
+// Epilogues that store through TMA stage one 32-row x 128-byte box per warp,
+// double-buffered: 4 warps x 2 x 4 KB.
+constexpr uint32_t kStoreBoxBytes = 32 * 128;
+constexpr uint32_t kStoreStagingBytes = 4 * 2 * kStoreBoxBytes;
+
+// Per-warp state of a TMA-storing epilogue.
+struct EpiCtx {
+  uint8_t* stg;     // this warp's two 4 KB staging boxes (1024-byte aligned)
+  int buf;          // box to fill next
+  int lane;
+  int64_t row0;     // first output row of this warp's 32-row block
+};
+
+// Write this thread's 128-byte row (8 x 16 B) into the warp's staging box in
+// the 128-byte swizzled order TMA expects (chunk j of row r at j ^ (r & 7)),
+// then one lane stores the 32-row box at (c0, row0).  All 32 lanes call it.
+__device__ __forceinline__ void stage_and_store(EpiCtx& ctx, const CUtensorMap* tm, const uint32_t (&w)[32],
+                                                int32_t c0) {
+  uint8_t* box = ctx.stg + ctx.buf * kStoreBoxBytes;
+  if (ctx.lane == 0) bulk_wait_group_read<1>();   // the store that last used this box has read it
+  __syncwarp();
+  uint4* row = reinterpret_cast<uint4*>(box + ctx.lane * 128);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) row[j ^ (ctx.lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (ctx.lane == 0) {
+    tma_store_2d(tm, box, c0, static_cast<int32_t>(ctx.row0));
+    bulk_commit_group();
+  }
+  ctx.buf ^= 1;
+}
 
 struct TileSched {
   int num_m, num_n, group_m;
@@ -68,13 +100,14 @@ __device__ __forceinline__ void record_failure(uint32_t* status, volatile int* a
 template <bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmArgs args, const typename Epi::Params ep) {
+                     const __grid_constant__ CUtensorMap tmC, const GemmArgs args, const typename Epi::Params ep) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   uint8_t* sA = smem;                         // kStages x 16 KB
   uint8_t* sB = smem + kStages * kABytes;     // kStages x 32 KB
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint8_t* sC = smem + kStages * kStageBytes; // Epi::kStagingBytes (0 or 32 KB)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sC + Epi::kStagingBytes);
   uint64_t* full = bars;                      // TMA -> MMA
   uint64_t* empty = bars + kStages;           // MMA -> TMA
   uint64_t* tfull = bars + 2 * kStages;       // MMA -> epilogue (2 accumulators)
@@ -102,6 +135,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (Epi::kStagingBytes) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -210,7 +244,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // -------------------------------------------------- epilogue warps
     const int quad = warp & 3;
-    const int row = quad * 32 + lane;
+    EpiCtx ctx{sC + (warp - 2) * 2 * kStoreBoxBytes, 0, lane, 0};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -223,12 +257,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_after();
       const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * kBN) + (static_cast<uint32_t>(quad * 32) << 16);
-      Epi::run(ep, taddr, static_cast<int64_t>(mb) * kBM + row, mb, nb);
+      ctx.row0 = static_cast<int64_t>(mb) * kBM + quad * 32;
+      Epi::run(ep, &tmC, taddr, ctx.row0 + lane, nb, ctx);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (Epi::kStagingBytes && lane == 0) bulk_wait_group<0>();   // this warp's stores are complete
   }
 
   __syncthreads();

@@ -324,3 +324,8 @@ VP_EXPORT int vp_stage_timing_read(float* ms, int32_t* counts, int n) {
 VP_EXPORT const char* vp_stage_name(int stage) {
   return (stage >= 0 && stage < kNumStages) ? kStageNames[stage] : nullptr;
 }
+
+VP_EXPORT vp_status vp_test_set_gemm_variant(int pair) {
+  set_gemm_variant(pair);
+  return VP_OK;
+}

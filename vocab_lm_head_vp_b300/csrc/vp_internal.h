@@ -28,6 +28,8 @@ cudaError_t bf16_dw_chunk(const void* dz, int64_t ldz, const void* X, int64_t N,
                           float* dW, uint32_t* status, cudaStream_t stream);
 cudaError_t bf16_gemm_test(const void* A, const void* B, float* D, int64_t M, int64_t Ncols, int64_t K, int a_mn,
                            int b_mn, uint32_t* status, cudaStream_t stream);
+// 1: tcgen05 GEMMs run as 2-SM CTA pairs (256 x 256 tiles); 0 (default): one SM per 128 x 256 tile.
+void set_gemm_variant(int pair);
 constexpr int kBf16TileV = 256;  // vocab width of one forward tile (statistics record granularity)
 
 // ---- fp32 CUDA-core path (ce_simt.cu)
