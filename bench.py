@@ -4,7 +4,13 @@ one batch -- embedding gather of the batch's ids, fused LM head + CE forward,
 and its backward (dX, dW) -- on seeded synthetic inputs resident in HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload v128k] [--no-cpu-baseline]
+                    [--workload v128k] [--path fused|split] [--no-cpu-baseline]
+
+``--path fused`` (default) runs the LM head as one vp_lmhead_ce_fwd_bwd call
+(tile probabilities saved in fp16, 3 GEMMs per step); ``--path split`` runs
+vp_lmhead_ce_fwd + vp_lmhead_ce_bwd (logits recomputed, 4 GEMMs per step).
+The other path is also timed briefly after the timed region and reported
+under ``other_path`` (not part of ``value``).
 
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs the same
 step on its own seeded batch (weak scaling, no collective on the data path;
@@ -30,7 +36,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused LM-head+CE fwd+bwd tokens/s and % of bf16 tensor peak at V=128256"
 UNIT = "tokens/s"
-GEMM_STAGES = ("lse_stats_gemm", "dz_recompute_gemm", "dw_gemm", "dx_gemm")
+GEMM_STAGES = {"split": ("lse_stats_gemm", "dz_recompute_gemm", "dw_gemm", "dx_gemm"),
+               "fused": ("lse_p_gemm", "dw_gemm", "dx_gemm")}
 
 
 def parse_args():
@@ -43,6 +50,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU work budget of the oracle baseline")
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--path", choices=["fused", "split"], default="fused",
+                   help="fused: one fwd+bwd call with saved probabilities; split: fwd, then bwd with recompute")
+    p.add_argument("--other-path-steps", type=int, default=5, help="timed steps of the other path (0: skip)")
     p.add_argument("--gemm-variant", choices=["pair", "single"], default="single",
                    help="tcgen05 GEMM form: 256x256 tiles on SM pairs, or 128x256 tiles on one SM")
     return p.parse_args()
@@ -244,18 +254,31 @@ def run_ours(args):
           "n_bad": torch.empty(1, dtype=torch.int32, device=dev)}
     dX = torch.empty_like(X)
     dW = torch.empty((V, H), dtype=torch.float32, device=dev)
-    wsf = torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 0), dtype=torch.uint8, device=dev)
-    wsb = torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 1), dtype=torch.uint8, device=dev)
+    fo["dX"], fo["dW"] = dX, dW
 
-    def step(Xs, ys):
-        vp.embed_fwd(ys, W, T, out=emb)
-        vp.lmhead_ce_fwd(Xs, W, ys, T, workspace=wsf, out=fo)
-        vp.lmhead_ce_bwd(Xs, W, ys, fo["lse"], T, workspace=wsb, dX=dX, dW=dW)
+    def make_step(path):
+        """One step of the given path and the workspaces it uses."""
+        if path == "fused":
+            ws = torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 2), dtype=torch.uint8, device=dev)
 
+            def step(Xs, ys):
+                vp.embed_fwd(ys, W, T, out=emb)
+                vp.lmhead_ce_fwd_bwd(Xs, W, ys, T, workspace=ws, out=fo)
+            return step, [ws]
+        wsf = torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 0), dtype=torch.uint8, device=dev)
+        wsb = torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 1), dtype=torch.uint8, device=dev)
+
+        def step(Xs, ys):
+            vp.embed_fwd(ys, W, T, out=emb)
+            vp.lmhead_ce_fwd(Xs, W, ys, T, workspace=wsf, out=fo)
+            vp.lmhead_ce_bwd(Xs, W, ys, fo["lse"], T, workspace=wsb, dX=dX, dW=dW)
+        return step, [wsf, wsb]
+
+    step, workspaces = make_step(args.path)
     for _ in range(args.warmup):
         step(X, y)
     torch.cuda.synchronize()
-    assert vp.read_device_status(wsf) == 0 and vp.read_device_status(wsb) == 0
+    assert all(vp.read_device_status(w) == 0 for w in workspaces)
 
     # ---------------- timed region
     uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
@@ -298,6 +321,28 @@ def run_ours(args):
     e2e_s = max_over_ranks(e2e_s, world, dev)
     h2d = Xh.numel() * 2 + yh.numel() * 8
     d2h = loss_h.numel() * 4 + 4
+    assert all(vp.read_device_status(w) == 0 for w in workspaces)
+    del workspaces, step
+
+    # ---------------- the other path, briefly (reported beside, not in `value`)
+    other = None
+    if args.other_path_steps > 0:
+        opath = "split" if args.path == "fused" else "fused"
+        ostep, ows = make_step(opath)
+        for _ in range(2):
+            ostep(X, y)
+        torch.cuda.synchronize()
+        barrier()
+        e0.record()
+        for _ in range(args.other_path_steps):
+            ostep(X, y)
+        e1.record()
+        torch.cuda.synchronize()
+        oms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.other_path_steps
+        assert all(vp.read_device_status(w) == 0 for w in ows)
+        other = {"path": opath, "steps": args.other_path_steps, "ms_per_step": oms,
+                 "value": job_tokens_per_s(N, world, 1, oms / 1e3), "unit": UNIT}
+        del ostep, ows
 
     if rank != 0:
         if world > 1:
@@ -308,27 +353,40 @@ def run_ours(args):
     sec = ms / 1e3
     value = job_tokens_per_s(N, world, args.steps, sec)
     alg = 6.0 * N * H * V          # fwd 2NHV + dX 2NHV + dW 2NHV
-    exe = 8.0 * N * H * V          # + the logit recompute in the backward
-    gemm_ms = sum(stages[s][0] for s in GEMM_STAGES)
-    gemm_n = sum(stages[s][1] for s in GEMM_STAGES)
-    per_launch_flops = 2.0 * N * H * V          # every GEMM launch: one vocab chunk = all of V
+    # the split path also recomputes the logits in the backward
+    exe = (8.0 if args.path == "split" else 6.0) * N * H * V
+    gstages = GEMM_STAGES[args.path]
+    gemm_ms = sum(stages[s][0] for s in gstages)
+    gemm_n = sum(stages[s][1] for s in gstages)
+    per_launch_flops = 2.0 * N * H * V          # every GEMM launch: all N tokens x all V
     avg_launch_s = gemm_ms / max(1, gemm_n) / 1e3
     achieved = per_launch_flops / avg_launch_s / 1e12
     emb_ms, emb_n = stages["embed_gather"]
     emb_bytes = 2.0 * N * H * 2 + 8.0 * N
     emb_gbs = emb_bytes / (emb_ms / max(1, emb_n) / 1e3) / 1e9
+    extra = {}
+    if args.path == "fused":
+        dzp_ms, dzp_n = stages["dz_from_p"]
+        valid_rows = int(((inp.targets >= 0) & (inp.targets < V)).sum())
+        # read fp16 p and write bf16 dZ for valid rows; write zeros for ignored ones
+        dzp_bytes = (4.0 * valid_rows + 2.0 * (N - valid_rows)) * V
+        dzp_gbs = dzp_bytes / (dzp_ms / max(1, dzp_n) / 1e3) / 1e9
+        extra["roofline_dz_from_p"] = {"kernel": "dz_from_p_kernel", "bound": "hbm", "achieved": dzp_gbs,
+                                       "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dzp_gbs / peaks["hbm_gbs"]}
     launches = sum(c for _, c in stages.values())
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) X, N(0,0.02^2) W, Zipf targets)",
         "config": dict(workload_config(wl), parallelism=f"replicas x{world}, no data-path collective",
-                       vocab_chunks=1, gemm_variant=args.gemm_variant),
+                       path=args.path, chunks=1, gemm_variant=args.gemm_variant),
         "tflops_algorithmic": alg * args.steps / sec / 1e12,
         "tflops_executed": exe * args.steps / sec / 1e12,
         "pct_bf16_peak_algorithmic": 100.0 * alg * args.steps / sec / 1e12 / peaks["bf16_tflops"],
         "pct_bf16_peak_executed": 100.0 * exe * args.steps / sec / 1e12 / peaks["bf16_tflops"],
-        "roofline": {"kernel": "umma_gemm_kernel (tcgen05; 4 launches/step: lse stats, dZ recompute, dW, dX)",
+        "roofline": {"kernel": ("umma_gemm_kernel (tcgen05; 3 launches/step: lse stats + saved p, dW, dX)"
+                                if args.path == "fused" else
+                                "umma_gemm_kernel (tcgen05; 4 launches/step: lse stats, dZ recompute, dW, dX)"),
                      "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops_sustained"],
                      "peak_kind": f"bf16 sustained ({peaks['source']})",
@@ -336,6 +394,7 @@ def run_ours(args):
         "roofline_embed": {"kernel": "embed_gather_kernel", "bound": "hbm", "achieved": emb_gbs,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": emb_gbs / peaks["hbm_gbs"],
                            "note": "Zipf ids repeat rows (L2 hits)"},
+        **extra,
         "stages_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in stages.items() if v[1]},
         "gpu_launches": launches,
         "clocks": clk,
@@ -343,6 +402,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h,
                 "note": "X and targets copied from pinned host memory and loss read back every step; "
                         "the weight W is model state resident in HBM"},
+        "other_path": other,
     }
     if world == 1 and not args.no_cpu_baseline:
         v, n, t = oracle_tokens_per_s(inp, args.cpu_seconds)

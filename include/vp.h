@@ -90,6 +90,11 @@ vp_status vp_embed_fwd(const int64_t* ids, const void* W, void* out,
  *           `vocab_chunk` ids (<= 0 or >= V: one chunk, the fastest).  Any
  *           workspace at least this large for some chunk works; the backward
  *           derives its chunk from the bytes it is given.
+ *   pass 2: vp_lmhead_ce_fwd_bwd.  VP_BF16: the last argument is a TOKEN
+ *           chunk (rounded down to a multiple of 128; <= 0 or >= N: all N
+ *           tokens at once, the fastest), about N_c * (2*round8(V) + 20*V/256)
+ *           bytes; the call derives its chunk from the bytes it is given.
+ *           VP_F32: the larger of pass 0 and pass 1 (last argument = vocab chunk).
  * Returns 0 for invalid arguments.
  */
 size_t vp_lmhead_ce_workspace_size(int64_t N, int64_t H, int64_t V, int T,
@@ -187,6 +192,43 @@ vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t* targets,
                            int64_t ignore_index, vp_dtype dtype,
                            void* dX, float* dW,
                            void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * vp_lmhead_ce_fwd_bwd -- forward and backward in one call, with the
+ * probabilities saved in between instead of recomputed.
+ *
+ * "Vocab Parallelism" sec. 5.3.1-5.3.3: the forward of vp_lmhead_ce_fwd and
+ * the backward of vp_lmhead_ce_bwd for an upstream gradient known up front
+ * (dloss, or the mean over valid tokens when dloss is NULL, the usual
+ * training case).  Sec. 5.3.2 keeps each shard's softmax from the forward for
+ * its local gradient p - onehot; here the forward's epilogue writes, for every
+ * 256-wide vocab tile, p = exp(z - m_tile) in fp16 (m_tile = the row's maximum
+ * over that tile) next to the (m_t, S_t, z_y^(t)) statistics, the merge gives
+ * lse, one bandwidth-bound pass turns p in place into
+ *     dZ = g (p exp(m_tile - lse) - 1[j=y])   (bf16),
+ * and dW = dZ^T X, dX = dZ W run on the tensor cores.  Against
+ * vp_lmhead_ce_fwd + vp_lmhead_ce_bwd this skips the logit recompute
+ * (6NHV instead of 8NHV flops) at the price of holding N_c x V 2-byte
+ * probabilities: tokens are processed in chunks of N_c rows (all N when the
+ * workspace allows), so the fp32 [N,V] logits are never materialised and the
+ * saved tile is bounded by the workspace.  The f32 dtype runs the forward and
+ * the recompute backward of the split calls.
+ *
+ * Arguments and outputs are those of vp_lmhead_ce_fwd and vp_lmhead_ce_bwd:
+ *   dloss      f32 [N] or NULL (NULL: gradient of loss_mean)
+ *   loss, lse  f32 [N] written;  loss_mean, shard_stats, n_bad as in the forward
+ *   dX         dtype [N,H] overwritten;  dW  f32 [V,H] overwritten
+ *   workspace  >= vp_lmhead_ce_workspace_size(..., pass 2, c) for some chunk c
+ * Errors as for the other calls; nothing is launched on an argument error.
+ */
+vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int64_t* targets,
+                               const float* dloss,
+                               int64_t N, int64_t H, int64_t V, int T,
+                               int64_t ignore_index, vp_dtype dtype,
+                               float* loss, float* lse, float* loss_mean,
+                               float* shard_stats, int32_t* n_bad,
+                               void* dX, float* dW,
+                               void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * vp_read_device_status -- synchronise `stream` and copy the device status

@@ -89,4 +89,35 @@ def test_workspace_sizes(lib):
     c = vp.workspace_size(N, H, V, T, vp.VP_BF16, 1, 16032)
     assert c >= N * 15872 * 2 + N * H * 4                              # chunk rounded to 256, + fp32 dX partial
     assert vp.workspace_size(N, H, V, 7, vp.VP_BF16, 1) == 0           # V % T != 0
-    assert vp.workspace_size(6, 64, 16, 4, vp.VP_F32, 2) == 0          # unknown pass
+    assert vp.workspace_size(6, 64, 16, 4, vp.VP_F32, 3) == 0          # unknown pass
+
+
+def test_fused_workspace_sizes(lib):
+    N, H, V, T = 16384, 4096, 128256, 8
+    full = vp.workspace_size(N, H, V, T, vp.VP_BF16, 2)
+    # fp16 p / bf16 dZ [N, V] + per tile and token: 2 (m, S) slots, the tile max; + z_y, g
+    body = N * V * 2 + 501 * N * (2 * 8 + 4) + 2 * N * 4
+    assert body <= full < body + 8192
+    half = vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 8192)
+    assert half < full / 2 + N * 8 and half > full / 2 - N * V
+    assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 100) == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 128)
+    # fp32: the larger of the split forward and backward
+    f32 = vp.workspace_size(6, 64, 16, 4, vp.VP_F32, 2)
+    assert f32 == max(vp.workspace_size(6, 64, 16, 4, vp.VP_F32, 0), vp.workspace_size(6, 64, 16, 4, vp.VP_F32, 1))
+
+
+def test_fused_rejects_bad_arguments(lib):
+    X, W, y, ws = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
+    loss, lse, dX, dW = P(0x50000), P(0x60000), P(0x70000), P(0x80000)
+    f = lib.vp_lmhead_ce_fwd_bwd
+
+    def call(N=300, H=64, V=1000, T=4, dt=vp.VP_BF16, X=X, dX=dX, dW=dW, wsb=1 << 30):
+        return f(X, W, y, None, N, H, V, T, -100, dt, loss, lse, None, None, None, dX, dW, ws, wsb, None)
+    assert call(T=3) == 1                    # V % T != 0
+    assert call(dX=None) == 1
+    assert call(dW=None) == 1
+    assert call(X=P(0x10008)) == 2           # X not 16-byte aligned
+    assert call(dX=P(0x70008)) == 2
+    assert call(H=60) == 2                   # H * 2 bytes not a multiple of 16
+    assert call(wsb=4096) == 3               # no token chunk fits
+    assert call(dt=vp.VP_F32, wsb=64) == 3

@@ -23,13 +23,20 @@ def _free():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("path", ["split", "fused"])
 @pytest.mark.parametrize("name", ["v32k", "v128k", "v152k"])
-def test_fullsize_sampled_rows(name):
+def test_fullsize_sampled_rows(name, path):
+    """``split``: vp_lmhead_ce_fwd + vp_lmhead_ce_bwd; ``fused``:
+    vp_lmhead_ce_fwd_bwd (the call the bench times), all tokens in one chunk."""
     inp = synth.make_inputs(name)
     wl = inp.wl
     X, W, y = dev_inputs(inp)
-    f = vp.lmhead_ce_fwd(X, W, y, wl.T)
-    dX, dW = vp.lmhead_ce_bwd(X, W, y, f["lse"], wl.T)
+    if path == "split":
+        f = vp.lmhead_ce_fwd(X, W, y, wl.T)
+        dX, dW = vp.lmhead_ce_bwd(X, W, y, f["lse"], wl.T)
+    else:
+        f = vp.lmhead_ce_fwd_bwd(X, W, y, wl.T)
+        dX, dW = f["dX"], f["dW"]
     torch.cuda.synchronize()
     assert vp.read_device_status(f["workspace"]) == 0
     valid = (inp.targets >= 0) & (inp.targets < wl.V)
@@ -57,13 +64,18 @@ def test_fullsize_sampled_rows(name):
     assert abs(a - b) <= 2e-2 * max(abs(a), abs(b)) + 1e-6, (a, b)
 
 
-def test_v32k_shape_full_gradients():
+@pytest.mark.parametrize("path", ["split", "fused"])
+def test_v32k_shape_full_gradients(path):
     """H=4096, V=32000, T=4 with 512 tokens: every loss and every dX/dW entry."""
     inp = synth.make_inputs("v32k", N=512)
     wl = inp.wl
     X, W, y = dev_inputs(inp)
-    f = vp.lmhead_ce_fwd(X, W, y, wl.T, shard_stats=True)
-    dX, dW = vp.lmhead_ce_bwd(X, W, y, f["lse"], wl.T)
+    if path == "split":
+        f = vp.lmhead_ce_fwd(X, W, y, wl.T, shard_stats=True)
+        dX, dW = vp.lmhead_ce_bwd(X, W, y, f["lse"], wl.T)
+    else:
+        f = vp.lmhead_ce_fwd_bwd(X, W, y, wl.T, shard_stats=True)
+        dX, dW = f["dX"], f["dW"]
     torch.cuda.synchronize()
     o = ref.lmhead_ce_forward(inp.X, inp.W, inp.targets, wl.V, wl.T)
     assert_loss_close(np64(f["loss"]), o["loss"], "bf16", scale=o["lse"])

@@ -8,6 +8,7 @@ no fallback: without the built ``libvp.so`` every call raises.
     out = embed_fwd(ids, W, T)
     fwd = lmhead_ce_fwd(X, W, targets, T, ignore_index=-100)   # loss, lse, mean ...
     dX, dW = lmhead_ce_bwd(X, W, targets, fwd["lse"], T)
+    out = lmhead_ce_fwd_bwd(X, W, targets, T)                   # both, probabilities saved
     loss = lmhead_ce(X, W, targets, T)                          # autograd wrapper
 """
 from __future__ import annotations
@@ -17,7 +18,7 @@ import os
 
 import torch
 
-__all__ = ["embed_fwd", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce", "workspace_size", "read_device_status",
+__all__ = ["embed_fwd", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce_fwd_bwd", "lmhead_ce", "workspace_size", "read_device_status",
            "test_gemm_bf16", "set_gemm_variant", "stage_timing_enable", "stage_timing_read", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
 
 VP_F32, VP_BF16 = 0, 1
@@ -58,6 +59,8 @@ def _load():
     L.vp_lmhead_ce_fwd.argtypes = [P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, P, P, P, SZ, P]
     L.vp_lmhead_ce_bwd.restype = I32
     L.vp_lmhead_ce_bwd.argtypes = [P, P, P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, SZ, P]
+    L.vp_lmhead_ce_fwd_bwd.restype = I32
+    L.vp_lmhead_ce_fwd_bwd.argtypes = [P, P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, P, P, P, P, P, SZ, P]
     L.vp_read_device_status.restype = I32
     L.vp_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     L.vp_test_gemm_bf16.restype = I32
@@ -194,6 +197,49 @@ def lmhead_ce_bwd(X, W, targets, lse, T, ignore_index=IGNORE_INDEX, dloss=None, 
         _stream(dev))
     _check("vp_lmhead_ce_bwd", code)
     return dX, dW
+
+
+def lmhead_ce_fwd_bwd(X, W, targets, T, ignore_index=IGNORE_INDEX, dloss=None, shard_stats=False, token_chunk=None,
+                      workspace=None, out=None) -> dict:
+    """Forward and backward in one call (probabilities saved, no logit
+    recompute).  Returns the forward's loss, lse, mean, n_bad (and
+    shard_stats if asked) plus dX (X's dtype) and dW (fp32) of the mean loss,
+    or of sum_n dloss[n] * loss[n] when dloss is given."""
+    _need(X, "X")
+    _need(W, "W", X.dtype, X.device)
+    _need(targets, "targets", torch.int64, X.device)
+    if dloss is not None:
+        _need(dloss, "dloss", torch.float32, X.device)
+    N, H = X.shape
+    V = W.shape[0]
+    dev = X.device
+    if out is None:
+        out = {"loss": torch.empty(N, dtype=torch.float32, device=dev),
+               "lse": torch.empty(N, dtype=torch.float32, device=dev),
+               "mean": torch.empty(1, dtype=torch.float32, device=dev),
+               "n_bad": torch.empty(1, dtype=torch.int32, device=dev),
+               "dX": torch.empty_like(X),
+               "dW": torch.empty((V, H), dtype=torch.float32, device=dev)}
+        if shard_stats:
+            out["shard_stats"] = torch.empty((T, 3, N), dtype=torch.float32, device=dev)
+    _need(out["dX"], "dX", X.dtype, dev)
+    _need(out["dW"], "dW", torch.float32, dev)
+    if workspace is None:
+        ws_bytes = workspace_size(N, H, V, T, _dtype_code(X), 2, token_chunk or 0)
+        if ws_bytes == 0:
+            raise VpError("vp_lmhead_ce_workspace_size", 1)
+        ws = _workspace(ws_bytes, dev, None)
+    else:
+        # the library picks the largest token chunk the given bytes hold (VP_ERR_WORKSPACE if none)
+        ws = workspace
+        ws_bytes = ws.numel() * ws.element_size()
+    code = _load().vp_lmhead_ce_fwd_bwd(
+        _ptr(X), _ptr(W), _ptr(targets), _ptr(dloss), N, H, V, T, ignore_index, _dtype_code(X), _ptr(out["loss"]),
+        _ptr(out["lse"]), _ptr(out.get("mean")), _ptr(out.get("shard_stats")), _ptr(out.get("n_bad")),
+        _ptr(out["dX"]), _ptr(out["dW"]), _ptr(ws), ws_bytes, _stream(dev))
+    _check("vp_lmhead_ce_fwd_bwd", code)
+    out["workspace"] = ws
+    return out
 
 
 def read_device_status(workspace: torch.Tensor) -> int:

@@ -5,11 +5,15 @@
 //                vocab tile, the local max m and sum exp(z - m), plus the
 //                target logit when the tile owns the target ("Vocab
 //                Parallelism" sec. 5.3.1; interview note figure 2).
+//   EpiLseStatsP the same statistics, plus the tile's probabilities relative
+//                to its row maximum, kept in fp16 for the fused backward (the
+//                saved-probability backward of sec. 5.3.2).
 //   EpiDZ        backward: recomputed logits -> dZ = g (exp(z - lse) - 1[j=y])
 //                stored as bf16 for one vocab chunk (sec. 5.3.2).
 //   EpiStore     dX / dW: fp32 accumulator -> fp32 store, fp32 read-add-store,
 //                or bf16 store (optionally adding an fp32 partial first).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "umma_gemm.cuh"
@@ -27,17 +31,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 // ------------------------------------------------------------------ forward
-struct EpiLseStats {
-  static constexpr uint32_t kStagingBytes = 0;
+// kStoreP = false: statistics only (the split forward; logits never stored).
+// kStoreP = true (the fused forward + backward): after the statistics pass the
+// epilogue reads the accumulator row a second time and writes
+// p = exp(z - m_tile) in fp16 through TMA, where m_tile is the row's maximum
+// over the tile's valid columns (stored in tmax).  p lies in (0, 1], where fp16
+// carries 11 significant bits, so the later gradient
+// exp(z - lse) = p * exp(m_tile - lse) keeps a relative error near 2^-11.
+template <bool kStoreP>
+struct EpiLseStatsT {
+  static constexpr uint32_t kStagingBytes = kStoreP ? kStoreStagingBytes : 0;
   struct Params {
     float2* partial;          // [num_vtiles * maxseg][N] (m, S)
     float* zy;                // [N] target logit, written by the owning tile
     const int64_t* targets;   // [N]
     int64_t N, V, Vs;         // tokens, vocab, shard width V/T
     int maxseg;               // record slots per vocab tile
+    float* tmax;              // [num_vtiles][N] row maximum of each tile (kStoreP)
   };
-  __device__ static void run(const Params& p, const CUtensorMap*, uint32_t taddr, int64_t n, int nb, EpiCtx&) {
+  __device__ static void run(const Params& p, const CUtensorMap* tm, uint32_t taddr, int64_t n, int nb,
+                             EpiCtx& ctx) {
     const int64_t v0 = static_cast<int64_t>(nb) * kBN;
     const int64_t vend = min(v0 + kBN, p.V);
     const bool row_ok = n < p.N;
@@ -46,7 +65,7 @@ struct EpiLseStats {
     int64_t t = v0 / p.Vs;
     int64_t seg_end = min((t + 1) * p.Vs, vend);
     int k = 0;
-    float m = -INFINITY, s = 0.f, zyv = 0.f;
+    float m = -INFINITY, s = 0.f, zyv = 0.f, tmx = -INFINITY;
     bool have_zy = false;
     float2* rec = p.partial + (static_cast<int64_t>(nb) * p.maxseg) * p.N + n;
 #pragma unroll 1
@@ -70,6 +89,7 @@ struct EpiLseStats {
         float cm = as_f(r[0]);
 #pragma unroll
         for (int q = 1; q < 32; ++q) cm = fmaxf(cm, as_f(r[q]));
+        if (kStoreP) tmx = fmaxf(tmx, cm);
         if (cm > m) {
           s *= ex2_approx((m - cm) * kLog2e);
           m = cm;
@@ -99,6 +119,7 @@ struct EpiLseStats {
             s = 0.f;
           }
           const float z = as_f(r[q]);
+          if (kStoreP) tmx = fmaxf(tmx, z);
           if (z > m) {
             s = s * ex2_approx((m - z) * kLog2e) + 1.f;
             m = z;
@@ -112,8 +133,34 @@ struct EpiLseStats {
       rec[static_cast<int64_t>(k) * p.N] = make_float2(m, s);
       if (have_zy) p.zy[n] = zyv;
     }
+    if constexpr (kStoreP) {
+      if (row_ok) p.tmax[static_cast<int64_t>(nb) * p.N + n] = tmx;
+      const bool warp_live = ctx.row0 < p.N;
+      const float nt = -tmx * kLog2e;
+#pragma unroll 1
+      for (int b = 0; b < kBN / 64; ++b) {
+        const int64_t col0 = v0 + b * 64;
+        if (col0 >= vend) break;
+        uint32_t w[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld32(taddr + b * 64 + h * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 32; q += 2)
+            w[h * 16 + q / 2] = pack_f16x2(ex2_approx(fmaf(as_f(r[q]), kLog2e, nt)),
+                                           ex2_approx(fmaf(as_f(r[q + 1]), kLog2e, nt)));
+        }
+        // columns >= V and rows >= N are clipped by the tensor map
+        if (warp_live) stage_and_store(ctx, tm, w, static_cast<int32_t>(col0));
+      }
+    }
   }
 };
+using EpiLseStats = EpiLseStatsT<false>;
+using EpiLseStatsP = EpiLseStatsT<true>;
 
 // ------------------------------------------------------------------ backward dZ
 // dZ boxes of 32 rows x 64 bf16 columns go out through TMA (the tensor map
@@ -373,8 +420,20 @@ cudaError_t bf16_lse_stats(const void* X, const void* W, const int64_t* targets,
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, X, N, H, H, kBK, kBM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, W, V, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
-  EpiLseStats::Params p{partial, zy, targets, N, V, Vs, maxseg};
+  EpiLseStats::Params p{partial, zy, targets, N, V, Vs, maxseg, nullptr};
   return launch_any<false, false, EpiLseStats>(ta, tb, ta, N, V, H, p, status, stream, 2048);
+}
+
+cudaError_t bf16_lse_stats_p(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H, int64_t V,
+                             int64_t Vs, float2* partial, int maxseg, float* zy, float* tmax, void* P, int64_t ldp,
+                             uint32_t* status, cudaStream_t stream) {
+  CUtensorMap ta, tb, tc;
+  if (!make_tmap_bf16(&ta, X, N, H, H, kBK, kBM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, W, V, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
+  // fp16 boxes of 32 rows x 64 columns (128 bytes), clipped at V columns and N rows
+  if (!make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, P, N, V, ldp, 64, 32)) return cudaErrorInvalidValue;
+  EpiLseStatsP::Params p{partial, zy, targets, N, V, Vs, maxseg, tmax};
+  return launch_any<false, false, EpiLseStatsP>(ta, tb, tc, N, V, H, p, status, stream, 2048);
 }
 
 cudaError_t bf16_dz_chunk(const void* X, const void* W, const int64_t* targets, const float* lse, const float* g,
@@ -404,14 +463,16 @@ cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N,
 }
 
 cudaError_t bf16_dw_chunk(const void* dz, int64_t ldz, const void* X, int64_t N, int64_t H, int64_t c0,
-                          int64_t Vc, float* dW, uint32_t* status, cudaStream_t stream) {
+                          int64_t Vc, float* dW, bool accumulate, uint32_t* status, cudaStream_t stream) {
   // dW_c[Vc,H] = dZ_c^T[Vc,N] * X[N,H]: A = dZ_c viewed as [K=N rows][M=Vc cols]
   // (MN-major), B = X viewed as [K=N rows][N=H cols] (MN-major).
   CUtensorMap ta, tb, tc;
   if (!make_tmap_bf16(&ta, dz, N, Vc, ldz, 64, kBK)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, X, N, H, H, 64, kBK)) return cudaErrorInvalidValue;
-  if (!make_store_tmap(&tc, false, dW + c0 * H, Vc, H, H)) return cudaErrorInvalidValue;
-  EpiStore::Params p{nullptr, H, Vc, H, kStoreF32};
+  // accumulate: dW_c += dZ_c^T X (the sum over token chunks), read and written by the same CTA
+  float* out = dW + c0 * H;
+  if (!make_store_tmap(&tc, false, out, Vc, H, H)) return cudaErrorInvalidValue;
+  EpiStore::Params p{accumulate ? out : nullptr, H, Vc, H, accumulate ? kAddF32 : kStoreF32};
   return launch_any<true, true, EpiStore>(ta, tb, tc, Vc, H, N, p, status, stream, 1024);
 }
 

@@ -31,7 +31,7 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2)
 __global__ void lse_merge_kernel(const float2* __restrict__ partial, const float* __restrict__ zy,
                                  const int64_t* __restrict__ targets, int64_t N, int64_t V, int64_t Vs, int T,
                                  int tile_v, int maxseg, int64_t ignore_index, float* __restrict__ loss,
-                                 float* __restrict__ lse, float* __restrict__ shard_stats) {
+                                 float* __restrict__ lse, float* __restrict__ shard_stats, int64_t ss_ld) {
   const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (n >= N) return;
   const int64_t y = targets[n];
@@ -48,9 +48,9 @@ __global__ void lse_merge_kernel(const float2* __restrict__ partial, const float
       merge_ms(mt, st, r.x, r.y);
     }
     if (shard_stats) {
-      shard_stats[(static_cast<int64_t>(t) * 3 + 0) * N + n] = mt;
-      shard_stats[(static_cast<int64_t>(t) * 3 + 1) * N + n] = st;
-      shard_stats[(static_cast<int64_t>(t) * 3 + 2) * N + n] = (valid && y >= a && y < b) ? zyn : 0.f;
+      shard_stats[(static_cast<int64_t>(t) * 3 + 0) * ss_ld + n] = mt;
+      shard_stats[(static_cast<int64_t>(t) * 3 + 1) * ss_ld + n] = st;
+      shard_stats[(static_cast<int64_t>(t) * 3 + 2) * ss_ld + n] = (valid && y >= a && y < b) ? zyn : 0.f;
     }
     merge_ms(m, s, mt, st);
   }
@@ -125,14 +125,21 @@ __global__ void __launch_bounds__(kRedThreads) upstream_scale_kernel(const int64
 
 }  // namespace
 
+cudaError_t lse_merge_ld(const float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
+                         int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
+                         float* shard_stats, int64_t ss_ld, cudaStream_t stream) {
+  const int threads = 256;
+  const int64_t blocks = (N + threads - 1) / threads;
+  lse_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      partial, zy, targets, N, V, Vs, T, tile_v, maxseg, ignore_index, loss, lse, shard_stats, ss_ld);
+  return cudaGetLastError();
+}
+
 cudaError_t lse_merge(const float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
                       int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
                       float* shard_stats, cudaStream_t stream) {
-  const int threads = 256;
-  const int64_t blocks = (N + threads - 1) / threads;
-  lse_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(partial, zy, targets, N, V, Vs, T, tile_v,
-                                                                          maxseg, ignore_index, loss, lse, shard_stats);
-  return cudaGetLastError();
+  return lse_merge_ld(partial, zy, targets, N, V, Vs, T, tile_v, maxseg, ignore_index, loss, lse, shard_stats, N,
+                      stream);
 }
 
 cudaError_t loss_mean_and_bad(const float* loss, const int64_t* targets, int64_t N, int64_t V, int64_t ignore_index,

@@ -90,12 +90,47 @@ int64_t bwd_chunk_from_ws(int64_t N, int64_t H, int64_t V, vp_dtype dt, size_t w
   return vc >= tile || vc == V ? vc : 0;
 }
 
+// ---------------- fused workspace (bf16), token chunk Nc:
+// header | g [N] | records [ntiles*maxseg][Nc] | z_y [Nc] | tmax [ntiles][Nc] | P, then dZ, [Nc][ldp] 2-byte
+struct FusedLayout {
+  int64_t Nc, ldp, ntiles;
+  int maxseg;
+  size_t off_g, off_partial, off_zy, off_tmax, off_p, total;
+};
+FusedLayout fused_layout(int64_t N, int64_t V, int T, int64_t Nc) {
+  FusedLayout L;
+  L.Nc = Nc;
+  L.ldp = (V + 7) / 8 * 8;
+  L.ntiles = (V + kBf16TileV - 1) / kBf16TileV;
+  L.maxseg = lse_maxseg(V, V / T, T);
+  L.off_g = kHeader;
+  L.off_partial = align_up(L.off_g + size_t(N) * sizeof(float), kAlign);
+  L.off_zy = align_up(L.off_partial + size_t(L.ntiles) * L.maxseg * Nc * sizeof(float2), kAlign);
+  L.off_tmax = align_up(L.off_zy + size_t(Nc) * sizeof(float), kAlign);
+  L.off_p = align_up(L.off_tmax + size_t(L.ntiles) * Nc * sizeof(float), kAlign);
+  L.total = align_up(L.off_p + size_t(Nc) * L.ldp * 2, kAlign);
+  return L;
+}
+constexpr int64_t kFusedRowAlign = 128;   // token chunks are whole 128-row GEMM blocks
+// Largest token chunk that fits in ws bytes: all N, else a multiple of 128 (0 if none fits).
+int64_t fused_chunk_from_ws(int64_t N, int64_t V, int T, size_t ws) {
+  if (fused_layout(N, V, T, N).total <= ws) return N;
+  const size_t per_row = fused_layout(N, V, T, 2).total - fused_layout(N, V, T, 1).total;
+  const size_t fixed = fused_layout(N, V, T, 0).total;
+  if (ws < fixed || per_row == 0) return 0;
+  int64_t nc = int64_t((ws - fixed) / per_row) / kFusedRowAlign * kFusedRowAlign;
+  if (nc >= N) nc = (N - 1) / kFusedRowAlign * kFusedRowAlign;
+  while (nc >= kFusedRowAlign && fused_layout(N, V, T, nc).total > ws) nc -= kFusedRowAlign;
+  return nc >= kFusedRowAlign ? nc : 0;
+}
+
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 // ---------------- optional per-launch event timing (vp_stage_timing_enable)
-enum Stage { kEmbed, kLseGemm, kMerge, kMean, kScale, kDzGemm, kDwGemm, kDxGemm, kNumStages };
-const char* const kStageNames[kNumStages] = {"embed_gather", "lse_stats_gemm", "lse_merge",  "loss_mean",
-                                             "upstream_scale", "dz_recompute_gemm", "dw_gemm", "dx_gemm"};
+enum Stage { kEmbed, kLseGemm, kMerge, kMean, kScale, kDzGemm, kDwGemm, kDxGemm, kLsePGemm, kDzFromP, kNumStages };
+const char* const kStageNames[kNumStages] = {"embed_gather",   "lse_stats_gemm",    "lse_merge", "loss_mean",
+                                             "upstream_scale", "dz_recompute_gemm", "dw_gemm",   "dx_gemm",
+                                             "lse_p_gemm",     "dz_from_p"};
 struct StageTimer {
   int cap = 0, used = 0;
   cudaEvent_t* ev = nullptr;  // 2 per launch
@@ -148,6 +183,20 @@ VP_EXPORT size_t vp_lmhead_ce_workspace_size(int64_t N, int64_t H, int64_t V, in
                                              int64_t vocab_chunk) {
   if (!dtype_ok(dtype) || !shape_ok(N, H, V, T)) return 0;
   if (pass == 0) return fwd_layout(N, V, T, dtype).total;
+  if (pass == 2 && dtype == VP_BF16) {
+    int64_t nc = N;
+    if (vocab_chunk > 0 && vocab_chunk < N) {
+      nc = vocab_chunk / kFusedRowAlign * kFusedRowAlign;
+      if (nc < kFusedRowAlign) nc = kFusedRowAlign;
+      if (nc > N) nc = N;
+    }
+    return fused_layout(N, V, T, nc).total;
+  }
+  if (pass == 2) {   // fp32: the forward, then the recompute backward in the same bytes
+    const size_t f = fwd_layout(N, V, T, dtype).total;
+    const size_t b = vp_lmhead_ce_workspace_size(N, H, V, T, dtype, 1, vocab_chunk);
+    return f > b ? f : b;
+  }
   if (pass != 1) return 0;
   int64_t vc = V;
   if (vocab_chunk > 0 && vocab_chunk < V) {
@@ -159,11 +208,18 @@ VP_EXPORT size_t vp_lmhead_ce_workspace_size(int64_t N, int64_t H, int64_t V, in
   return bwd_layout_for_chunk(N, H, V, dtype, vc).total;
 }
 
-static vp_status check_common(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H, int64_t V,
-                              int T, vp_dtype dtype, const void* ws) {
+static vp_status check_args(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H, int64_t V,
+                            int T, vp_dtype dtype, const void* ws) {
   if (!X || !W || !targets || !ws || !dtype_ok(dtype) || !shape_ok(N, H, V, T)) return VP_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(W) || !aligned16(ws) || (H * esize_of(dtype)) % 16 != 0) return VP_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(targets) & 7u) != 0) return VP_ERR_UNSUPPORTED;
+  return VP_OK;
+}
+
+static vp_status check_common(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H, int64_t V,
+                              int T, vp_dtype dtype, const void* ws) {
+  vp_status st = check_args(X, W, targets, N, H, V, T, dtype, ws);
+  if (st != VP_OK) return st;
   if (dtype == VP_BF16 && !tensor_map_encoder()) return VP_ERR_CUDA;
   return VP_OK;
 }
@@ -227,7 +283,7 @@ VP_EXPORT vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t
     if (dtype == VP_BF16) {
       e = timed(kDzGemm, s, [&] { return bf16_dz_chunk(X, W, targets, lse, g, N, H, c0, vc, dz, L.ldz, status, s); });
       if (e == cudaSuccess)
-        e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(dz, L.ldz, X, N, H, c0, vc, dW, status, s); });
+        e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(dz, L.ldz, X, N, H, c0, vc, dW, false, status, s); });
       if (e == cudaSuccess) {
         // dX over chunks: bf16 store (one chunk), else fp32 store / fp32 add / bf16 = fp32 partial + last
         void* out = (single || last) ? dX : static_cast<void*>(acc);
@@ -251,6 +307,68 @@ VP_EXPORT vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t
         });
     }
   }
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int64_t* targets, const float* dloss,
+                                         int64_t N, int64_t H, int64_t V, int T, int64_t ignore_index,
+                                         vp_dtype dtype, float* loss, float* lse, float* loss_mean,
+                                         float* shard_stats, int32_t* n_bad, void* dX, float* dW, void* workspace,
+                                         size_t ws_bytes, void* stream) {
+  if (!loss || !lse || !dX || !dW) return VP_ERR_INVALID_ARG;
+  vp_status st = check_args(X, W, targets, N, H, V, T, dtype, workspace);
+  if (st != VP_OK) return st;
+  if (!aligned16(dX) || !aligned16(dW)) return VP_ERR_UNSUPPORTED;
+  if (dtype == VP_F32) {
+    // CUDA-core fp32 path: the forward, then the recompute backward, both in this workspace
+    if (ws_bytes < fwd_layout(N, V, T, dtype).total || bwd_chunk_from_ws(N, H, V, dtype, ws_bytes) <= 0)
+      return VP_ERR_WORKSPACE;
+    st = vp_lmhead_ce_fwd(X, W, targets, N, H, V, T, ignore_index, dtype, loss, lse, loss_mean, shard_stats, n_bad,
+                          workspace, ws_bytes, stream);
+    if (st != VP_OK) return st;
+    return vp_lmhead_ce_bwd(X, W, targets, lse, dloss, N, H, V, T, ignore_index, dtype, dX, dW, workspace, ws_bytes,
+                            stream);
+  }
+  const int64_t Nc = fused_chunk_from_ws(N, V, T, ws_bytes);
+  if (Nc <= 0) return VP_ERR_WORKSPACE;
+  if (!tensor_map_encoder()) return VP_ERR_CUDA;
+  const FusedLayout L = fused_layout(N, V, T, Nc);
+  cudaStream_t s = as_stream(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  float* g = reinterpret_cast<float*>(ws + L.off_g);
+  float2* partial = reinterpret_cast<float2*>(ws + L.off_partial);
+  float* zy = reinterpret_cast<float*>(ws + L.off_zy);
+  float* tmax = reinterpret_cast<float*>(ws + L.off_tmax);
+  void* P = ws + L.off_p;
+  const int64_t Vs = V / T;
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = timed(kScale, s, [&] { return upstream_scale(targets, dloss, N, V, ignore_index, g, s); });
+  for (int64_t n0 = 0; n0 < N && e == cudaSuccess; n0 += Nc) {
+    const int64_t nc = (N - n0) < Nc ? (N - n0) : Nc;
+    const void* Xc = static_cast<const uint8_t*>(X) + n0 * H * 2;
+    const int64_t* yc = targets + n0;
+    e = timed(kLsePGemm, s, [&] {
+      return bf16_lse_stats_p(Xc, W, yc, nc, H, V, Vs, partial, L.maxseg, zy, tmax, P, L.ldp, status, s);
+    });
+    if (e == cudaSuccess)
+      e = timed(kMerge, s, [&] {
+        return lse_merge_ld(partial, zy, yc, nc, V, Vs, T, kBf16TileV, L.maxseg, ignore_index, loss + n0, lse + n0,
+                            shard_stats ? shard_stats + n0 : nullptr, N, s);
+      });
+    if (e == cudaSuccess)
+      e = timed(kDzFromP, s, [&] { return dz_from_p(P, L.ldp, tmax, lse + n0, g + n0, yc, nc, V, s); });
+    // dW = sum over token chunks of dZ_c^T X_c; dX rows of this chunk are complete
+    if (e == cudaSuccess)
+      e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(P, L.ldp, Xc, nc, H, 0, V, dW, n0 > 0, status, s); });
+    if (e == cudaSuccess)
+      e = timed(kDxGemm, s, [&] {
+        return bf16_dx_chunk(P, L.ldp, W, nc, H, 0, V, static_cast<uint8_t*>(dX) + n0 * H * 2, nullptr, 3, status,
+                             s);
+      });
+  }
+  if (e == cudaSuccess && (loss_mean || n_bad))
+    e = timed(kMean, s, [&] { return loss_mean_and_bad(loss, targets, N, V, ignore_index, loss_mean, n_bad, s); });
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
 }
 

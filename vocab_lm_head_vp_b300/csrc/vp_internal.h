@@ -25,7 +25,12 @@ cudaError_t bf16_dz_chunk(const void* X, const void* W, const int64_t* targets, 
 cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N, int64_t H, int64_t c0, int64_t Vc,
                           void* out, const float* partial, int mode, uint32_t* status, cudaStream_t stream);
 cudaError_t bf16_dw_chunk(const void* dz, int64_t ldz, const void* X, int64_t N, int64_t H, int64_t c0, int64_t Vc,
-                          float* dW, uint32_t* status, cudaStream_t stream);
+                          float* dW, bool accumulate, uint32_t* status, cudaStream_t stream);
+// Forward statistics plus p = exp(z - tile row max) in fp16 into P [N][ldp]
+// and the tile row maxima into tmax [num_vtiles][N].
+cudaError_t bf16_lse_stats_p(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H, int64_t V,
+                             int64_t Vs, float2* partial, int maxseg, float* zy, float* tmax, void* P, int64_t ldp,
+                             uint32_t* status, cudaStream_t stream);
 cudaError_t bf16_gemm_test(const void* A, const void* B, float* D, int64_t M, int64_t Ncols, int64_t K, int a_mn,
                            int b_mn, uint32_t* status, cudaStream_t stream);
 // 1: tcgen05 GEMMs run as 2-SM CTA pairs (256 x 256 tiles); 0 (default): one SM per 128 x 256 tile.
@@ -47,6 +52,14 @@ int f32_maxseg(int64_t V, int64_t Vs, int T);
 cudaError_t lse_merge(const float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
                       int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
                       float* shard_stats, cudaStream_t stream);
+// The same, for a block of N rows whose shard_stats rows sit in a [T][3][ss_ld] array.
+cudaError_t lse_merge_ld(const float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
+                         int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
+                         float* shard_stats, int64_t ss_ld, cudaStream_t stream);
+// In place: P [N][ldp] fp16 probabilities relative to the tile row maxima ->
+// dZ bf16 = g (p exp(tmax - lse) - 1[j = y]).
+cudaError_t dz_from_p(void* P, int64_t ldp, const float* tmax, const float* lse, const float* g,
+                      const int64_t* targets, int64_t N, int64_t V, cudaStream_t stream);
 cudaError_t loss_mean_and_bad(const float* loss, const int64_t* targets, int64_t N, int64_t V, int64_t ignore_index,
                               float* loss_mean, int32_t* n_bad, cudaStream_t stream);
 cudaError_t upstream_scale(const int64_t* targets, const float* dloss, int64_t N, int64_t V, int64_t ignore_index,
