@@ -53,9 +53,35 @@ def parse_args():
     p.add_argument("--path", choices=["fused", "split"], default="fused",
                    help="fused: one fwd+bwd call with saved probabilities; split: fwd, then bwd with recompute")
     p.add_argument("--other-path-steps", type=int, default=5, help="timed steps of the other path (0: skip)")
+    p.add_argument("--embed-iters", type=int, default=20, help="launches per case of the gather microbench (0: skip)")
     p.add_argument("--gemm-variant", choices=["pair", "single"], default="single",
                    help="tcgen05 GEMM form: 256x256 tiles on SM pairs, or 128x256 tiles on one SM")
     return p.parse_args()
+
+
+# DRAM bytes (read + write) per launch of the tcgen05 GEMM kernel in the fused
+# v128k step, from one ncu capture (profiles/launches_fused_step_v128k.md: mean of
+# the three GEMM launches of two steps).  They describe the kernel built from the
+# sources hashed here; once those change, `traffic` is reported as null until a
+# new capture replaces the number.
+GEMM_TRAFFIC = {"workload": "v128k", "path": "fused", "gemm_variant": "single", "bytes_per_launch": 25.33e9,
+                "by_launch": {"lse_p_gemm": 12.82e9, "dw_gemm": 25.00e9, "dx_gemm": 38.16e9},
+                "sources": ("vocab_lm_head_vp_b300/csrc/ce_bf16.cu", "vocab_lm_head_vp_b300/csrc/ptx.cuh",
+                            "vocab_lm_head_vp_b300/csrc/umma_gemm.cuh"),
+                "sha256": "c78af5847690e828ce1b521d07e9ba392abbbb90791927711c5edf5d318ce3e7"}
+
+
+def gemm_traffic(workload, path, variant):
+    """ncu DRAM bytes per GEMM launch if they were taken on this kernel and step, else None."""
+    import hashlib
+    t = GEMM_TRAFFIC
+    if (workload, path, variant) != (t["workload"], t["path"], t["gemm_variant"]):
+        return None
+    h = hashlib.sha256()
+    for f in t["sources"]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return t["bytes_per_launch"] if h.hexdigest() == t["sha256"] else None
 
 
 def load_peaks():
@@ -174,6 +200,23 @@ def oracle_tokens_per_s(inp, budget_s):
     return n / t, n, t
 
 
+def embed_roofline(in_step_gbs, micro, peaks):
+    """The gather's bandwidth: the uniform-id V128k launch with L2 flushed is the
+    headline (no row repeats); the Zipf and V152k cases and the in-step figure
+    (event overhead included, L2 warm) are reported beside it."""
+    r = {"kernel": "embed_gather_kernel", "bound": "hbm", "unit": "GB/s", "peak": peaks["hbm_gbs"],
+         "in_step_gbs": in_step_gbs}
+    if micro:
+        a = micro["v128k_uniform"]["GB/s"]
+        r.update({"achieved": a, "frac": a / peaks["hbm_gbs"], "frac_of_8TBs": a / 8000.0,
+                  "workload": "v128k shape (N=16384, H=4096, V=128256), uniform ids, L2 flushed before each launch",
+                  "cases": micro})
+    else:
+        r.update({"achieved": in_step_gbs, "frac": in_step_gbs / peaks["hbm_gbs"],
+                  "workload": "in-step launch, Zipf ids (repeated rows hit in L2)"})
+    return r
+
+
 def cores_used():
     try:
         return len(os.sched_getaffinity(0))
@@ -219,6 +262,41 @@ def workload_config(wl):
             "l2": ("no flush: inputs larger than L2 (W %.2f GB, X %.0f MB; L2 126 MB)" if wl.V * wl.H * 2 > 126e6
                    else "inputs fit in L2 (W %.2f GB, X %.0f MB); no flush") % (wl.V * wl.H * 2 / 1e9,
                                                                                  wl.N * wl.H * 2 / 1e6)}
+
+
+# ------------------------------------------------------------------ embedding gather alone
+def embed_microbench(vp, dev, iters=20):
+    """vp_embed_fwd timed launch by launch (CUDA events on the launching
+    stream) at the V128k and V152k shapes, uniform and Zipf(1.1) ids, with the
+    L2 flushed (a 256 MB write) before every launch.  Algorithmic bytes per
+    launch: read N rows + write N rows + N int64 ids."""
+    import torch
+    import synth
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    for name in ("v128k", "v152k"):
+        wl = synth.WORKLOADS[name]
+        g = torch.Generator(device=dev).manual_seed(wl.seed)
+        W = torch.randn(wl.V, wl.H, generator=g, device=dev).to(torch.bfloat16)
+        o = torch.empty((wl.N, wl.H), dtype=torch.bfloat16, device=dev)
+        rng = np.random.default_rng(wl.seed)
+        for kind, ids in (("uniform", rng.integers(0, wl.V, wl.N)), ("zipf", synth.zipf_ids(rng, wl.N, wl.V, 1.1))):
+            idt = torch.from_numpy(ids).to(dev)
+            times = []
+            for i in range(iters + 3):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                vp.embed_fwd(idt, W, wl.T, out=o)
+                e1.record()
+                torch.cuda.synchronize()
+                if i >= 3:
+                    times.append(e0.elapsed_time(e1))
+            ms = statistics.median(times)
+            nbytes = 2.0 * wl.N * wl.H * 2 + 8.0 * wl.N
+            out[f"{name}_{kind}"] = {"N": wl.N, "H": wl.H, "V": wl.V, "ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9}
+        del W, o
+    return out
 
 
 # ------------------------------------------------------------------ our arm
@@ -324,6 +402,8 @@ def run_ours(args):
     assert all(vp.read_device_status(w) == 0 for w in workspaces)
     del workspaces, step
 
+    emb_micro = embed_microbench(vp, dev) if args.embed_iters > 0 else None
+
     # ---------------- the other path, briefly (reported beside, not in `value`)
     other = None
     if args.other_path_steps > 0:
@@ -364,6 +444,12 @@ def run_ours(args):
     emb_ms, emb_n = stages["embed_gather"]
     emb_bytes = 2.0 * N * H * 2 + 8.0 * N
     emb_gbs = emb_bytes / (emb_ms / max(1, emb_n) / 1e3) / 1e9
+    # operands once + outputs once, averaged over the step's GEMM launches
+    lse_b = N * H * 2 + V * H * 2 + (N * V * 2 if args.path == "fused" else 0)
+    dz_b = N * H * 2 + V * H * 2 + N * V * 2               # split path's recompute launch
+    dw_b = N * V * 2 + N * H * 2 + V * H * 4
+    dx_b = N * V * 2 + V * H * 2 + N * H * 2
+    gemm_alg_bytes = ((lse_b + dw_b + dx_b) / 3 if args.path == "fused" else (lse_b + dz_b + dw_b + dx_b) / 4)
     extra = {}
     if args.path == "fused":
         dzp_ms, dzp_n = stages["dz_from_p"]
@@ -390,10 +476,11 @@ def run_ours(args):
                      "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops_sustained"],
                      "peak_kind": f"bf16 sustained ({peaks['source']})",
-                     "frac_of_burst": achieved / peaks["bf16_tflops"], "traffic": None},
-        "roofline_embed": {"kernel": "embed_gather_kernel", "bound": "hbm", "achieved": emb_gbs,
-                           "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": emb_gbs / peaks["hbm_gbs"],
-                           "note": "Zipf ids repeat rows (L2 hits)"},
+                     "frac_of_burst": achieved / peaks["bf16_tflops"],
+                     "traffic": gemm_traffic(wl.name, args.path, args.gemm_variant),
+                     "traffic_unit": "bytes per launch (ncu dram read + write)",
+                     "algorithmic_bytes_per_launch": gemm_alg_bytes},
+        "roofline_embed": embed_roofline(emb_gbs, emb_micro, peaks),
         **extra,
         "stages_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in stages.items() if v[1]},
         "gpu_launches": launches,
