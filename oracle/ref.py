@@ -12,7 +12,8 @@ exact float64 values of their bf16 bit patterns.
 Sources (page title, section):
   [VP-book]  MiniMind-tron book, ch. 5 "Vocab Parallelism":
              sec. 5.2.1 Vocab Parallel Embedding (shard ranges, masked lookup,
-             the V=8 worked table), sec. 5.3.1 forward (max-shifted CE, the three
+             the V=8 worked table), sec. 5.2.2 (embedding and LM head tied to
+             one parameter), sec. 5.3.1 forward (max-shifted CE, the three
              [B,S] statistics), sec. 5.3.2 backward (p - onehot, local),
              sec. 5.3.3 ignore_index (mean over valid tokens).
   [VP-note]  "Vocab parallelism: how to split embedding and LM head" (interview
@@ -77,6 +78,40 @@ def embed(ids: np.ndarray, W: np.ndarray, V: int, T: int) -> np.ndarray:
     for t in range(T):
         acc = acc + embed_shard_partial(ids, W, V, T, t)
     return acc
+
+
+# --------------------------------------------------------------------------
+# Embedding backward  ([VP-book] sec. 5.2.1 masked lookup; sec. 5.2.2 the
+# embedding and the LM head share one [V,H] parameter, so its gradient is the
+# sum of both layers' gradients)
+# --------------------------------------------------------------------------
+def embed_shard_grad(ids: np.ndarray, dOut: np.ndarray, V: int, T: int, t: int) -> np.ndarray:
+    """Gradient of shard t's masked local lookup with respect to its slice W_t,
+    taking the lookup's steps backwards: the zeroing of masked output rows
+    passes them no gradient, and the gather of local rows adds each remaining
+    token's upstream row into local row id - start (token order)."""
+    start, end = shard_bounds(V, T)[t]
+    ids = np.asarray(ids, dtype=np.int64)
+    g = np.array(dOut, dtype=np.float64)
+    mask = (ids < start) | (ids >= end)
+    local = ids - start
+    local[mask] = 0
+    g[mask] = 0.0                                   # backward of "output[mask] = 0"
+    dW_t = np.zeros((end - start, g.shape[1]), dtype=np.float64)
+    np.add.at(dW_t, local, g)                       # backward of "W_t[local]"
+    return dW_t
+
+
+def embed_backward(ids: np.ndarray, dOut: np.ndarray, V: int, T: int, dW0=None) -> np.ndarray:
+    """Gradient of the summed shard outputs with respect to the tied weight
+    W [V,H].  The forward's sum over shards hands every shard the same upstream
+    rows dOut, so shard t's slice gradient fills rows [tV/T, (t+1)V/T).  With
+    dW0 (the tied weight's other gradient, the LM head's) the two are added."""
+    H = np.asarray(dOut).shape[1]
+    dW = np.zeros((V, H), dtype=np.float64) if dW0 is None else np.array(dW0, dtype=np.float64)
+    for t, (start, end) in enumerate(shard_bounds(V, T)):
+        dW[start:end] += embed_shard_grad(ids, dOut, V, T, t)
+    return dW
 
 
 # --------------------------------------------------------------------------

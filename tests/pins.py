@@ -256,7 +256,84 @@ def pin_rows_variant(o):
     np.testing.assert_allclose(r["dX"], b["dX"][rows], rtol=1e-12, atol=1e-15)
 
 
+# ---------------------------------------------------------------- embedding backward
+def pin_embed_bwd_worked_table(o):
+    """Backward of the V=8, T=2, ids [1,6] table (sec. 5.2.1): position n's
+    output row is the weight row the table's SUM line names, so its upstream
+    row lands in that weight row and nowhere else -- not in the local row 0
+    (global rows 0 and 4) that the masked positions looked up."""
+    g = read("embed_v8_t2_ids_1_6.txt")
+    V, T = int(g["V"][0]), int(g["T"][0])
+    ids = np.array([int(v) for v in g["ids"]])
+    G = np.random.default_rng(6).standard_normal((len(ids), 3)) + 10.0
+    want = np.zeros((V, 3))
+    for n, s in enumerate(g["sum"]):
+        if s != "0":
+            want[int(s[1:])] += G[n]
+    assert np.array_equal(o.embed_backward(ids, G, V, T), want)
+
+
+def pin_embed_bwd_adjoint(o):
+    """<embed(ids, W), G> = <W, embed_backward(ids, G)> for random W, G: the
+    backward is the adjoint of the (separately pinned) forward, for every
+    T | V, with out-of-range ids and repeated ids."""
+    rng = np.random.default_rng(12)
+    V, H, N = 24, 7, 40
+    ids = rng.integers(-3, V + 3, N)
+    ids[:6] = [0, 0, 6, 6, V - 1, 12]
+    W = rng.standard_normal((V, H))
+    G = rng.standard_normal((N, H))
+    for T in (1, 2, 3, 4, 6, 8, 12, 24):
+        lhs = float((o.embed(ids, W, V, T) * G).sum())
+        dW = o.embed_backward(ids, G, V, T)
+        rhs = float((W * dW).sum())
+        assert abs(lhs - rhs) <= 1e-12 * (np.abs(G).sum() * np.abs(W).max()), (T, lhs, rhs)
+        # rows no valid id names (local row 0 of a shard included) get nothing
+        assert not dW[np.setdiff1d(np.arange(V), ids)].any(), T
+
+
+def pin_embed_bwd_library(o):
+    """torch.nn.functional.embedding's autograd (float64, CPU) on the valid ids
+    equals the oracle for every T, and a given dW0 is added (the tied weight)."""
+    rng = np.random.default_rng(13)
+    V, H, N = 30, 5, 64
+    ids = rng.integers(0, V, N)
+    ids[:10] = 3                                   # a heavily repeated id
+    ids[10:13] = [-1, V, -100]                     # out of range: no gradient
+    G = rng.standard_normal((N, H))
+    valid = (ids >= 0) & (ids < V)
+    W = torch.zeros((V, H), dtype=torch.float64, requires_grad=True)
+    out = torch.nn.functional.embedding(torch.from_numpy(ids[valid]), W)
+    out.backward(torch.from_numpy(G[valid]))
+    want = W.grad.numpy()
+    D = rng.standard_normal((V, H))
+    for T in (1, 2, 3, 5, 6, 10, 15, 30):
+        np.testing.assert_allclose(o.embed_backward(ids, G, V, T), want, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(o.embed_backward(ids, G, V, T, dW0=D), want + D, rtol=0, atol=1e-12)
+
+
+def pin_embed_bwd_finite_differences(o):
+    """Central differences of L(W) = sum <embed(ids, W), G> in every weight
+    entry (L is linear, so they are exact up to rounding)."""
+    rng = np.random.default_rng(14)
+    V, H, N, T = 8, 3, 11, 4
+    ids = rng.integers(-1, V + 1, N)
+    W = rng.standard_normal((V, H))
+    G = rng.standard_normal((N, H))
+    dW = o.embed_backward(ids, G, V, T)
+    h = 0.5
+    for v in range(V):
+        for c in range(H):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[v, c] += h
+            Wm[v, c] -= h
+            fd = ((o.embed(ids, Wp, V, T) * G).sum() - (o.embed(ids, Wm, V, T) * G).sum()) / (2 * h)
+            assert abs(fd - dW[v, c]) <= 1e-12, (v, c, fd, dW[v, c])
+
+
 ALL_PINS = [pin_embed_worked_table, pin_embed_figure1, pin_embed_brute_force,
+            pin_embed_bwd_worked_table, pin_embed_bwd_adjoint, pin_embed_bwd_library,
+            pin_embed_bwd_finite_differences,
             pin_ce_library, pin_ce_closed_form, pin_ce_ignore_and_bad,
             pin_shard_invariance, pin_page_t4_simulation,
             pin_grad_library, pin_grad_finite_differences, pin_rows_variant]

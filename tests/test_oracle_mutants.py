@@ -68,6 +68,33 @@ def _embed_no_mask(ids, W, V, T, t):
     return W_t[local]                                                 # zeroing step dropped
 
 
+def _embed_bwd_keep_masked(ids, dOut, V, T, t):
+    start, end = ref.shard_bounds(V, T)[t]
+    ids = np.asarray(ids, dtype=np.int64)
+    local = np.where((ids < start) | (ids >= end), 0, ids - start)
+    dW_t = np.zeros((end - start, np.asarray(dOut).shape[1]))
+    np.add.at(dW_t, local, np.asarray(dOut, dtype=np.float64))     # masked rows not zeroed
+    return dW_t
+
+
+def _embed_bwd_assign(ids, dOut, V, T, t):
+    start, end = ref.shard_bounds(V, T)[t]
+    ids = np.asarray(ids, dtype=np.int64)
+    keep = (ids >= start) & (ids < end)
+    dW_t = np.zeros((end - start, np.asarray(dOut).shape[1]))
+    dW_t[ids[keep] - start] = np.asarray(dOut, dtype=np.float64)[keep]   # repeats overwrite, not add
+    return dW_t
+
+
+def _embed_bwd_global_row(ids, dOut, V, T, t):
+    start, end = ref.shard_bounds(V, T)[t]
+    ids = np.asarray(ids, dtype=np.int64)
+    keep = (ids >= start) & (ids < end)
+    dW_t = np.zeros((end - start, np.asarray(dOut).shape[1]))
+    np.add.at(dW_t, np.clip(ids[keep], 0, end - start - 1), np.asarray(dOut, dtype=np.float64)[keep])  # no "- start"
+    return dW_t
+
+
 _ORIG = {k: getattr(ref, k) for k in ("cross_entropy", "merge_local_stats")}
 
 MUTANTS = {
@@ -78,6 +105,9 @@ MUTANTS = {
     "mean_scale_over_N": ("upstream_scale", _scale_by_n),
     "merge_no_rescale": ("merge_local_stats", _merge_no_rescale),
     "embed_no_mask": ("embed_shard_partial", _embed_no_mask),
+    "embed_bwd_keep_masked_rows": ("embed_shard_grad", _embed_bwd_keep_masked),
+    "embed_bwd_assign_not_add": ("embed_shard_grad", _embed_bwd_assign),
+    "embed_bwd_global_row": ("embed_shard_grad", _embed_bwd_global_row),
 }
 
 
