@@ -299,6 +299,42 @@ def embed_microbench(vp, dev, iters=20):
     return out
 
 
+def embed_bwd_microbench(vp, dev, iters=20):
+    """vp_embed_bwd (accumulate into the tied weight's fp32 gradient) at the
+    V128k shape with the workload's Zipf ids and with uniform ids, L2 flushed
+    before every launch.  Algorithmic bytes: read dOut (N x H bf16) and the
+    ids, read and write every touched fp32 row of dW once."""
+    import torch
+    import synth
+    wl = synth.WORKLOADS["v128k"]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    g = torch.Generator(device=dev).manual_seed(wl.seed)
+    G = torch.randn(wl.N, wl.H, generator=g, device=dev).to(torch.bfloat16)
+    dW = torch.zeros((wl.V, wl.H), dtype=torch.float32, device=dev)
+    ws = torch.empty(vp._load().vp_embed_bwd_workspace_size(wl.N, wl.H, wl.V, wl.T, vp.VP_BF16),
+                     dtype=torch.uint8, device=dev)
+    rng = np.random.default_rng(wl.seed)
+    out = {}
+    for kind, ids in (("zipf", synth.zipf_ids(rng, wl.N, wl.V, 1.1)), ("uniform", rng.integers(0, wl.V, wl.N))):
+        idt = torch.from_numpy(ids).to(dev)
+        times = []
+        for i in range(iters + 3):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            vp.embed_bwd(idt, G, wl.V, wl.T, dW=dW, accumulate=True, workspace=ws)
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        distinct = len(np.unique(ids))
+        nbytes = wl.N * wl.H * 2.0 + 8.0 * wl.N + 2.0 * distinct * wl.H * 4
+        out[kind] = {"ms": ms, "distinct_ids": distinct, "alg_bytes": nbytes, "GB/s": nbytes / (ms / 1e3) / 1e9}
+    del G, dW, ws
+    return out
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args):
     import torch
@@ -403,6 +439,7 @@ def run_ours(args):
     del workspaces, step
 
     emb_micro = embed_microbench(vp, dev) if args.embed_iters > 0 else None
+    emb_bwd_micro = embed_bwd_microbench(vp, dev) if args.embed_iters > 0 else None
 
     # ---------------- the other path, briefly (reported beside, not in `value`)
     other = None
@@ -481,6 +518,10 @@ def run_ours(args):
                      "traffic_unit": "bytes per launch (ncu dram read + write)",
                      "algorithmic_bytes_per_launch": gemm_alg_bytes},
         "roofline_embed": embed_roofline(emb_gbs, emb_micro, peaks),
+        "embed_bwd": None if emb_bwd_micro is None else {
+            "kernel": "vp_embed_bwd (key sort + run sums + cross-run sums), accumulate into fp32 dW",
+            "workload": "v128k shape, L2 flushed before each launch", "bound": "hbm", "unit": "GB/s",
+            "peak": peaks["hbm_gbs"], "cases": emb_bwd_micro},
         **extra,
         "stages_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in stages.items() if v[1]},
         "gpu_launches": launches,

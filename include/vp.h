@@ -84,6 +84,35 @@ vp_status vp_embed_fwd(const int64_t* ids, const void* W, void* out,
                        void* stream);
 
 /*
+ * vp_embed_bwd -- backward of vp_embed_fwd into the tied weight's gradient.
+ *
+ * "Vocab Parallelism" sec. 5.2.1: shard t's lookup zeroes the output rows of
+ * ids outside its range, so those rows pass it no gradient, and the gather
+ * adds every other token's upstream row into local row id - t*V/T.  Summed
+ * over the shards (each sees the same upstream rows, the forward's sum being
+ * an all-reduce), weight row v receives the rows of exactly the tokens with
+ * id v.  Sec. 5.2.2 ties the embedding and the LM head to one parameter, so
+ * its gradient is the sum of both layers': pass the LM head's dW (from
+ * vp_lmhead_ce_bwd or vp_lmhead_ce_fwd_bwd) with accumulate = 1.
+ *     dW[v,:] = (accumulate ? dW[v,:] : 0) + sum_{n: ids[n] = v} dOut[n,:]
+ * in fp32; ids outside [0,V) contribute nothing.  Deterministic: no atomics;
+ * each row's sum runs over its tokens in increasing n in runs of 32 sorted
+ * positions, the run sums added in order, then added to the existing row.
+ *
+ *   ids       int64 [N]
+ *   dOut      dtype [N,H]    upstream gradient of the embedding output
+ *   dW        f32 [V,H]      accumulate != 0: added to; 0: overwritten
+ *                            (rows no token names are set to zero)
+ *   workspace >= vp_embed_bwd_workspace_size(N, H, V, T, dtype) bytes,
+ *             16-byte aligned (sort keys and per-run partial sums)
+ * Requires H*sizeof(dtype) % 16 == 0 and 16-byte aligned dOut, dW.
+ */
+size_t vp_embed_bwd_workspace_size(int64_t N, int64_t H, int64_t V, int T, vp_dtype dtype);
+vp_status vp_embed_bwd(const int64_t* ids, const void* dOut, float* dW,
+                       int64_t N, int64_t H, int64_t V, int T, vp_dtype dtype,
+                       int accumulate, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * vp_lmhead_ce_workspace_size -- bytes of device workspace for a call.
  *   pass 0: vp_lmhead_ce_fwd (exact size needed).
  *   pass 1: vp_lmhead_ce_bwd with the vocab processed in chunks of

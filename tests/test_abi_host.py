@@ -121,3 +121,18 @@ def test_fused_rejects_bad_arguments(lib):
     assert call(H=60) == 2                   # H * 2 bytes not a multiple of 16
     assert call(wsb=4096) == 3               # no token chunk fits
     assert call(dt=vp.VP_F32, wsb=64) == 3
+
+
+def test_embed_bwd_rejects_bad_arguments(lib):
+    ids, G, dW, ws = P(0x1000), P(0x2000), P(0x3000), P(0x4000)
+    f = lib.vp_embed_bwd
+    nb = lib.vp_embed_bwd_workspace_size(100, 64, 1000, 4, vp.VP_BF16)
+    # sort keys (next power of two of N) + two partial sums of H floats per 32-token run
+    assert nb >= 128 * 8 + 2 * 4 * 64 * 4
+    assert lib.vp_embed_bwd_workspace_size(100, 64, 1000, 3, vp.VP_BF16) == 0     # V % T != 0
+    assert f(ids, G, dW, 100, 64, 1000, 3, vp.VP_BF16, 0, ws, nb, None) == 1
+    assert f(None, G, dW, 100, 64, 1000, 4, vp.VP_BF16, 0, ws, nb, None) == 1
+    assert f(ids, P(0x2008), dW, 100, 64, 1000, 4, vp.VP_BF16, 0, ws, nb, None) == 2
+    assert f(ids, G, P(0x3004), 100, 64, 1000, 4, vp.VP_BF16, 0, ws, nb, None) == 2
+    assert f(ids, G, dW, 100, 60, 1000, 4, vp.VP_BF16, 0, ws, nb, None) == 2   # H*2 % 16 != 0
+    assert f(ids, G, dW, 100, 64, 1000, 4, vp.VP_BF16, 0, ws, 64, None) == 3

@@ -18,7 +18,7 @@ import os
 
 import torch
 
-__all__ = ["embed_fwd", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce_fwd_bwd", "lmhead_ce", "workspace_size", "read_device_status",
+__all__ = ["embed_fwd", "embed_bwd", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce_fwd_bwd", "lmhead_ce", "workspace_size", "read_device_status",
            "test_gemm_bf16", "set_gemm_variant", "stage_timing_enable", "stage_timing_read", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
 
 VP_F32, VP_BF16 = 0, 1
@@ -53,6 +53,10 @@ def _load():
     L.vp_version.restype = ctypes.c_char_p
     L.vp_embed_fwd.restype = I32
     L.vp_embed_fwd.argtypes = [P, P, P, I64, I64, I64, I32, I32, P]
+    L.vp_embed_bwd_workspace_size.restype = SZ
+    L.vp_embed_bwd_workspace_size.argtypes = [I64, I64, I64, I32, I32]
+    L.vp_embed_bwd.restype = I32
+    L.vp_embed_bwd.argtypes = [P, P, P, I64, I64, I64, I32, I32, I32, P, SZ, P]
     L.vp_lmhead_ce_workspace_size.restype = SZ
     L.vp_lmhead_ce_workspace_size.argtypes = [I64, I64, I64, I32, I32, I32, I64]
     L.vp_lmhead_ce_fwd.restype = I32
@@ -136,6 +140,30 @@ def embed_fwd(ids: torch.Tensor, W: torch.Tensor, T: int, out: torch.Tensor | No
     _check("vp_embed_fwd", _load().vp_embed_fwd(_ptr(ids), _ptr(W), _ptr(out), N, H, V, T, _dtype_code(W),
                                                 _stream(W.device)))
     return out
+
+
+def embed_bwd(ids: torch.Tensor, dOut: torch.Tensor, V: int, T: int, dW: torch.Tensor | None = None,
+              accumulate: bool = False, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """dW[v] (+)= sum of dOut[n] over tokens with ids[n] = v (fp32 [V,H]);
+    with accumulate=True it adds onto dW (the tied weight's LM-head gradient)."""
+    _need(dOut, "dOut")
+    _need(ids, "ids", torch.int64, dOut.device)
+    N, H = dOut.shape
+    dev = dOut.device
+    if dW is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs dW")
+        dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    _need(dW, "dW", torch.float32, dev)
+    L = _load()
+    nb = int(L.vp_embed_bwd_workspace_size(N, H, V, T, _dtype_code(dOut)))
+    if nb == 0:
+        raise VpError("vp_embed_bwd_workspace_size", 1)
+    ws = _workspace(nb, dev, workspace)
+    _check("vp_embed_bwd", L.vp_embed_bwd(_ptr(ids), _ptr(dOut), _ptr(dW), N, H, V, T, _dtype_code(dOut),
+                                          int(bool(accumulate)), _ptr(ws), ws.numel() * ws.element_size(),
+                                          _stream(dev)))
+    return dW
 
 
 def lmhead_ce_fwd(X, W, targets, T, ignore_index=IGNORE_INDEX, shard_stats=False, workspace=None,

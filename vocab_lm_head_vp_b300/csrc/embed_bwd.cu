@@ -1,0 +1,289 @@
+// Vocab-parallel embedding backward: the gradient of the masked shard lookup
+// ("Vocab Parallelism" sec. 5.2.1) with respect to the tied weight, added to
+// the LM head's gradient of the same parameter (sec. 5.2.2: embedding and LM
+// head share one [V,H] weight, so its gradient is the sum of both layers').
+//
+// Shard t's lookup zeroes the output rows of ids outside its range, so those
+// rows pass no gradient; every other token adds its upstream row dOut[n] into
+// weight row id_n.  Summed over shards, each valid id's row receives exactly
+// the upstream rows of the tokens carrying it:
+//     dW[v,:] (+)= sum over n with id_n = v, in increasing n, of dOut[n,:]
+// (fp32 accumulation; ids outside [0,V) contribute nothing).
+//
+// Deterministic, no atomics:
+//   1. keys (id << 32 | n) for valid ids, all-ones for the rest and the
+//      padding, bitonic-sorted: blocks sort 4096-key chunks in shared memory,
+//      longer merges take one global pass per step above the chunk and finish
+//      in shared memory.  The sorted order groups tokens by id, by n within.
+//   2. runs of kRun sorted positions: one thread per 16-byte column vector of
+//      the row walks the run in order and sums; a segment (one id) that starts
+//      and ends inside the run is added to dW at once, a segment cut by the
+//      run's edge leaves its partial sum in a head or tail slot of the run.
+//   3. the run that holds the start of a cut segment adds its tail, then the
+//      head slots of the following runs up to the one where the segment ends,
+//      in run order, and adds the total to dW.
+// A row's sum is therefore taken in token order within runs of kRun sorted
+// positions and over runs in order: the same bits on every call.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "vp_internal.h"
+
+namespace vp {
+namespace {
+
+constexpr uint64_t kSentinel = ~0ull;
+constexpr uint32_t kNoId = 0xffffffffu;
+constexpr int kChunk = 4096;          // keys sorted per block in shared memory
+constexpr int kSortThreads = 1024;
+constexpr int kRun = 32;              // sorted positions per run
+constexpr int kRedThreads = 256;
+
+__device__ __forceinline__ uint32_t key_id(uint64_t k) { return static_cast<uint32_t>(k >> 32); }
+
+__global__ void make_keys_kernel(const int64_t* __restrict__ ids, int64_t N, int64_t V, uint64_t* __restrict__ keys,
+                                 int64_t n_pad) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n_pad) return;
+  uint64_t k = kSentinel;
+  if (i < N) {
+    const int64_t id = ids[i];
+    if (id >= 0 && id < V) k = (static_cast<uint64_t>(id) << 32) | static_cast<uint64_t>(i);
+  }
+  keys[i] = k;
+}
+
+// Compare-exchange step j of merge size k on `len` keys in shared memory whose
+// first key has global index gbase.  Pair p -> (i, i + j).
+__device__ __forceinline__ void smem_step(uint64_t* s, int len, int64_t gbase, int64_t k, int j) {
+  for (int p = threadIdx.x; p < len / 2; p += blockDim.x) {
+    const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
+    const int l = i + j;
+    const bool asc = ((gbase + i) & k) == 0;
+    const uint64_t a = s[i], b = s[l];
+    if ((a > b) == asc) {
+      s[i] = b;
+      s[l] = a;
+    }
+  }
+  __syncthreads();
+}
+
+// Full bitonic sort of each chunk of len = min(kChunk, n_pad) keys, merge sizes 2..len.
+__global__ void __launch_bounds__(kSortThreads) bitonic_chunk_sort(uint64_t* __restrict__ keys, int len) {
+  __shared__ uint64_t s[kChunk];
+  const int64_t gbase = static_cast<int64_t>(blockIdx.x) * len;
+  for (int i = threadIdx.x; i < len; i += blockDim.x) s[i] = keys[gbase + i];
+  __syncthreads();
+  for (int k = 2; k <= len; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) smem_step(s, len, gbase, k, j);
+  for (int i = threadIdx.x; i < len; i += blockDim.x) keys[gbase + i] = s[i];
+}
+
+// Steps j = kChunk/2 .. 1 of merge size k (> kChunk) inside each chunk.
+__global__ void __launch_bounds__(kSortThreads) bitonic_chunk_merge(uint64_t* __restrict__ keys, int64_t k) {
+  __shared__ uint64_t s[kChunk];
+  const int64_t gbase = static_cast<int64_t>(blockIdx.x) * kChunk;
+  for (int i = threadIdx.x; i < kChunk; i += blockDim.x) s[i] = keys[gbase + i];
+  __syncthreads();
+  for (int j = kChunk >> 1; j > 0; j >>= 1) smem_step(s, kChunk, gbase, k, j);
+  for (int i = threadIdx.x; i < kChunk; i += blockDim.x) keys[gbase + i] = s[i];
+}
+
+// One global step (j >= kChunk) of merge size k: a thread per pair.
+__global__ void bitonic_global_step(uint64_t* __restrict__ keys, int64_t n_pad, int64_t k, int64_t j) {
+  const int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (p >= n_pad / 2) return;
+  const int64_t i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
+  const int64_t l = i + j;
+  const bool asc = (i & k) == 0;
+  const uint64_t a = keys[i], b = keys[l];
+  if ((a > b) == asc) {
+    keys[i] = b;
+    keys[l] = a;
+  }
+}
+
+// 16 bytes of an upstream row as fp32 values: 8 bf16 or 4 f32.
+template <int ESIZE>
+struct Vec {
+  static constexpr int kN = 16 / ESIZE;
+  float v[kN];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int q = 0; q < kN; ++q) v[q] = 0.f;
+  }
+  __device__ __forceinline__ void add(const uint4& u) {
+    if constexpr (ESIZE == 2) {
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[2 * q] += __uint_as_float(w[q] << 16);
+        v[2 * q + 1] += __uint_as_float(w[q] & 0xffff0000u);
+      }
+    } else {
+      v[0] += __uint_as_float(u.x);
+      v[1] += __uint_as_float(u.y);
+      v[2] += __uint_as_float(u.z);
+      v[3] += __uint_as_float(u.w);
+    }
+  }
+};
+
+// dst[0..kN) += v (fp32, 16-byte aligned)
+template <int ESIZE>
+__device__ __forceinline__ void add_to(float* dst, const Vec<ESIZE>& a) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int q = 0; q < Vec<ESIZE>::kN / 4; ++q) {
+    float4 x = d[q];
+    x.x += a.v[4 * q];
+    x.y += a.v[4 * q + 1];
+    x.z += a.v[4 * q + 2];
+    x.w += a.v[4 * q + 3];
+    d[q] = x;
+  }
+}
+template <int ESIZE>
+__device__ __forceinline__ void store_to(float* dst, const Vec<ESIZE>& a) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int q = 0; q < Vec<ESIZE>::kN / 4; ++q)
+    d[q] = make_float4(a.v[4 * q], a.v[4 * q + 1], a.v[4 * q + 2], a.v[4 * q + 3]);
+}
+
+__device__ __forceinline__ uint64_t key_at(const uint64_t* keys, int64_t n_pad, int64_t i) {
+  return (i >= 0 && i < n_pad) ? keys[i] : kSentinel;
+}
+
+// Phase 2: grid (runs, column blocks); thread = one 16-byte vector column of H.
+template <int ESIZE>
+__global__ void __launch_bounds__(kRedThreads)
+    embed_bwd_runs_kernel(const uint64_t* __restrict__ keys, int64_t n_pad, const uint4* __restrict__ dOut,
+                          int64_t rowvec, float* __restrict__ dW, int64_t H, float* __restrict__ head,
+                          float* __restrict__ tail) {
+  __shared__ uint64_t sk[kRun + 2];
+  const int64_t r = blockIdx.x;
+  const int64_t p0 = r * kRun;
+  for (int i = threadIdx.x; i < kRun + 2; i += blockDim.x) sk[i] = key_at(keys, n_pad, p0 - 1 + i);
+  __syncthreads();
+  const int64_t v = static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x;
+  if (v >= rowvec || key_id(sk[1]) == kNoId) return;
+  constexpr int kN = Vec<ESIZE>::kN;
+  const int64_t col = v * kN;   // first fp32 column of this vector
+  uint32_t cur = key_id(sk[1]);
+  bool start_inside = key_id(sk[0]) != cur;
+  Vec<ESIZE> acc;
+  acc.zero();
+  int i = 0;
+#pragma unroll 1
+  for (int i0 = 0; i0 < kRun; i0 += 8) {
+    uint4 buf[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint64_t k = sk[1 + i0 + u];
+      buf[u] = key_id(k) != kNoId ? __ldg(dOut + static_cast<int64_t>(k & 0xffffffffu) * rowvec + v)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t id = key_id(sk[1 + i0 + u]);
+      if (id == kNoId) break;
+      if (id != cur) {   // the segment of `cur` ended inside this run
+        if (start_inside)
+          add_to<ESIZE>(dW + static_cast<int64_t>(cur) * H + col, acc);
+        else
+          store_to<ESIZE>(head + r * H + col, acc);
+        cur = id;
+        start_inside = true;
+        acc.zero();
+      }
+      acc.add(buf[u]);
+      i = i0 + u + 1;
+    }
+    if (i < i0 + 8) break;   // reached the sentinels
+  }
+  const bool ends_inside = key_id(sk[1 + i]) != cur;
+  if (start_inside && ends_inside)
+    add_to<ESIZE>(dW + static_cast<int64_t>(cur) * H + col, acc);
+  else if (!start_inside)
+    store_to<ESIZE>(head + r * H + col, acc);   // continued from an earlier run (it may run on past this one)
+  else
+    store_to<ESIZE>(tail + r * H + col, acc);   // starts here and continues into the next run
+}
+
+// Phase 3: the run holding the start of a segment cut at its end adds the
+// segment's partials in run order.
+template <int ESIZE>
+__global__ void __launch_bounds__(kRedThreads)
+    embed_bwd_cross_kernel(const uint64_t* __restrict__ keys, int64_t n_pad, int64_t runs, int64_t rowvec,
+                           float* __restrict__ dW, int64_t H, const float* __restrict__ head,
+                           const float* __restrict__ tail) {
+  const int64_t r = blockIdx.x;
+  const int64_t last = (r + 1) * kRun - 1;
+  const uint32_t id = key_id(key_at(keys, n_pad, last));
+  if (id == kNoId || key_id(key_at(keys, n_pad, last + 1)) != id) return;   // nothing continues past run r
+  if (key_id(key_at(keys, n_pad, r * kRun - 1)) == id) return;              // the segment started earlier
+  const int64_t v = static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x;
+  if (v >= rowvec) return;
+  constexpr int kN = Vec<ESIZE>::kN;
+  const int64_t col = v * kN;
+  float s[kN];
+#pragma unroll
+  for (int q = 0; q < kN; ++q) s[q] = tail[r * H + col + q];
+  for (int64_t r2 = r + 1; r2 < runs; ++r2) {
+#pragma unroll
+    for (int q = 0; q < kN; ++q) s[q] += head[r2 * H + col + q];
+    if (key_id(key_at(keys, n_pad, (r2 + 1) * kRun)) != id) break;   // the segment ends in run r2
+  }
+  Vec<ESIZE> a;
+#pragma unroll
+  for (int q = 0; q < kN; ++q) a.v[q] = s[q];
+  add_to<ESIZE>(dW + static_cast<int64_t>(id) * H + col, a);
+}
+
+int64_t pad_pow2(int64_t n) {
+  int64_t p = 2;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+size_t embed_bwd_workspace(int64_t N, int64_t H) {
+  const int64_t runs = (N + kRun - 1) / kRun;
+  return size_t(pad_pow2(N)) * sizeof(uint64_t) + 2 * size_t(runs) * H * sizeof(float);
+}
+
+cudaError_t embed_bwd(const int64_t* ids, const void* dOut, float* dW, int64_t N, int64_t H, int64_t V, int esize,
+                      bool accumulate, void* workspace, cudaStream_t stream) {
+  const int64_t n_pad = pad_pow2(N);
+  const int64_t runs = (N + kRun - 1) / kRun;
+  uint64_t* keys = static_cast<uint64_t*>(workspace);
+  float* head = reinterpret_cast<float*>(keys + n_pad);
+  float* tail = head + runs * H;
+  cudaError_t e = cudaSuccess;
+  if (!accumulate) e = cudaMemsetAsync(dW, 0, size_t(V) * H * sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  make_keys_kernel<<<static_cast<unsigned>((n_pad + 255) / 256), 256, 0, stream>>>(ids, N, V, keys, n_pad);
+  const int len = static_cast<int>(n_pad < kChunk ? n_pad : kChunk);
+  bitonic_chunk_sort<<<static_cast<unsigned>(n_pad / len), kSortThreads, 0, stream>>>(keys, len);
+  for (int64_t k = 2 * kChunk; k <= n_pad; k <<= 1) {
+    for (int64_t j = k >> 1; j >= kChunk; j >>= 1)
+      bitonic_global_step<<<static_cast<unsigned>((n_pad / 2 + 255) / 256), 256, 0, stream>>>(keys, n_pad, k, j);
+    bitonic_chunk_merge<<<static_cast<unsigned>(n_pad / kChunk), kSortThreads, 0, stream>>>(keys, k);
+  }
+  const int64_t rowvec = H * esize / 16;
+  const dim3 grid(static_cast<unsigned>(runs), static_cast<unsigned>((rowvec + kRedThreads - 1) / kRedThreads));
+  const uint4* src = static_cast<const uint4*>(dOut);
+  if (esize == 2) {
+    embed_bwd_runs_kernel<2><<<grid, kRedThreads, 0, stream>>>(keys, n_pad, src, rowvec, dW, H, head, tail);
+    embed_bwd_cross_kernel<2><<<grid, kRedThreads, 0, stream>>>(keys, n_pad, runs, rowvec, dW, H, head, tail);
+  } else {
+    embed_bwd_runs_kernel<4><<<grid, kRedThreads, 0, stream>>>(keys, n_pad, src, rowvec, dW, H, head, tail);
+    embed_bwd_cross_kernel<4><<<grid, kRedThreads, 0, stream>>>(keys, n_pad, runs, rowvec, dW, H, head, tail);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace vp

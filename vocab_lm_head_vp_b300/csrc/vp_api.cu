@@ -127,10 +127,12 @@ int64_t fused_chunk_from_ws(int64_t N, int64_t V, int T, size_t ws) {
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 // ---------------- optional per-launch event timing (vp_stage_timing_enable)
-enum Stage { kEmbed, kLseGemm, kMerge, kMean, kScale, kDzGemm, kDwGemm, kDxGemm, kLsePGemm, kDzFromP, kNumStages };
+enum Stage {
+  kEmbed, kLseGemm, kMerge, kMean, kScale, kDzGemm, kDwGemm, kDxGemm, kLsePGemm, kDzFromP, kEmbedBwd, kNumStages
+};
 const char* const kStageNames[kNumStages] = {"embed_gather",   "lse_stats_gemm",    "lse_merge", "loss_mean",
                                              "upstream_scale", "dz_recompute_gemm", "dw_gemm",   "dx_gemm",
-                                             "lse_p_gemm",     "dz_from_p"};
+                                             "lse_p_gemm",     "dz_from_p",         "embed_bwd"};
 struct StageTimer {
   int cap = 0, used = 0;
   cudaEvent_t* ev = nullptr;  // 2 per launch
@@ -176,6 +178,25 @@ VP_EXPORT vp_status vp_embed_fwd(const int64_t* ids, const void* W, void* out, i
   if ((reinterpret_cast<uintptr_t>(ids) & 7u) != 0) return VP_ERR_UNSUPPORTED;
   cudaStream_t s = as_stream(stream);
   cudaError_t e = timed(kEmbed, s, [&] { return embed_gather(ids, W, out, N, H, V, V / T, T, es, s); });
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+VP_EXPORT size_t vp_embed_bwd_workspace_size(int64_t N, int64_t H, int64_t V, int T, vp_dtype dtype) {
+  if (!dtype_ok(dtype) || !shape_ok(N, H, V, T)) return 0;
+  return align_up(embed_bwd_workspace(N, H), kAlign);
+}
+
+VP_EXPORT vp_status vp_embed_bwd(const int64_t* ids, const void* dOut, float* dW, int64_t N, int64_t H, int64_t V,
+                                 int T, vp_dtype dtype, int accumulate, void* workspace, size_t ws_bytes,
+                                 void* stream) {
+  if (!ids || !dOut || !dW || !workspace || !dtype_ok(dtype) || !shape_ok(N, H, V, T)) return VP_ERR_INVALID_ARG;
+  const int es = esize_of(dtype);
+  if (!aligned16(dOut) || !aligned16(dW) || !aligned16(workspace) || (H * es) % 16 != 0) return VP_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(ids) & 7u) != 0) return VP_ERR_UNSUPPORTED;
+  if (ws_bytes < embed_bwd_workspace(N, H)) return VP_ERR_WORKSPACE;
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e =
+      timed(kEmbedBwd, s, [&] { return embed_bwd(ids, dOut, dW, N, H, V, es, accumulate != 0, workspace, s); });
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
 }
 

@@ -69,4 +69,9 @@ cudaError_t upstream_scale(const int64_t* targets, const float* dloss, int64_t N
 cudaError_t embed_gather(const int64_t* ids, const void* W, void* out, int64_t N, int64_t H, int64_t V,
                          int64_t Vs, int T, int esize, cudaStream_t stream);
 
+// ---- embedding backward (embed_bwd.cu)
+size_t embed_bwd_workspace(int64_t N, int64_t H);
+cudaError_t embed_bwd(const int64_t* ids, const void* dOut, float* dW, int64_t N, int64_t H, int64_t V, int esize,
+                      bool accumulate, void* workspace, cudaStream_t stream);
+
 }  // namespace vp
