@@ -3,9 +3,10 @@
 // lse_merge: the on-device form of the pages' cross-shard reductions ("Vocab
 // Parallelism" sec. 5.3.1; "Vocab parallelism: how to split embedding and LM
 // head", figure 2 and key formulas).  For token n, the per-tile records
-// (m, S) of shard t are merged into the shard's (m_t, S_t); the shards then
-// merge into m = max_t m_t, S = sum_t S_t e^(m_t - m), lse = m + log S, and
-// loss = lse - z_y for a valid target (0 otherwise).
+// (m, S) of shard t are merged into the shard's (m_t, S_t) (one thread per
+// token and shard); the shards then merge into m = max_t m_t,
+// S = sum_t S_t e^(m_t - m), lse = m + log S, and loss = lse - z_y for a
+// valid target, 0 otherwise (one thread per token, shards in order).
 //
 // loss_mean_and_bad: L = sum_n loss_n / max(1, N_valid) (sec. 5.3.3) and the
 // count of targets that are neither ignore_index nor inside [0, V).
@@ -28,6 +29,34 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2)
   }
 }
 
+// Slot of shard t's first tile: where the shard's merged (m_t, S_t) is left.
+__device__ __forceinline__ int64_t shard_slot(int t, int64_t Vs, int tile_v, int maxseg) {
+  const int64_t nb = static_cast<int64_t>(t) * Vs / tile_v;
+  const int k = t - static_cast<int>((nb * tile_v) / Vs);
+  return nb * maxseg + k;
+}
+
+// Step 1, one thread per (token, shard): the shard's tile records, in tile
+// order, into (m_t, S_t), written over the record of the shard's first tile
+// (a record slot belongs to exactly one shard, so only this thread touches it).
+__global__ void shard_merge_kernel(float2* __restrict__ partial, int64_t N, int64_t Vs, int T, int tile_v,
+                                   int maxseg) {
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  for (int t = blockIdx.y; t < T; t += gridDim.y) {
+    const int64_t a = static_cast<int64_t>(t) * Vs;
+    const int64_t b = a + Vs;
+    float mt = -INFINITY, st = 0.f;
+    for (int64_t nb = a / tile_v; nb <= (b - 1) / tile_v; ++nb) {
+      const int k = t - static_cast<int>((nb * tile_v) / Vs);   // slot of shard t inside tile nb
+      const float2 r = partial[(nb * maxseg + k) * N + n];
+      merge_ms(mt, st, r.x, r.y);
+    }
+    partial[shard_slot(t, Vs, tile_v, maxseg) * N + n] = make_float2(mt, st);
+  }
+}
+
+// Step 2, one thread per token: the shards in order t = 0..T-1.
 __global__ void lse_merge_kernel(const float2* __restrict__ partial, const float* __restrict__ zy,
                                  const int64_t* __restrict__ targets, int64_t N, int64_t V, int64_t Vs, int T,
                                  int tile_v, int maxseg, int64_t ignore_index, float* __restrict__ loss,
@@ -39,20 +68,14 @@ __global__ void lse_merge_kernel(const float2* __restrict__ partial, const float
   const float zyn = valid ? zy[n] : 0.f;
   float m = -INFINITY, s = 0.f;
   for (int t = 0; t < T; ++t) {
-    const int64_t a = static_cast<int64_t>(t) * Vs;
-    const int64_t b = a + Vs;
-    float mt = -INFINITY, st = 0.f;
-    for (int64_t nb = a / tile_v; nb <= (b - 1) / tile_v; ++nb) {
-      const int k = t - static_cast<int>((nb * tile_v) / Vs);   // slot of shard t inside tile nb
-      const float2 r = partial[(nb * maxseg + k) * N + n];
-      merge_ms(mt, st, r.x, r.y);
-    }
+    const float2 r = partial[shard_slot(t, Vs, tile_v, maxseg) * N + n];
     if (shard_stats) {
-      shard_stats[(static_cast<int64_t>(t) * 3 + 0) * ss_ld + n] = mt;
-      shard_stats[(static_cast<int64_t>(t) * 3 + 1) * ss_ld + n] = st;
-      shard_stats[(static_cast<int64_t>(t) * 3 + 2) * ss_ld + n] = (valid && y >= a && y < b) ? zyn : 0.f;
+      const int64_t a = static_cast<int64_t>(t) * Vs;
+      shard_stats[(static_cast<int64_t>(t) * 3 + 0) * ss_ld + n] = r.x;
+      shard_stats[(static_cast<int64_t>(t) * 3 + 1) * ss_ld + n] = r.y;
+      shard_stats[(static_cast<int64_t>(t) * 3 + 2) * ss_ld + n] = (valid && y >= a && y < a + Vs) ? zyn : 0.f;
     }
-    merge_ms(m, s, mt, st);
+    merge_ms(m, s, r.x, r.y);
   }
   const float l = m + logf(s);
   lse[n] = l;
@@ -125,17 +148,20 @@ __global__ void __launch_bounds__(kRedThreads) upstream_scale_kernel(const int64
 
 }  // namespace
 
-cudaError_t lse_merge_ld(const float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
+cudaError_t lse_merge_ld(float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
                          int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
                          float* shard_stats, int64_t ss_ld, cudaStream_t stream) {
   const int threads = 256;
   const int64_t blocks = (N + threads - 1) / threads;
+  const dim3 grid1(static_cast<unsigned>(blocks), static_cast<unsigned>(T < 65535 ? T : 65535));
+  // the records are scratch of this call: step 1 leaves each shard's merge in one of them
+  shard_merge_kernel<<<grid1, threads, 0, stream>>>(partial, N, Vs, T, tile_v, maxseg);
   lse_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
       partial, zy, targets, N, V, Vs, T, tile_v, maxseg, ignore_index, loss, lse, shard_stats, ss_ld);
   return cudaGetLastError();
 }
 
-cudaError_t lse_merge(const float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
+cudaError_t lse_merge(float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
                       int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
                       float* shard_stats, cudaStream_t stream) {
   return lse_merge_ld(partial, zy, targets, N, V, Vs, T, tile_v, maxseg, ignore_index, loss, lse, shard_stats, N,

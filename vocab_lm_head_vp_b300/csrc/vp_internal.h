@@ -49,11 +49,12 @@ cudaError_t f32_gemm(const float* A, int64_t sam, int64_t sak, const float* B, i
 int f32_maxseg(int64_t V, int64_t Vs, int T);
 
 // ---- merge / prep (merge.cu)
-cudaError_t lse_merge(const float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
+cudaError_t lse_merge(float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
                       int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
                       float* shard_stats, cudaStream_t stream);
 // The same, for a block of N rows whose shard_stats rows sit in a [T][3][ss_ld] array.
-cudaError_t lse_merge_ld(const float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
+// Both leave each shard's merged (m_t, S_t) in one of the records (scratch of the call).
+cudaError_t lse_merge_ld(float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
                          int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
                          float* shard_stats, int64_t ss_ld, cudaStream_t stream);
 // In place: P [N][ldp] fp16 probabilities relative to the tile row maxima ->
