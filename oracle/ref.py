@@ -80,6 +80,22 @@ def embed(ids: np.ndarray, W: np.ndarray, V: int, T: int) -> np.ndarray:
     return acc
 
 
+def embed_sp(ids: np.ndarray, W: np.ndarray, V: int, T: int, rank: int) -> np.ndarray:
+    """Sequence parallelism on ([VP-book] sec. 5.2.1): the T shard partials are
+    reduce-scattered along the token dimension, so rank r keeps token rows
+    [r N/T, (r+1) N/T) of their sum (taken in order t = 0..T-1 from +0.0).
+    N % T must be 0."""
+    ids = np.asarray(ids, dtype=np.int64)
+    N = ids.shape[0]
+    if N % T != 0 or not 0 <= rank < T:
+        raise ValueError(f"reduce-scatter over T={T} ranks needs N % T == 0 and 0 <= rank < T (N={N})")
+    total = np.zeros((N, np.asarray(W).shape[1]), dtype=np.float64)
+    for t in range(T):
+        total = total + embed_shard_partial(ids, W, V, T, t)
+    rows = N // T
+    return total[rank * rows:(rank + 1) * rows]
+
+
 # --------------------------------------------------------------------------
 # Embedding backward  ([VP-book] sec. 5.2.1 masked lookup; sec. 5.2.2 the
 # embedding and the LM head share one [V,H] parameter, so its gradient is the

@@ -256,6 +256,32 @@ def pin_rows_variant(o):
     np.testing.assert_allclose(r["dX"], b["dX"][rows], rtol=1e-12, atol=1e-15)
 
 
+def pin_embed_sp(o):
+    """SP on (sec. 5.2.1, reduce-scatter): with the V=8, T=2, ids [1,6] table,
+    rank 0 keeps token 1's row E1 and rank 1 token 6's row E6; in general the
+    ranks' slices, stacked in rank order, are the SP-off result (all-reduce)."""
+    g = read("embed_v8_t2_ids_1_6.txt")
+    V, T = int(g["V"][0]), int(g["T"][0])
+    ids = np.array([int(v) for v in g["ids"]])
+    W = np.random.default_rng(8).standard_normal((V, 3)) + 10.0
+    for r in range(T):
+        assert np.array_equal(o.embed_sp(ids, W, V, T, r), _row_of(g["sum"][r], W)[None, :]), r
+    rng = np.random.default_rng(15)
+    V, H, N = 24, 5, 48
+    ids = rng.integers(-2, V + 2, N)
+    W = rng.standard_normal((V, H))
+    W[3, 1] = -0.0
+    for T in (1, 2, 3, 4, 6, 8, 12, 24):
+        whole = np.concatenate([o.embed_sp(ids, W, V, T, r) for r in range(T)])
+        assert np.array_equal(whole, o.embed(ids, W, V, T)), T
+    try:
+        o.embed_sp(ids[:47], W, V, 2, 0)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("N % T != 0 must be rejected")
+
+
 # ---------------------------------------------------------------- embedding backward
 def pin_embed_bwd_worked_table(o):
     """Backward of the V=8, T=2, ids [1,6] table (sec. 5.2.1): position n's
@@ -332,7 +358,7 @@ def pin_embed_bwd_finite_differences(o):
 
 
 ALL_PINS = [pin_embed_worked_table, pin_embed_figure1, pin_embed_brute_force,
-            pin_embed_bwd_worked_table, pin_embed_bwd_adjoint, pin_embed_bwd_library,
+            pin_embed_sp, pin_embed_bwd_worked_table, pin_embed_bwd_adjoint, pin_embed_bwd_library,
             pin_embed_bwd_finite_differences,
             pin_ce_library, pin_ce_closed_form, pin_ce_ignore_and_bad,
             pin_shard_invariance, pin_page_t4_simulation,

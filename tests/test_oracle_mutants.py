@@ -95,6 +95,14 @@ def _embed_bwd_global_row(ids, dOut, V, T, t):
     return dW_t
 
 
+def _embed_sp_wrong_slice(ids, W, V, T, rank):
+    ids = np.asarray(ids, dtype=np.int64)
+    rows = len(ids) // T
+    if len(ids) % T:
+        raise ValueError
+    return ref.embed(ids, W, V, T)[(T - 1 - rank) * rows:(T - rank) * rows]   # ranks reversed
+
+
 _ORIG = {k: getattr(ref, k) for k in ("cross_entropy", "merge_local_stats")}
 
 MUTANTS = {
@@ -108,6 +116,7 @@ MUTANTS = {
     "embed_bwd_keep_masked_rows": ("embed_shard_grad", _embed_bwd_keep_masked),
     "embed_bwd_assign_not_add": ("embed_shard_grad", _embed_bwd_assign),
     "embed_bwd_global_row": ("embed_shard_grad", _embed_bwd_global_row),
+    "embed_sp_wrong_slice": ("embed_sp", _embed_sp_wrong_slice),
 }
 
 
