@@ -84,6 +84,28 @@ vp_status vp_embed_fwd(const int64_t* ids, const void* W, void* out,
                        void* stream);
 
 /*
+ * vp_embed_fwd_sp -- vp_embed_fwd with sequence parallelism on: one rank's
+ * slice of the reduce-scattered shard sum.
+ *
+ * "Vocab Parallelism" sec. 5.2.1: with SP off the T shard outputs are
+ * all-reduced (vp_embed_fwd); with SP on they are reduce-scattered along the
+ * token dimension, so rank r keeps token rows [r*N/T, (r+1)*N/T) of the sum:
+ *     out[i,:] = vp_embed_fwd(ids, W)[rank*N/T + i, :],   i < N/T
+ * bit-exact, same -0.0 rule.  The T ranks' outputs stacked in rank order are
+ * the SP-off output.  Its backward (the all-gather of the ranks' upstream
+ * slices, then each shard's masked scatter) is vp_embed_bwd on the stacked
+ * [N,H] upstream gradient.
+ *
+ *   ids   int64 [N]        all N token ids (rank r reads its N/T)
+ *   W     dtype [V,H]
+ *   out   dtype [N/T,H]    written
+ *   rank  0 <= rank < T;  N % T must be 0 (else VP_ERR_INVALID_ARG)
+ */
+vp_status vp_embed_fwd_sp(const int64_t* ids, const void* W, void* out,
+                          int64_t N, int64_t H, int64_t V, int T, int rank,
+                          vp_dtype dtype, void* stream);
+
+/*
  * vp_embed_bwd -- backward of vp_embed_fwd into the tied weight's gradient.
  *
  * "Vocab Parallelism" sec. 5.2.1: shard t's lookup zeroes the output rows of
@@ -200,8 +222,9 @@ vp_status vp_lmhead_ce_fwd_noalloc(const void* X, const void* W, const int64_t* 
  *
  * "Vocab Parallelism" sec. 5.3.2 and the interview note's key formulas: the
  * logit gradient is local to each shard, dZ[n,j] = g_n (softmax_j - 1[j=y_n]),
- * with g_n = dloss[n] (or 1/max(1,N_valid) when dloss is NULL, the gradient of
- * the mean) on valid tokens and 0 on ignored ones.  Each logit tile is
+ * with g_n = dloss[n], or, when dloss is NULL, dmean[0]/max(1,N_valid) (the
+ * gradient of dmean * loss_mean; dmean NULL means 1), on valid tokens and 0 on
+ * ignored ones.  Each logit tile is
  * recomputed from X and W, dZ is formed in the epilogue and stored in bf16
  * (f32 for VP_F32) scratch for one vocab chunk, then
  *     dW[chunk] = dZ_chunk^T X,     dX += dZ_chunk W[chunk]
@@ -210,13 +233,15 @@ vp_status vp_lmhead_ce_fwd_noalloc(const void* X, const void* W, const int64_t* 
  *
  *   lse    f32 [N]           from vp_lmhead_ce_fwd
  *   dloss  f32 [N] or NULL
+ *   dmean  f32 [1] (device) or NULL: upstream gradient of loss_mean, used
+ *          when dloss is NULL (autograd's incoming gradient, a loss scale)
  *   dX     dtype [N,H]       overwritten
  *   dW     f32 [V,H]         overwritten (fp32 so that a caller can add the
  *                            tied embedding's gradient)
  *   workspace  >= vp_lmhead_ce_workspace_size(..., pass 1, c) for some chunk c
  */
 vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t* targets,
-                           const float* lse, const float* dloss,
+                           const float* lse, const float* dloss, const float* dmean,
                            int64_t N, int64_t H, int64_t V, int T,
                            int64_t ignore_index, vp_dtype dtype,
                            void* dX, float* dW,
@@ -244,14 +269,15 @@ vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t* targets,
  * the recompute backward of the split calls.
  *
  * Arguments and outputs are those of vp_lmhead_ce_fwd and vp_lmhead_ce_bwd:
- *   dloss      f32 [N] or NULL (NULL: gradient of loss_mean)
+ *   dloss      f32 [N] or NULL (NULL: gradient of dmean * loss_mean)
+ *   dmean      f32 [1] (device) or NULL (= 1), used when dloss is NULL
  *   loss, lse  f32 [N] written;  loss_mean, shard_stats, n_bad as in the forward
  *   dX         dtype [N,H] overwritten;  dW  f32 [V,H] overwritten
  *   workspace  >= vp_lmhead_ce_workspace_size(..., pass 2, c) for some chunk c
  * Errors as for the other calls; nothing is launched on an argument error.
  */
 vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int64_t* targets,
-                               const float* dloss,
+                               const float* dloss, const float* dmean,
                                int64_t N, int64_t H, int64_t V, int T,
                                int64_t ignore_index, vp_dtype dtype,
                                float* loss, float* lse, float* loss_mean,

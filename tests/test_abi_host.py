@@ -73,10 +73,13 @@ def test_ce_rejects_bad_arguments(lib):
     assert call(args(H=63)) == 2
     assert call(args(wsb=16)) == 3                                   # workspace too small
     bwd = lib.vp_lmhead_ce_bwd
-    assert bwd(X, W, y, lse, None, 6, 64, 16, 3, -100, vp.VP_F32, P(0x70000), P(0x80000), ws, 1 << 20, None) == 1
-    assert bwd(X, W, y, None, None, 6, 64, 16, 4, -100, vp.VP_F32, P(0x70000), P(0x80000), ws, 1 << 20, None) == 1
-    assert bwd(X, W, y, lse, None, 6, 64, 16, 4, -100, vp.VP_F32, P(0x70008), P(0x80000), ws, 1 << 20, None) == 2
-    assert bwd(X, W, y, lse, None, 6, 64, 16, 4, -100, vp.VP_F32, P(0x70000), P(0x80000), ws, 64, None) == 3
+    assert bwd(X, W, y, lse, None, None, 6, 64, 16, 3, -100, vp.VP_F32, P(0x70000), P(0x80000), ws, 1 << 20,
+               None) == 1
+    assert bwd(X, W, y, None, None, None, 6, 64, 16, 4, -100, vp.VP_F32, P(0x70000), P(0x80000), ws, 1 << 20,
+               None) == 1
+    assert bwd(X, W, y, lse, None, None, 6, 64, 16, 4, -100, vp.VP_F32, P(0x70008), P(0x80000), ws, 1 << 20,
+               None) == 2
+    assert bwd(X, W, y, lse, None, None, 6, 64, 16, 4, -100, vp.VP_F32, P(0x70000), P(0x80000), ws, 64, None) == 3
 
 
 def test_workspace_sizes(lib):
@@ -112,7 +115,7 @@ def test_fused_rejects_bad_arguments(lib):
     f = lib.vp_lmhead_ce_fwd_bwd
 
     def call(N=300, H=64, V=1000, T=4, dt=vp.VP_BF16, X=X, dX=dX, dW=dW, wsb=1 << 30):
-        return f(X, W, y, None, N, H, V, T, -100, dt, loss, lse, None, None, None, dX, dW, ws, wsb, None)
+        return f(X, W, y, None, None, N, H, V, T, -100, dt, loss, lse, None, None, None, dX, dW, ws, wsb, None)
     assert call(T=3) == 1                    # V % T != 0
     assert call(dX=None) == 1
     assert call(dW=None) == 1
@@ -136,3 +139,12 @@ def test_embed_bwd_rejects_bad_arguments(lib):
     assert f(ids, G, P(0x3004), 100, 64, 1000, 4, vp.VP_BF16, 0, ws, nb, None) == 2
     assert f(ids, G, dW, 100, 60, 1000, 4, vp.VP_BF16, 0, ws, nb, None) == 2   # H*2 % 16 != 0
     assert f(ids, G, dW, 100, 64, 1000, 4, vp.VP_BF16, 0, ws, 64, None) == 3
+
+
+def test_embed_sp_rejects_bad_arguments(lib):
+    ids, W, out = P(0x1000), P(0x2000), P(0x3000)
+    f = lib.vp_embed_fwd_sp
+    assert f(ids, W, out, 10, 8, 16, 4, 0, vp.VP_BF16, None) == 1     # N % T != 0
+    assert f(ids, W, out, 12, 8, 16, 4, 4, vp.VP_BF16, None) == 1     # rank >= T
+    assert f(ids, W, out, 12, 8, 16, 4, -1, vp.VP_BF16, None) == 1
+    assert f(ids, W, P(0x3008), 12, 8, 16, 4, 1, vp.VP_BF16, None) == 2

@@ -234,6 +234,19 @@ def test_autograd_wrapper():
     assert abs(loss.item() - o["mean"]) <= 2e-2 + 1e-2 * abs(o["mean"])
 
 
+def test_autograd_upstream_scale():
+    """(3 * loss).backward(): the incoming gradient reaches the library as a
+    device scalar and scales dX and dW by 3."""
+    inp = synth.small_case(96, 64, 512, 2, "bf16", seed=4, ignore_frac=0.1)
+    X, W, y = dev_inputs(inp)
+    X.requires_grad_(True)
+    W.requires_grad_(True)
+    (3.0 * vp.lmhead_ce(X, W, y, 2)).backward()
+    b = ref.lmhead_ce_backward(inp.X, inp.W, inp.targets, inp.wl.V)
+    assert rel_fro(np64(X.grad), 3.0 * b["dX"]) <= 2e-2
+    assert rel_fro(np64(W.grad), 3.0 * b["dW"]) <= 2e-2
+
+
 def test_results_repeatable():
     """Two calls on the same inputs give bit-identical results (no atomics in
     any reduction)."""

@@ -130,3 +130,33 @@ def test_tied_weight_gradient():
     b = ref.lmhead_ce_backward(inp.X, inp.W, inp.targets, 1000)
     want = ref.embed_backward(ids, np64(G), 1000, 4, dW0=b["dW"])
     assert rel_fro(np64(o["dW"]), want) <= 2e-2
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_embed_sp_ranks(dtype):
+    """SP on: every rank's slice bit-exact against the oracle's reduce-scatter,
+    the V=8 worked table included (rank 0 keeps E1, rank 1 E6)."""
+    g = read("embed_v8_t2_ids_1_6.txt")
+    V, T = int(g["V"][0]), int(g["T"][0])
+    ids = np.array([int(v) for v in g["ids"]])
+    W = torch.arange(V * 8, dtype=torch.float32).reshape(V, 8).add(1.0).to(_tdt(dtype)).cuda()
+    for r in range(T):
+        out = vp.embed_fwd_sp(torch.from_numpy(ids).cuda(), W, T, r)
+        assert np.array_equal(np64(out), ref.embed_sp(ids, np64(W), V, T, r)), r
+    rng = np.random.default_rng(4)
+    V, H, N, T = 1200, 136, 960, 8
+    ids = rng.integers(-5, V + 5, N)
+    Wn = torch.from_numpy(rng.standard_normal((V, H)).astype(np.float32)).to(_tdt(dtype))
+    Wn[7, 3] = -0.0
+    ids[0] = 7
+    Wd = Wn.cuda()
+    W64 = np64(Wn)
+    idt = torch.from_numpy(ids).cuda()
+    for r in range(T):
+        out = vp.embed_fwd_sp(idt, Wd, T, r)
+        torch.cuda.synchronize()
+        want = ref.embed_sp(ids, W64, V, T, r)
+        assert np.array_equal(np64(out), want), r
+        if r == 0:
+            bits = out.view(torch.int16 if dtype == "bf16" else torch.int32).cpu().numpy()
+            assert bits[0, 3] == 0          # -0.0 came out +0.0

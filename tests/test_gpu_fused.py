@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle.ref as ref
 import synth
 import vocab_lm_head_vp_b300 as vp
 from gpu_util import dev_inputs, np64, rel_fro
@@ -130,3 +131,15 @@ def test_fused_gemm_forms(pair):
         _check(inp, 6, o, dX, dW)
     finally:
         vp.set_gemm_variant(False)
+
+
+def test_fused_loss_scale_dmean():
+    """dmean (a device scalar, e.g. a loss scale) multiplies the mean's gradient."""
+    inp = synth.small_case(300, 128, 1000, 4, "bf16", seed=9, ignore_frac=0.1)
+    X, W, y = dev_inputs(inp)
+    scale = torch.tensor([1024.0], device="cuda")
+    o = vp.lmhead_ce_fwd_bwd(X, W, y, 4, dmean=scale)
+    torch.cuda.synchronize()
+    b = ref.lmhead_ce_backward(inp.X, inp.W, inp.targets, inp.wl.V)
+    assert rel_fro(np64(o["dX"]), 1024.0 * b["dX"]) <= 2e-2
+    assert rel_fro(np64(o["dW"]), 1024.0 * b["dW"]) <= 2e-2

@@ -18,7 +18,7 @@ import os
 
 import torch
 
-__all__ = ["embed_fwd", "embed_bwd", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce_fwd_bwd", "lmhead_ce", "workspace_size", "read_device_status",
+__all__ = ["embed_fwd", "embed_fwd_sp", "embed_bwd", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce_fwd_bwd", "lmhead_ce", "workspace_size", "read_device_status",
            "test_gemm_bf16", "set_gemm_variant", "stage_timing_enable", "stage_timing_read", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
 
 VP_F32, VP_BF16 = 0, 1
@@ -53,6 +53,8 @@ def _load():
     L.vp_version.restype = ctypes.c_char_p
     L.vp_embed_fwd.restype = I32
     L.vp_embed_fwd.argtypes = [P, P, P, I64, I64, I64, I32, I32, P]
+    L.vp_embed_fwd_sp.restype = I32
+    L.vp_embed_fwd_sp.argtypes = [P, P, P, I64, I64, I64, I32, I32, I32, P]
     L.vp_embed_bwd_workspace_size.restype = SZ
     L.vp_embed_bwd_workspace_size.argtypes = [I64, I64, I64, I32, I32]
     L.vp_embed_bwd.restype = I32
@@ -62,9 +64,9 @@ def _load():
     L.vp_lmhead_ce_fwd.restype = I32
     L.vp_lmhead_ce_fwd.argtypes = [P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, P, P, P, SZ, P]
     L.vp_lmhead_ce_bwd.restype = I32
-    L.vp_lmhead_ce_bwd.argtypes = [P, P, P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, SZ, P]
+    L.vp_lmhead_ce_bwd.argtypes = [P, P, P, P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, SZ, P]
     L.vp_lmhead_ce_fwd_bwd.restype = I32
-    L.vp_lmhead_ce_fwd_bwd.argtypes = [P, P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, P, P, P, P, P, SZ, P]
+    L.vp_lmhead_ce_fwd_bwd.argtypes = [P, P, P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, P, P, P, P, P, SZ, P]
     L.vp_read_device_status.restype = I32
     L.vp_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     L.vp_test_gemm_bf16.restype = I32
@@ -142,6 +144,21 @@ def embed_fwd(ids: torch.Tensor, W: torch.Tensor, T: int, out: torch.Tensor | No
     return out
 
 
+def embed_fwd_sp(ids: torch.Tensor, W: torch.Tensor, T: int, rank: int, out: torch.Tensor | None = None):
+    """Sequence-parallel embedding: rank's token rows [rank N/T, (rank+1) N/T)
+    of the shard sum (the reduce-scatter of the shard outputs)."""
+    _need(W, "W")
+    _need(ids, "ids", torch.int64, W.device)
+    V, H = W.shape
+    N = ids.numel()
+    if out is None:
+        out = torch.empty((N // T, H), dtype=W.dtype, device=W.device)
+    _need(out, "out", W.dtype, W.device)
+    _check("vp_embed_fwd_sp", _load().vp_embed_fwd_sp(_ptr(ids), _ptr(W), _ptr(out), N, H, V, T, rank,
+                                                      _dtype_code(W), _stream(W.device)))
+    return out
+
+
 def embed_bwd(ids: torch.Tensor, dOut: torch.Tensor, V: int, T: int, dW: torch.Tensor | None = None,
               accumulate: bool = False, workspace: torch.Tensor | None = None) -> torch.Tensor:
     """dW[v] (+)= sum of dOut[n] over tokens with ids[n] = v (fp32 [V,H]);
@@ -197,15 +214,17 @@ def lmhead_ce_fwd(X, W, targets, T, ignore_index=IGNORE_INDEX, shard_stats=False
 
 
 def lmhead_ce_bwd(X, W, targets, lse, T, ignore_index=IGNORE_INDEX, dloss=None, vocab_chunk=None,
-                  workspace=None, dX=None, dW=None):
-    """Backward of the mean loss (or of sum_n dloss[n] * loss[n]): (dX in X's
-    dtype, dW in fp32)."""
+                  workspace=None, dX=None, dW=None, dmean=None):
+    """Backward of dmean * loss_mean (dmean: a 1-element device tensor, default
+    1) or of sum_n dloss[n] * loss[n]: (dX in X's dtype, dW in fp32)."""
     _need(X, "X")
     _need(W, "W", X.dtype, X.device)
     _need(targets, "targets", torch.int64, X.device)
     _need(lse, "lse", torch.float32, X.device)
     if dloss is not None:
         _need(dloss, "dloss", torch.float32, X.device)
+    if dmean is not None:
+        _need(dmean, "dmean", torch.float32, X.device)
     N, H = X.shape
     V = W.shape[0]
     dev = X.device
@@ -220,7 +239,8 @@ def lmhead_ce_bwd(X, W, targets, lse, T, ignore_index=IGNORE_INDEX, dloss=None, 
         raise VpError("vp_lmhead_ce_workspace_size", 1)
     ws = _workspace(ws_bytes, dev, workspace)
     code = _load().vp_lmhead_ce_bwd(
-        _ptr(X), _ptr(W), _ptr(targets), _ptr(lse), _ptr(dloss), N, H, V, T, ignore_index, _dtype_code(X),
+        _ptr(X), _ptr(W), _ptr(targets), _ptr(lse), _ptr(dloss), _ptr(dmean), N, H, V, T, ignore_index,
+        _dtype_code(X),
         _ptr(dX), _ptr(dW), _ptr(ws), ws_bytes if workspace is None else ws.numel() * ws.element_size(),
         _stream(dev))
     _check("vp_lmhead_ce_bwd", code)
@@ -228,7 +248,7 @@ def lmhead_ce_bwd(X, W, targets, lse, T, ignore_index=IGNORE_INDEX, dloss=None, 
 
 
 def lmhead_ce_fwd_bwd(X, W, targets, T, ignore_index=IGNORE_INDEX, dloss=None, shard_stats=False, token_chunk=None,
-                      workspace=None, out=None) -> dict:
+                      workspace=None, out=None, dmean=None) -> dict:
     """Forward and backward in one call (probabilities saved, no logit
     recompute).  Returns the forward's loss, lse, mean, n_bad (and
     shard_stats if asked) plus dX (X's dtype) and dW (fp32) of the mean loss,
@@ -238,6 +258,8 @@ def lmhead_ce_fwd_bwd(X, W, targets, T, ignore_index=IGNORE_INDEX, dloss=None, s
     _need(targets, "targets", torch.int64, X.device)
     if dloss is not None:
         _need(dloss, "dloss", torch.float32, X.device)
+    if dmean is not None:
+        _need(dmean, "dmean", torch.float32, X.device)
     N, H = X.shape
     V = W.shape[0]
     dev = X.device
@@ -262,7 +284,8 @@ def lmhead_ce_fwd_bwd(X, W, targets, T, ignore_index=IGNORE_INDEX, dloss=None, s
         ws = workspace
         ws_bytes = ws.numel() * ws.element_size()
     code = _load().vp_lmhead_ce_fwd_bwd(
-        _ptr(X), _ptr(W), _ptr(targets), _ptr(dloss), N, H, V, T, ignore_index, _dtype_code(X), _ptr(out["loss"]),
+        _ptr(X), _ptr(W), _ptr(targets), _ptr(dloss), _ptr(dmean), N, H, V, T, ignore_index, _dtype_code(X),
+        _ptr(out["loss"]),
         _ptr(out["lse"]), _ptr(out.get("mean")), _ptr(out.get("shard_stats")), _ptr(out.get("n_bad")),
         _ptr(out["dX"]), _ptr(out["dW"]), _ptr(ws), ws_bytes, _stream(dev))
     _check("vp_lmhead_ce_fwd_bwd", code)
@@ -327,10 +350,11 @@ class _LMHeadCE(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad):
         X, W, targets, lse = ctx.saved_tensors
-        # d(g * mean)/dl_n = g / N_valid: pass the per-token upstream gradient
-        valid = (targets >= 0) & (targets < W.shape[0]) & (targets != ctx.ignore_index)
-        dloss = (valid.float() * (grad.float() / valid.sum().clamp(min=1))).contiguous()
-        dX, dW = lmhead_ce_bwd(X, W, targets, lse, ctx.T, ctx.ignore_index, dloss=dloss)
+        # the incoming gradient of the mean goes to the library as a device scalar
+        dmean = grad.reshape(1)
+        if dmean.dtype != torch.float32 or not dmean.is_contiguous():
+            dmean = dmean.to(torch.float32).contiguous()
+        dX, dW = lmhead_ce_bwd(X, W, targets, lse, ctx.T, ctx.ignore_index, dmean=dmean)
         return dX, dW.to(W.dtype), None, None, None
 
 

@@ -24,6 +24,19 @@ namespace vp {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Rows (of the output's M dimension) per tile group of each launch: the
+// persistent CTAs walk down a group's m-blocks before moving along n, so CTAs
+// running at the same time share operand tiles in L2.
+#ifndef VP_GROUP_ROWS_LOGITS
+#define VP_GROUP_ROWS_LOGITS 4096   // forward / recompute: token rows (W re-read once per group)
+#endif
+#ifndef VP_GROUP_ROWS_DX
+#define VP_GROUP_ROWS_DX 1024       // dX: token rows
+#endif
+#ifndef VP_GROUP_ROWS_DW
+#define VP_GROUP_ROWS_DW 2048       // dW: vocab rows
+#endif
+
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -421,7 +434,7 @@ cudaError_t bf16_lse_stats(const void* X, const void* W, const int64_t* targets,
   if (!make_tmap_bf16(&ta, X, N, H, H, kBK, kBM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, W, V, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
   EpiLseStats::Params p{partial, zy, targets, N, V, Vs, maxseg, nullptr};
-  return launch_any<false, false, EpiLseStats>(ta, tb, ta, N, V, H, p, status, stream, 2048);
+  return launch_any<false, false, EpiLseStats>(ta, tb, ta, N, V, H, p, status, stream, VP_GROUP_ROWS_LOGITS);
 }
 
 cudaError_t bf16_lse_stats_p(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H, int64_t V,
@@ -433,7 +446,7 @@ cudaError_t bf16_lse_stats_p(const void* X, const void* W, const int64_t* target
   // fp16 boxes of 32 rows x 64 columns (128 bytes), clipped at V columns and N rows
   if (!make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, P, N, V, ldp, 64, 32)) return cudaErrorInvalidValue;
   EpiLseStatsP::Params p{partial, zy, targets, N, V, Vs, maxseg, tmax};
-  return launch_any<false, false, EpiLseStatsP>(ta, tb, tc, N, V, H, p, status, stream, 2048);
+  return launch_any<false, false, EpiLseStatsP>(ta, tb, tc, N, V, H, p, status, stream, VP_GROUP_ROWS_LOGITS);
 }
 
 cudaError_t bf16_dz_chunk(const void* X, const void* W, const int64_t* targets, const float* lse, const float* g,
@@ -445,7 +458,7 @@ cudaError_t bf16_dz_chunk(const void* X, const void* W, const int64_t* targets, 
   if (!make_tmap_bf16(&tb, Wc, Vc, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
   if (!make_store_tmap(&tc, true, dz, N, Vc, ldz)) return cudaErrorInvalidValue;
   EpiDZ::Params p{lse, g, targets, N, c0, Vc};
-  return launch_any<false, false, EpiDZ>(ta, tb, tc, N, Vc, H, p, status, stream, 2048);
+  return launch_any<false, false, EpiDZ>(ta, tb, tc, N, Vc, H, p, status, stream, VP_GROUP_ROWS_LOGITS);
 }
 
 cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N, int64_t H, int64_t c0,
@@ -459,7 +472,7 @@ cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N,
   if (!make_tmap_bf16(&tb, Wc, Vc, H, H, 64, kBK)) return cudaErrorInvalidValue;
   if (!make_store_tmap(&tc, mode >= kStoreBf16AddPartial, out, N, H, H)) return cudaErrorInvalidValue;
   EpiStore::Params p{mode == kAddF32 ? static_cast<const float*>(out) : partial, H, N, H, mode};
-  return launch_any<false, true, EpiStore>(ta, tb, tc, N, H, Vc, p, status, stream, 1024);
+  return launch_any<false, true, EpiStore>(ta, tb, tc, N, H, Vc, p, status, stream, VP_GROUP_ROWS_DX);
 }
 
 cudaError_t bf16_dw_chunk(const void* dz, int64_t ldz, const void* X, int64_t N, int64_t H, int64_t c0,
@@ -473,7 +486,7 @@ cudaError_t bf16_dw_chunk(const void* dz, int64_t ldz, const void* X, int64_t N,
   float* out = dW + c0 * H;
   if (!make_store_tmap(&tc, false, out, Vc, H, H)) return cudaErrorInvalidValue;
   EpiStore::Params p{accumulate ? out : nullptr, H, Vc, H, accumulate ? kAddF32 : kStoreF32};
-  return launch_any<true, true, EpiStore>(ta, tb, tc, Vc, H, N, p, status, stream, 1024);
+  return launch_any<true, true, EpiStore>(ta, tb, tc, Vc, H, N, p, status, stream, VP_GROUP_ROWS_DW);
 }
 
 // Plain GEMM entry used by the unit tests of the core: D[M,N] = A * B^T with

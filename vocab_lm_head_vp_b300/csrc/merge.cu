@@ -11,8 +11,9 @@
 // loss_mean_and_bad: L = sum_n loss_n / max(1, N_valid) (sec. 5.3.3) and the
 // count of targets that are neither ignore_index nor inside [0, V).
 //
-// upstream_scale: g_n = dloss_n (or 1/max(1, N_valid)) on valid tokens, 0 on
-// ignored ones -- the per-row factor of the logit gradient (sec. 5.3.2-5.3.3).
+// upstream_scale: g_n = dloss_n (or dmean/max(1, N_valid), dmean = 1 when not
+// given) on valid tokens, 0 on ignored ones -- the per-row factor of the logit
+// gradient (sec. 5.3.2-5.3.3).
 #include <cuda_runtime.h>
 
 #include "vp_internal.h"
@@ -123,7 +124,8 @@ __global__ void __launch_bounds__(kRedThreads) loss_mean_kernel(const float* __r
 }
 
 __global__ void __launch_bounds__(kRedThreads) upstream_scale_kernel(const int64_t* __restrict__ targets,
-                                                                     const float* __restrict__ dloss, int64_t N,
+                                                                     const float* __restrict__ dloss,
+                                                                     const float* __restrict__ dmean, int64_t N,
                                                                      int64_t V, int64_t ignore_index,
                                                                      float* __restrict__ g) {
   __shared__ int s_valid[kRedThreads];
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(kRedThreads) upstream_scale_kernel(const int64
     if (threadIdx.x < w) s_valid[threadIdx.x] += s_valid[threadIdx.x + w];
     __syncthreads();
   }
-  const float inv = 1.0f / static_cast<float>(s_valid[0] > 1 ? s_valid[0] : 1);
+  const float inv = (dmean ? *dmean : 1.0f) / static_cast<float>(s_valid[0] > 1 ? s_valid[0] : 1);
   for (int64_t n = threadIdx.x; n < N; n += kRedThreads) {
     const int64_t y = targets[n];
     const bool valid = y >= 0 && y < V && y != ignore_index;
@@ -174,9 +176,10 @@ cudaError_t loss_mean_and_bad(const float* loss, const int64_t* targets, int64_t
   return cudaGetLastError();
 }
 
-cudaError_t upstream_scale(const int64_t* targets, const float* dloss, int64_t N, int64_t V, int64_t ignore_index,
+cudaError_t upstream_scale(const int64_t* targets, const float* dloss, const float* dmean, int64_t N, int64_t V,
+                           int64_t ignore_index,
                            float* g, cudaStream_t stream) {
-  upstream_scale_kernel<<<1, kRedThreads, 0, stream>>>(targets, dloss, N, V, ignore_index, g);
+  upstream_scale_kernel<<<1, kRedThreads, 0, stream>>>(targets, dloss, dmean, N, V, ignore_index, g);
   return cudaGetLastError();
 }
 

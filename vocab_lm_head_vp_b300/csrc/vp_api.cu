@@ -181,6 +181,21 @@ VP_EXPORT vp_status vp_embed_fwd(const int64_t* ids, const void* W, void* out, i
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
 }
 
+VP_EXPORT vp_status vp_embed_fwd_sp(const int64_t* ids, const void* W, void* out, int64_t N, int64_t H, int64_t V,
+                                    int T, int rank, vp_dtype dtype, void* stream) {
+  if (!ids || !W || !out || !dtype_ok(dtype) || !shape_ok(N, H, V, T)) return VP_ERR_INVALID_ARG;
+  if (N % T != 0 || rank < 0 || rank >= T) return VP_ERR_INVALID_ARG;
+  const int es = esize_of(dtype);
+  if (!aligned16(W) || !aligned16(out) || (H * es) % 16 != 0) return VP_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(ids) & 7u) != 0) return VP_ERR_UNSUPPORTED;
+  cudaStream_t s = as_stream(stream);
+  const int64_t rows = N / T;
+  // rank's token slice of the shard sum: the gather of exactly those tokens
+  cudaError_t e =
+      timed(kEmbed, s, [&] { return embed_gather(ids + rank * rows, W, out, rows, H, V, V / T, T, es, s); });
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
 VP_EXPORT size_t vp_embed_bwd_workspace_size(int64_t N, int64_t H, int64_t V, int T, vp_dtype dtype) {
   if (!dtype_ok(dtype) || !shape_ok(N, H, V, T)) return 0;
   return align_up(embed_bwd_workspace(N, H), kAlign);
@@ -279,7 +294,8 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd(const void* X, const void* W, const int64_t
 }
 
 VP_EXPORT vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t* targets, const float* lse,
-                                     const float* dloss, int64_t N, int64_t H, int64_t V, int T,
+                                     const float* dloss, const float* dmean, int64_t N, int64_t H, int64_t V,
+                                     int T,
                                      int64_t ignore_index, vp_dtype dtype, void* dX, float* dW, void* workspace,
                                      size_t ws_bytes, void* stream) {
   if (!lse || !dX || !dW) return VP_ERR_INVALID_ARG;
@@ -296,7 +312,8 @@ VP_EXPORT vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t
   void* dz = ws + L.off_dz;
   float* acc = reinterpret_cast<float*>(ws + L.off_acc);
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
-  if (e == cudaSuccess) e = timed(kScale, s, [&] { return upstream_scale(targets, dloss, N, V, ignore_index, g, s); });
+  if (e == cudaSuccess)
+    e = timed(kScale, s, [&] { return upstream_scale(targets, dloss, dmean, N, V, ignore_index, g, s); });
   const bool single = Vc >= V;
   for (int64_t c0 = 0; c0 < V && e == cudaSuccess; c0 += Vc) {
     const int64_t vc = (V - c0) < Vc ? (V - c0) : Vc;
@@ -332,7 +349,7 @@ VP_EXPORT vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t
 }
 
 VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int64_t* targets, const float* dloss,
-                                         int64_t N, int64_t H, int64_t V, int T, int64_t ignore_index,
+                                         const float* dmean, int64_t N, int64_t H, int64_t V, int T, int64_t ignore_index,
                                          vp_dtype dtype, float* loss, float* lse, float* loss_mean,
                                          float* shard_stats, int32_t* n_bad, void* dX, float* dW, void* workspace,
                                          size_t ws_bytes, void* stream) {
@@ -347,8 +364,8 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int
     st = vp_lmhead_ce_fwd(X, W, targets, N, H, V, T, ignore_index, dtype, loss, lse, loss_mean, shard_stats, n_bad,
                           workspace, ws_bytes, stream);
     if (st != VP_OK) return st;
-    return vp_lmhead_ce_bwd(X, W, targets, lse, dloss, N, H, V, T, ignore_index, dtype, dX, dW, workspace, ws_bytes,
-                            stream);
+    return vp_lmhead_ce_bwd(X, W, targets, lse, dloss, dmean, N, H, V, T, ignore_index, dtype, dX, dW, workspace,
+                            ws_bytes, stream);
   }
   const int64_t Nc = fused_chunk_from_ws(N, V, T, ws_bytes);
   if (Nc <= 0) return VP_ERR_WORKSPACE;
@@ -364,7 +381,8 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int
   void* P = ws + L.off_p;
   const int64_t Vs = V / T;
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
-  if (e == cudaSuccess) e = timed(kScale, s, [&] { return upstream_scale(targets, dloss, N, V, ignore_index, g, s); });
+  if (e == cudaSuccess)
+    e = timed(kScale, s, [&] { return upstream_scale(targets, dloss, dmean, N, V, ignore_index, g, s); });
   for (int64_t n0 = 0; n0 < N && e == cudaSuccess; n0 += Nc) {
     const int64_t nc = (N - n0) < Nc ? (N - n0) : Nc;
     const void* Xc = static_cast<const uint8_t*>(X) + n0 * H * 2;

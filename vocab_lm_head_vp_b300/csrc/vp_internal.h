@@ -63,7 +63,8 @@ cudaError_t dz_from_p(void* P, int64_t ldp, const float* tmax, const float* lse,
                       const int64_t* targets, int64_t N, int64_t V, cudaStream_t stream);
 cudaError_t loss_mean_and_bad(const float* loss, const int64_t* targets, int64_t N, int64_t V, int64_t ignore_index,
                               float* loss_mean, int32_t* n_bad, cudaStream_t stream);
-cudaError_t upstream_scale(const int64_t* targets, const float* dloss, int64_t N, int64_t V, int64_t ignore_index,
+cudaError_t upstream_scale(const int64_t* targets, const float* dloss, const float* dmean, int64_t N, int64_t V,
+                           int64_t ignore_index,
                            float* g, cudaStream_t stream);
 
 // ---- embedding (embed.cu)
