@@ -61,14 +61,14 @@ def parse_args():
 
 # DRAM bytes (read + write) per launch of the tcgen05 GEMM kernel in the fused
 # v128k step, from one ncu capture (profiles/launches_fused_step_v128k.md: mean of
-# the three GEMM launches of two steps).  They describe the kernel built from the
+# the three GEMM launches over four steps).  They describe the kernel built from the
 # sources hashed here; once those change, `traffic` is reported as null until a
 # new capture replaces the number.
-GEMM_TRAFFIC = {"workload": "v128k", "path": "fused", "gemm_variant": "single", "bytes_per_launch": 25.33e9,
-                "by_launch": {"lse_p_gemm": 12.82e9, "dw_gemm": 25.00e9, "dx_gemm": 38.16e9},
+GEMM_TRAFFIC = {"workload": "v128k", "path": "fused", "gemm_variant": "single", "bytes_per_launch": 22.51e9,
+                "by_launch": {"lse_p_gemm": 8.73e9, "dw_gemm": 22.23e9, "dx_gemm": 36.58e9},
                 "sources": ("vocab_lm_head_vp_b300/csrc/ce_bf16.cu", "vocab_lm_head_vp_b300/csrc/ptx.cuh",
                             "vocab_lm_head_vp_b300/csrc/umma_gemm.cuh"),
-                "sha256": "c78af5847690e828ce1b521d07e9ba392abbbb90791927711c5edf5d318ce3e7"}
+                "sha256": "f45b566df537368b5861aa3391cb8f3f545ee0261f3894d3c053ba4c2b1a2876"}
 
 
 def gemm_traffic(workload, path, variant):
