@@ -50,7 +50,9 @@ vp_status vp_test_set_gemm_variant(int pair);
  *   Launches beyond max_launches are not recorded (see the count returned).
  * vp_stage_timing_read(ms, counts, n): waits for the recorded events and
  *   writes, for stage s < n, the summed milliseconds and the number of
- *   launches; returns the number of stages, or -1 on a CUDA error.
+ *   kernels launched in the stage's timed regions (lse_merge is two kernels
+ *   per region, embed_bwd several); returns the number of stages, or -1 on a
+ *   CUDA error.
  * vp_stage_name(s): the stage's name (static storage), NULL past the end.
  */
 vp_status vp_stage_timing_enable(int max_launches);

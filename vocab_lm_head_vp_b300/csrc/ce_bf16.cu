@@ -16,6 +16,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "umma_gemm.cuh"
 #include "umma_gemm_2sm.cuh"
 #include "vp_internal.h"
@@ -321,15 +323,35 @@ bool make_store_tmap(CUtensorMap* m, bool bf16, const void* base, int64_t rows, 
               : make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, cols, ld, 32, 32);
 }
 
+// Launch-configuration facts are cached per device: a process may drive
+// several GPUs, and a function's shared-memory opt-in is made per device.
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  return dev;
+}
+
 int sm_count() {
-  static int n = 0;
+  static std::atomic<int> cache[kMaxDevices];
+  const int dev = current_device();
+  int n = cache[dev].load(std::memory_order_relaxed);
   if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
   return n;
+}
+
+// Opt `kern` in to `smem` bytes of dynamic shared memory on the current device, once.
+template <class Kern>
+cudaError_t ensure_smem(Kern kern, size_t smem, std::atomic<int>* done) {
+  const int dev = current_device();
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+  return e;
 }
 
 template <bool A_MN, bool B_MN, class Epi>
@@ -338,12 +360,9 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
                         cudaStream_t stream, int group_m) {
   auto kern = umma_gemm_kernel<A_MN, B_MN, Epi>;
   constexpr size_t smem = kGemmSmemBytes + Epi::kStagingBytes;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<int> attr_done[kMaxDevices];
+  const cudaError_t e = ensure_smem(kern, smem, attr_done);
+  if (e != cudaSuccess) return e;
   GemmArgs a;
   a.sched.num_m = static_cast<int>((M + kBM - 1) / kBM);
   a.sched.num_n = static_cast<int>((Ncols + kBN - 1) / kBN);
@@ -375,17 +394,19 @@ cudaError_t launch_gemm_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const 
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  static int max_pairs = 0;
+  static std::atomic<int> attr_done[kMaxDevices];
+  static std::atomic<int> pairs_cache[kMaxDevices];
+  const cudaError_t e = ensure_smem(kern, smem, attr_done);
+  if (e != cudaSuccess) return e;
+  const int dev = current_device();
+  int max_pairs = pairs_cache[dev].load(std::memory_order_relaxed);
   if (max_pairs == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(2 * (sm_count() / 2));
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg) != cudaSuccess || max_pairs <= 0) {
       cudaGetLastError();
-      n = sm_count() / 2;
+      max_pairs = sm_count() / 2;
     }
-    max_pairs = n;
+    pairs_cache[dev].store(max_pairs, std::memory_order_relaxed);
   }
   GemmArgs a;
   a.sched.num_m = static_cast<int>((M + kPairBM - 1) / kPairBM);

@@ -250,6 +250,16 @@ int64_t pad_pow2(int64_t n) {
 
 }  // namespace
 
+int embed_bwd_kernels(int64_t N) {
+  const int64_t n_pad = pad_pow2(N);
+  int k = 4;   // keys, chunk sort, run sums, cross-run sums
+  for (int64_t m = 2 * kChunk; m <= n_pad; m <<= 1) {
+    for (int64_t j = m >> 1; j >= kChunk; j >>= 1) ++k;   // global steps
+    ++k;                                                   // the chunk merge
+  }
+  return k;
+}
+
 size_t embed_bwd_workspace(int64_t N, int64_t H) {
   const int64_t runs = (N + kRun - 1) / kRun;
   return size_t(pad_pow2(N)) * sizeof(uint64_t) + 2 * size_t(runs) * H * sizeof(float);

@@ -126,6 +126,8 @@ int64_t fused_chunk_from_ws(int64_t N, int64_t V, int T, size_t ws) {
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+constexpr int kMergeKernels = 2;   // lse_merge: the per-shard pass, then the per-token pass
+
 // ---------------- optional per-launch event timing (vp_stage_timing_enable)
 enum Stage {
   kEmbed, kLseGemm, kMerge, kMean, kScale, kDzGemm, kDwGemm, kDxGemm, kLsePGemm, kDzFromP, kEmbedBwd, kNumStages
@@ -137,14 +139,16 @@ struct StageTimer {
   int cap = 0, used = 0;
   cudaEvent_t* ev = nullptr;  // 2 per launch
   int* stage = nullptr;
+  int* kernels = nullptr;   // kernels launched inside each timed region
 } g_timer;
 
 template <class F>
-cudaError_t timed(Stage st, cudaStream_t s, F&& launch) {
+cudaError_t timed(Stage st, cudaStream_t s, F&& launch, int kernels = 1) {
   int slot = -1;
   if (g_timer.cap > 0 && g_timer.used < g_timer.cap) {
     slot = g_timer.used++;
     g_timer.stage[slot] = st;
+    g_timer.kernels[slot] = kernels;
     cudaEventRecord(g_timer.ev[2 * slot], s);
   }
   cudaError_t e = launch();
@@ -211,7 +215,8 @@ VP_EXPORT vp_status vp_embed_bwd(const int64_t* ids, const void* dOut, float* dW
   if (ws_bytes < embed_bwd_workspace(N, H)) return VP_ERR_WORKSPACE;
   cudaStream_t s = as_stream(stream);
   cudaError_t e =
-      timed(kEmbedBwd, s, [&] { return embed_bwd(ids, dOut, dW, N, H, V, es, accumulate != 0, workspace, s); });
+      timed(kEmbedBwd, s, [&] { return embed_bwd(ids, dOut, dW, N, H, V, es, accumulate != 0, workspace, s); },
+            embed_bwd_kernels(N));
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
 }
 
@@ -287,7 +292,7 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd(const void* X, const void* W, const int64_t
     e = timed(kMerge, s, [&] {
       return lse_merge(partial, zy, targets, N, V, Vs, T, L.tile_v, L.maxseg, ignore_index, loss, lse, shard_stats,
                        s);
-    });
+    }, kMergeKernels);
   if (e == cudaSuccess && (loss_mean || n_bad))
     e = timed(kMean, s, [&] { return loss_mean_and_bad(loss, targets, N, V, ignore_index, loss_mean, n_bad, s); });
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
@@ -394,7 +399,7 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int
       e = timed(kMerge, s, [&] {
         return lse_merge_ld(partial, zy, yc, nc, V, Vs, T, kBf16TileV, L.maxseg, ignore_index, loss + n0, lse + n0,
                             shard_stats ? shard_stats + n0 : nullptr, N, s);
-      });
+      }, kMergeKernels);
     if (e == cudaSuccess)
       e = timed(kDzFromP, s, [&] { return dz_from_p(P, L.ldp, tmax, lse + n0, g + n0, yc, nc, V, s); });
     // dW = sum over token chunks of dZ_c^T X_c; dX rows of this chunk are complete
@@ -437,21 +442,26 @@ VP_EXPORT vp_status vp_stage_timing_enable(int max_launches) {
     for (int i = 0; i < 2 * t.cap; ++i) cudaEventDestroy(t.ev[i]);
     delete[] t.ev;
     delete[] t.stage;
+    delete[] t.kernels;
     t.ev = nullptr;
     t.stage = nullptr;
+    t.kernels = nullptr;
   }
   t.cap = 0;
   t.used = 0;
   if (max_launches <= 0) return VP_OK;
   t.ev = new cudaEvent_t[2 * max_launches];
   t.stage = new int[max_launches];
+  t.kernels = new int[max_launches];
   for (int i = 0; i < 2 * max_launches; ++i) {
     if (cudaEventCreate(&t.ev[i]) != cudaSuccess) {
       for (int j = 0; j < i; ++j) cudaEventDestroy(t.ev[j]);
       delete[] t.ev;
       delete[] t.stage;
+      delete[] t.kernels;
       t.ev = nullptr;
       t.stage = nullptr;
+      t.kernels = nullptr;
       return VP_ERR_CUDA;
     }
   }
@@ -472,7 +482,7 @@ VP_EXPORT int vp_stage_timing_read(float* ms, int32_t* counts, int n) {
     const int s = t.stage[i];
     if (s < n) {
       if (ms) ms[s] += x;
-      if (counts) counts[s] += 1;
+      if (counts) counts[s] += t.kernels[i];
     }
   }
   return kNumStages;

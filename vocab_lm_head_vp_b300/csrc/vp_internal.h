@@ -73,6 +73,7 @@ cudaError_t embed_gather(const int64_t* ids, const void* W, void* out, int64_t N
 
 // ---- embedding backward (embed_bwd.cu)
 size_t embed_bwd_workspace(int64_t N, int64_t H);
+int embed_bwd_kernels(int64_t N);   // kernels one call launches (the dW memset not counted)
 cudaError_t embed_bwd(const int64_t* ids, const void* dOut, float* dW, int64_t N, int64_t H, int64_t V, int esize,
                       bool accumulate, void* workspace, cudaStream_t stream);
 
