@@ -488,7 +488,7 @@ def run_ours(args):
     dx_b = N * V * 2 + V * H * 2 + N * H * 2
     gemm_alg_bytes = ((lse_b + dw_b + dx_b) / 3 if args.path == "fused" else (lse_b + dz_b + dw_b + dx_b) / 4)
     extra = {}
-    if args.path == "fused":
+    if args.path == "fused" and stages.get("dz_from_p", (0.0, 0))[1] > 0:
         dzp_ms, dzp_n = stages["dz_from_p"]
         valid_rows = int(((inp.targets >= 0) & (inp.targets < V)).sum())
         # read fp16 p and write bf16 dZ for valid rows; write zeros for ignored ones

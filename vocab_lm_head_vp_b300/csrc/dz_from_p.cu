@@ -7,8 +7,11 @@
 //     P[n, j] = fp16(exp(z_nj - tmax[k][n]))        (j inside tile k)
 // where tmax[k][n] is the row's maximum over that tile.  Once the merge has
 // produced lse_n, the softmax is p_nj = P[n, j] * exp(tmax[k][n] - lse_n), so
-//     dZ[n, j] = bf16( c_nk * P[n, j] - g_n 1[j = y_n] ),  c_nk = g_n exp(tmax[k][n] - lse_n),
-// written over P in place (both elements are 2 bytes).
+//     dZ[n, j] = bf16( c_nk * P[n, j] - g_n 1[j = y_n] ),  c_nk = g_n exp(tmax[k][n] - lse_n).
+//
+// tile_scale turns tmax into c in place (one multiply per element is left for
+// the pass over P); dz_from_p then writes dZ over P in place (both elements
+// are 2 bytes).
 //
 // HBM-bound elementwise pass: 16-byte vectors (8 elements, all inside one
 // tile), consecutive threads on consecutive vectors of a row, kDzVecs vectors
@@ -47,10 +50,20 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t h2, float c, int j0, int
   return *reinterpret_cast<uint32_t*>(&o);
 }
 
+__global__ void tile_scale_kernel(float* __restrict__ tmax_c, const float* __restrict__ lse,
+                                  const float* __restrict__ g, int64_t N, int64_t ntiles) {
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  const float gn = g[n], ln = lse[n];
+  for (int64_t k = blockIdx.y; k < ntiles; k += gridDim.y) {
+    float* x = tmax_c + k * N + n;
+    *x = gn * expf(*x - ln);
+  }
+}
+
 __global__ void __launch_bounds__(kDzThreads, VP_DZ_MIN_BLOCKS)
-    dz_from_p_kernel(uint4* __restrict__ buf, int64_t ldv, int64_t nvec, const float* __restrict__ tmax,
-                     const float* __restrict__ lse, const float* __restrict__ g, const int64_t* __restrict__ targets,
-                     int64_t N) {
+    dz_from_p_kernel(uint4* __restrict__ buf, int64_t ldv, int64_t nvec, const float* __restrict__ cscale,
+                     const float* __restrict__ g, const int64_t* __restrict__ targets, int64_t N) {
   const int64_t base = static_cast<int64_t>(blockIdx.x) * (kDzThreads * kDzVecs) + threadIdx.x;
   for (int64_t n = blockIdx.y; n < N; n += gridDim.y) {
     const float gn = g[n];
@@ -63,7 +76,6 @@ __global__ void __launch_bounds__(kDzThreads, VP_DZ_MIN_BLOCKS)
       }
       continue;
     }
-    const float ln = lse[n];
     const int64_t y = targets[n];
     uint4 v[kDzVecs];
 #pragma unroll
@@ -76,7 +88,7 @@ __global__ void __launch_bounds__(kDzThreads, VP_DZ_MIN_BLOCKS)
       const int64_t idx = base + u * kDzThreads;
       if (idx < nvec) {
         const int64_t j0 = idx * 8;
-        const float c = gn * expf(tmax[(j0 / kBf16TileV) * N + n] - ln);
+        const float c = cscale[(j0 / kBf16TileV) * N + n];
         const int64_t yl = y - j0;   // target position inside this vector, if 0 <= yl < 8
         uint4 o;
         o.x = scale_pair(v[u].x, c, 0, yl, gn);
@@ -91,14 +103,22 @@ __global__ void __launch_bounds__(kDzThreads, VP_DZ_MIN_BLOCKS)
 
 }  // namespace
 
-cudaError_t dz_from_p(void* P, int64_t ldp, const float* tmax, const float* lse, const float* g,
-                      const int64_t* targets, int64_t N, int64_t V, cudaStream_t stream) {
+cudaError_t tile_scale(float* tmax_c, const float* lse, const float* g, int64_t N, int64_t V, cudaStream_t stream) {
+  if (N <= 0 || V <= 0) return cudaSuccess;
+  const int64_t ntiles = (V + kBf16TileV - 1) / kBf16TileV;
+  const dim3 grid(static_cast<unsigned>((N + 255) / 256), static_cast<unsigned>(ntiles < 65535 ? ntiles : 65535));
+  tile_scale_kernel<<<grid, 256, 0, stream>>>(tmax_c, lse, g, N, ntiles);
+  return cudaGetLastError();
+}
+
+cudaError_t dz_from_p(void* P, int64_t ldp, const float* cscale, const float* g, const int64_t* targets, int64_t N,
+                      int64_t V, cudaStream_t stream) {
   if (N <= 0 || V <= 0) return cudaSuccess;
   const int64_t nvec = (V + 7) / 8;   // vectors holding columns < V (the last may run into the row padding)
   const int64_t per_block = kDzThreads * kDzVecs;
   const dim3 grid(static_cast<unsigned>((nvec + per_block - 1) / per_block),
                   static_cast<unsigned>(N < 65535 ? N : 65535));
-  dz_from_p_kernel<<<grid, kDzThreads, 0, stream>>>(static_cast<uint4*>(P), ldp / 8, nvec, tmax, lse, g, targets, N);
+  dz_from_p_kernel<<<grid, kDzThreads, 0, stream>>>(static_cast<uint4*>(P), ldp / 8, nvec, cscale, g, targets, N);
   return cudaGetLastError();
 }
 
