@@ -475,9 +475,10 @@ def run_ours(args):
     gstages = GEMM_STAGES[args.path]
     gemm_ms = sum(stages[s][0] for s in gstages)
     gemm_n = sum(stages[s][1] for s in gstages)
-    per_launch_flops = 2.0 * N * H * V          # every GEMM launch: all N tokens x all V
-    avg_launch_s = gemm_ms / max(1, gemm_n) / 1e3
-    achieved = per_launch_flops / avg_launch_s / 1e12
+    # every step's GEMM launches together do 2NHV per stage (a stage may run as several
+    # token or vocab chunks): achieved = those flops / the launches' time
+    gemm_flops = 2.0 * N * H * V * len(gstages) * args.steps
+    achieved = gemm_flops / (gemm_ms / 1e3) / 1e12
     emb_ms, emb_n = stages["embed_gather"]
     emb_bytes = 2.0 * N * H * 2 + 8.0 * N
     emb_gbs = emb_bytes / (emb_ms / max(1, emb_n) / 1e3) / 1e9
@@ -487,6 +488,7 @@ def run_ours(args):
     dw_b = N * V * 2 + N * H * 2 + V * H * 4
     dx_b = N * V * 2 + V * H * 2 + N * H * 2
     gemm_alg_bytes = ((lse_b + dw_b + dx_b) / 3 if args.path == "fused" else (lse_b + dz_b + dw_b + dx_b) / 4)
+    gemm_launches_per_stage = gemm_n / max(1, len(gstages) * args.steps)   # > 1 when a stage runs in chunks
     extra = {}
     if args.path == "fused" and stages.get("dz_from_p", (0.0, 0))[1] > 0:
         dzp_ms, dzp_n = stages["dz_from_p"]
@@ -515,8 +517,10 @@ def run_ours(args):
                      "peak_kind": f"bf16 sustained ({peaks['source']})",
                      "frac_of_burst": achieved / peaks["bf16_tflops"],
                      "traffic": gemm_traffic(wl.name, args.path, args.gemm_variant),
-                     "traffic_unit": "bytes per launch (ncu dram read + write)",
-                     "algorithmic_bytes_per_launch": gemm_alg_bytes},
+                     "launches_per_gemm_stage": gemm_launches_per_stage,
+                     "traffic_unit": "bytes per GEMM stage (one 2NHV contraction; ncu dram read + write, "
+                                     "summed over the stage's launches)",
+                     "algorithmic_bytes_per_stage": gemm_alg_bytes},
         "roofline_embed": embed_roofline(emb_gbs, emb_micro, peaks),
         "embed_bwd": None if emb_bwd_micro is None else {
             "kernel": "vp_embed_bwd (key sort + run sums + cross-run sums), accumulate into fp32 dW",
