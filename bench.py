@@ -64,11 +64,11 @@ def parse_args():
 # the three GEMM launches over four steps).  They describe the kernel built from the
 # sources hashed here; once those change, `traffic` is reported as null until a
 # new capture replaces the number.
-GEMM_TRAFFIC = {"workload": "v128k", "path": "fused", "gemm_variant": "single", "bytes_per_launch": 22.51e9,
-                "by_launch": {"lse_p_gemm": 8.73e9, "dw_gemm": 22.23e9, "dx_gemm": 36.58e9},
+GEMM_TRAFFIC = {"workload": "v128k", "path": "fused", "gemm_variant": "single", "bytes_per_launch": 24.71e9,
+                "by_launch": {"lse_p_gemm": 8.79e9, "dw_gemm": 22.24e9, "dx_gemm": 43.11e9},
                 "sources": ("vocab_lm_head_vp_b300/csrc/ce_bf16.cu", "vocab_lm_head_vp_b300/csrc/ptx.cuh",
                             "vocab_lm_head_vp_b300/csrc/umma_gemm.cuh"),
-                "sha256": "f45b566df537368b5861aa3391cb8f3f545ee0261f3894d3c053ba4c2b1a2876"}
+                "sha256": "b5c88f904b1c2f9c6bf5cd867ebd51e2bde69365f70e54f22a882d7f23862dd9"}
 
 
 def gemm_traffic(workload, path, variant):
@@ -209,7 +209,8 @@ def embed_roofline(in_step_gbs, micro, peaks):
     if micro:
         a = micro["v128k_uniform"]["GB/s"]
         r.update({"achieved": a, "frac": a / peaks["hbm_gbs"], "frac_of_8TBs": a / 8000.0,
-                  "workload": "v128k shape (N=16384, H=4096, V=128256), uniform ids, L2 flushed before each launch",
+                  "workload": ("v128k shape (N=16384, H=4096, V=128256), uniform ids, L2 flushed before each "
+                               "launch, differential timing (flush+gather minus flush)"),
                   "cases": micro})
     else:
         r.update({"achieved": in_step_gbs, "frac": in_step_gbs / peaks["hbm_gbs"],
@@ -266,10 +267,12 @@ def workload_config(wl):
 
 # ------------------------------------------------------------------ embedding gather alone
 def embed_microbench(vp, dev, iters=20):
-    """vp_embed_fwd timed launch by launch (CUDA events on the launching
-    stream) at the V128k and V152k shapes, uniform and Zipf(1.1) ids, with the
-    L2 flushed (a 256 MB write) before every launch.  Algorithmic bytes per
-    launch: read N rows + write N rows + N int64 ids."""
+    """vp_embed_fwd at the V128k and V152k shapes, uniform and Zipf(1.1) ids,
+    with the L2 flushed (a 256 MB write) before every launch.  Differential
+    timing on the launching stream: `iters` x (flush, gather) between one pair
+    of CUDA events, minus `iters` x flush alone, so per-launch event overhead
+    (several microseconds against a ~40 us kernel) stays out.  Algorithmic
+    bytes per launch: read N rows + write N rows + N int64 ids."""
     import torch
     import synth
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -282,17 +285,23 @@ def embed_microbench(vp, dev, iters=20):
         rng = np.random.default_rng(wl.seed)
         for kind, ids in (("uniform", rng.integers(0, wl.V, wl.N)), ("zipf", synth.zipf_ids(rng, wl.N, wl.V, 1.1))):
             idt = torch.from_numpy(ids).to(dev)
-            times = []
-            for i in range(iters + 3):
-                flush.zero_()
+
+            def loop(with_gather):
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
                 e0.record()
-                vp.embed_fwd(idt, W, wl.T, out=o)
+                for _ in range(iters):
+                    flush.zero_()
+                    if with_gather:
+                        vp.embed_fwd(idt, W, wl.T, out=o)
                 e1.record()
                 torch.cuda.synchronize()
-                if i >= 3:
-                    times.append(e0.elapsed_time(e1))
-            ms = statistics.median(times)
+                return e0.elapsed_time(e1)
+
+            loop(True)   # warm-up
+            both = [loop(True) for _ in range(3)]
+            alone = [loop(False) for _ in range(3)]
+            ms = (statistics.median(both) - statistics.median(alone)) / iters
             nbytes = 2.0 * wl.N * wl.H * 2 + 8.0 * wl.N
             out[f"{name}_{kind}"] = {"N": wl.N, "H": wl.H, "V": wl.V, "ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9}
         del W, o
@@ -302,8 +311,9 @@ def embed_microbench(vp, dev, iters=20):
 def embed_bwd_microbench(vp, dev, iters=20):
     """vp_embed_bwd (accumulate into the tied weight's fp32 gradient) at the
     V128k shape with the workload's Zipf ids and with uniform ids, L2 flushed
-    before every launch.  Algorithmic bytes: read dOut (N x H bf16) and the
-    ids, read and write every touched fp32 row of dW once."""
+    before every call, differential timing as in embed_microbench.
+    Algorithmic bytes: read dOut (N x H bf16) and the ids, read and write
+    every touched fp32 row of dW once."""
     import torch
     import synth
     wl = synth.WORKLOADS["v128k"]
@@ -317,17 +327,23 @@ def embed_bwd_microbench(vp, dev, iters=20):
     out = {}
     for kind, ids in (("zipf", synth.zipf_ids(rng, wl.N, wl.V, 1.1)), ("uniform", rng.integers(0, wl.V, wl.N))):
         idt = torch.from_numpy(ids).to(dev)
-        times = []
-        for i in range(iters + 3):
-            flush.zero_()
+
+        def loop(with_bwd):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
             e0.record()
-            vp.embed_bwd(idt, G, wl.V, wl.T, dW=dW, accumulate=True, workspace=ws)
+            for _ in range(iters):
+                flush.zero_()
+                if with_bwd:
+                    vp.embed_bwd(idt, G, wl.V, wl.T, dW=dW, accumulate=True, workspace=ws)
             e1.record()
             torch.cuda.synchronize()
-            if i >= 3:
-                times.append(e0.elapsed_time(e1))
-        ms = statistics.median(times)
+            return e0.elapsed_time(e1)
+
+        loop(True)   # warm-up
+        both = [loop(True) for _ in range(3)]
+        alone = [loop(False) for _ in range(3)]
+        ms = (statistics.median(both) - statistics.median(alone)) / iters
         distinct = len(np.unique(ids))
         nbytes = wl.N * wl.H * 2.0 + 8.0 * wl.N + 2.0 * distinct * wl.H * 4
         out[kind] = {"ms": ms, "distinct_ids": distinct, "alg_bytes": nbytes, "GB/s": nbytes / (ms / 1e3) / 1e9}
@@ -524,7 +540,8 @@ def run_ours(args):
         "roofline_embed": embed_roofline(emb_gbs, emb_micro, peaks),
         "embed_bwd": None if emb_bwd_micro is None else {
             "kernel": "vp_embed_bwd (key sort + run sums + cross-run sums), accumulate into fp32 dW",
-            "workload": "v128k shape, L2 flushed before each launch", "bound": "hbm", "unit": "GB/s",
+            "workload": "v128k shape, L2 flushed before each call, differential timing", "bound": "hbm",
+            "unit": "GB/s",
             "peak": peaks["hbm_gbs"], "cases": emb_bwd_micro},
         **extra,
         "stages_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in stages.items() if v[1]},
