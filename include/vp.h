@@ -23,8 +23,9 @@
  *     FMAs (no TF32) for full fp32 accuracy.
  *   - Arguments are checked before any launch: N, H, V, T <= 0 or V % T != 0
  *     -> VP_ERR_INVALID_ARG; a NULL required pointer -> VP_ERR_INVALID_ARG;
- *     a pointer not 16-byte aligned or H*sizeof(dtype) not a multiple of 16
- *     -> VP_ERR_UNSUPPORTED; a workspace smaller than the minimum
+ *     a pointer not 16-byte aligned, H*sizeof(dtype) not a multiple of 16,
+ *     or a GEMM with 2^31 or more 128x256 output tiles (N*V, V*H or N*H
+ *     beyond about 7e13) -> VP_ERR_UNSUPPORTED; a workspace smaller than the minimum
  *     -> VP_ERR_WORKSPACE; a CUDA launch error -> VP_ERR_CUDA.  On any error
  *     nothing has been launched or written, except for VP_ERR_CUDA.
  *   - Every wait inside a kernel is bounded in time.  A wait that runs out

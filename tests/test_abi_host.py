@@ -148,3 +148,11 @@ def test_embed_sp_rejects_bad_arguments(lib):
     assert f(ids, W, out, 12, 8, 16, 4, 4, vp.VP_BF16, None) == 1     # rank >= T
     assert f(ids, W, out, 12, 8, 16, 4, -1, vp.VP_BF16, None) == 1
     assert f(ids, W, P(0x3008), 12, 8, 16, 4, 1, vp.VP_BF16, None) == 2
+
+
+def test_rejects_tile_counts_beyond_int32(lib):
+    X, W, y, ws = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
+    loss, lse = P(0x50000), P(0x60000)
+    N, V = (1 << 31) - 1, (1 << 31) - 2          # 2^24 x 2^23 logits tiles
+    assert lib.vp_lmhead_ce_fwd(X, W, y, N, 64, V, 2, -100, vp.VP_BF16, loss, lse, None, None, None, ws, 1 << 40,
+                                None) == 2

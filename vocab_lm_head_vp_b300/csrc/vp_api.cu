@@ -43,6 +43,14 @@ bool shape_ok(int64_t N, int64_t H, int64_t V, int T) {
          H < (int64_t(1) << 31);
 }
 
+// The persistent GEMMs number their 128 x 256 output tiles with 32-bit ints:
+// logits [N, V], dW [V, H] and dX [N, H] must each have fewer than 2^31 tiles.
+bool tiles_ok(int64_t N, int64_t H, int64_t V) {
+  const auto tiles = [](int64_t m, int64_t n) { return ((m + 127) / 128) * ((n + 255) / 256); };
+  const int64_t lim = int64_t(1) << 31;
+  return tiles(N, V) < lim && tiles(V, H) < lim && tiles(N, H) < lim;
+}
+
 // ---------------- forward workspace: header | partial records | z_y
 struct FwdLayout {
   int tile_v, maxseg;
@@ -253,6 +261,7 @@ VP_EXPORT size_t vp_lmhead_ce_workspace_size(int64_t N, int64_t H, int64_t V, in
 static vp_status check_args(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H, int64_t V,
                             int T, vp_dtype dtype, const void* ws) {
   if (!X || !W || !targets || !ws || !dtype_ok(dtype) || !shape_ok(N, H, V, T)) return VP_ERR_INVALID_ARG;
+  if (!tiles_ok(N, H, V)) return VP_ERR_UNSUPPORTED;
   if (!aligned16(X) || !aligned16(W) || !aligned16(ws) || (H * esize_of(dtype)) % 16 != 0) return VP_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(targets) & 7u) != 0) return VP_ERR_UNSUPPORTED;
   return VP_OK;
