@@ -12,9 +12,11 @@
 //
 // Deterministic, no atomics:
 //   1. keys (id << 32 | n) for valid ids, all-ones for the rest and the
-//      padding, bitonic-sorted: blocks sort 4096-key chunks in shared memory,
-//      longer merges take one global pass per step above the chunk and finish
-//      in shared memory.  The sorted order groups tokens by id, by n within.
+//      padding, sorted: blocks bitonic-sort 512-key chunks in shared memory,
+//      then groups of up to 8 sorted runs merge in one pass each, every key
+//      placing itself at its rank (binary searches in the other runs of its
+//      group; the keys are distinct, the all-ones ones tie-broken by run).
+//      The sorted order groups tokens by id, by n within.
 //   2. runs of kRun sorted positions: one thread per 16-byte column vector of
 //      the row walks the run in order and sums; a segment (one id) that starts
 //      and ends inside the run is added to dW at once, a segment cut by the
@@ -34,8 +36,9 @@ namespace {
 
 constexpr uint64_t kSentinel = ~0ull;
 constexpr uint32_t kNoId = 0xffffffffu;
-constexpr int kChunk = 4096;          // keys sorted per block in shared memory
-constexpr int kSortThreads = 1024;
+constexpr int kChunk = 512;           // keys sorted per block in shared memory
+constexpr int kMergeWays = 8;         // sorted runs merged per pass
+constexpr int kSortThreads = 256;
 constexpr int kRun = 32;              // sorted positions per run
 constexpr int kRedThreads = 256;
 
@@ -53,13 +56,14 @@ __global__ void make_keys_kernel(const int64_t* __restrict__ ids, int64_t N, int
   keys[i] = k;
 }
 
-// Compare-exchange step j of merge size k on `len` keys in shared memory whose
-// first key has global index gbase.  Pair p -> (i, i + j).
-__device__ __forceinline__ void smem_step(uint64_t* s, int len, int64_t gbase, int64_t k, int j) {
+// Compare-exchange step j of merge size k on `len` keys in shared memory.
+// Pair p -> (i, i + j); the direction follows the key's index inside the
+// chunk, so the last merge (k = len) leaves the chunk ascending.
+__device__ __forceinline__ void smem_step(uint64_t* s, int len, int k, int j) {
   for (int p = threadIdx.x; p < len / 2; p += blockDim.x) {
     const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
     const int l = i + j;
-    const bool asc = ((gbase + i) & k) == 0;
+    const bool asc = (i & k) == 0;
     const uint64_t a = s[i], b = s[l];
     if ((a > b) == asc) {
       s[i] = b;
@@ -69,39 +73,53 @@ __device__ __forceinline__ void smem_step(uint64_t* s, int len, int64_t gbase, i
   __syncthreads();
 }
 
-// Full bitonic sort of each chunk of len = min(kChunk, n_pad) keys, merge sizes 2..len.
+// Bitonic sort of each chunk of len = min(kChunk, n_pad) keys into ascending
+// order (merge sizes 2..len), ready for the rank merges.
 __global__ void __launch_bounds__(kSortThreads) bitonic_chunk_sort(uint64_t* __restrict__ keys, int len) {
   __shared__ uint64_t s[kChunk];
   const int64_t gbase = static_cast<int64_t>(blockIdx.x) * len;
   for (int i = threadIdx.x; i < len; i += blockDim.x) s[i] = keys[gbase + i];
   __syncthreads();
   for (int k = 2; k <= len; k <<= 1)
-    for (int j = k >> 1; j > 0; j >>= 1) smem_step(s, len, gbase, k, j);
+    for (int j = k >> 1; j > 0; j >>= 1) smem_step(s, len, k, j);
   for (int i = threadIdx.x; i < len; i += blockDim.x) keys[gbase + i] = s[i];
 }
 
-// Steps j = kChunk/2 .. 1 of merge size k (> kChunk) inside each chunk.
-__global__ void __launch_bounds__(kSortThreads) bitonic_chunk_merge(uint64_t* __restrict__ keys, int64_t k) {
-  __shared__ uint64_t s[kChunk];
-  const int64_t gbase = static_cast<int64_t>(blockIdx.x) * kChunk;
-  for (int i = threadIdx.x; i < kChunk; i += blockDim.x) s[i] = keys[gbase + i];
-  __syncthreads();
-  for (int j = kChunk >> 1; j > 0; j >>= 1) smem_step(s, kChunk, gbase, k, j);
-  for (int i = threadIdx.x; i < kChunk; i += blockDim.x) keys[gbase + i] = s[i];
-}
-
-// One global step (j >= kChunk) of merge size k: a thread per pair.
-__global__ void bitonic_global_step(uint64_t* __restrict__ keys, int64_t n_pad, int64_t k, int64_t j) {
-  const int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (p >= n_pad / 2) return;
-  const int64_t i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
-  const int64_t l = i + j;
-  const bool asc = (i & k) == 0;
-  const uint64_t a = keys[i], b = keys[l];
-  if ((a > b) == asc) {
-    keys[i] = b;
-    keys[l] = a;
+// Merge each group of G consecutive sorted runs of L keys (G, L, n_pad powers
+// of two, G * L dividing n_pad): a key's place in its group is its index in
+// its own run plus, for every other run of the group, the keys there that
+// precede it (an earlier run's equal keys first).  The G - 1 binary searches
+// advance in lockstep, one independent load per run and round.
+__global__ void rank_merge_kernel(const uint64_t* __restrict__ in, uint64_t* __restrict__ out, int64_t n_pad,
+                                  int64_t L, int G) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n_pad) return;
+  const int64_t run = i / L;
+  const int64_t first = run / G * G;
+  const uint64_t key = in[i];
+  int64_t lo[kMergeWays], hi[kMergeWays];
+#pragma unroll
+  for (int r = 0; r < kMergeWays; ++r) {
+    lo[r] = 0;
+    hi[r] = (r < G && first + r != run) ? L : 0;   // no search in the own run or past the group
   }
+  for (int64_t span = L; span > 0; span >>= 1) {   // log2(L) + 1 rounds finish every search
+#pragma unroll
+    for (int r = 0; r < kMergeWays; ++r) {
+      if (lo[r] < hi[r]) {
+        const int64_t mid = (lo[r] + hi[r]) >> 1;
+        const uint64_t x = in[(first + r) * L + mid];
+        if (first + r < run ? x <= key : x < key)
+          lo[r] = mid + 1;
+        else
+          hi[r] = mid;
+      }
+    }
+  }
+  int64_t pos = i - run * L;
+#pragma unroll
+  for (int r = 0; r < kMergeWays; ++r) pos += lo[r];
+  out[first * L + pos] = key;
 }
 
 // 16 bytes of an upstream row as fp32 values: 8 bf16 or 4 f32.
@@ -160,12 +178,15 @@ __device__ __forceinline__ uint64_t key_at(const uint64_t* keys, int64_t n_pad, 
 template <int ESIZE>
 __global__ void __launch_bounds__(kRedThreads)
     embed_bwd_runs_kernel(const uint64_t* __restrict__ keys, int64_t n_pad, const uint4* __restrict__ dOut,
-                          int64_t rowvec, float* __restrict__ dW, int64_t H, float* __restrict__ head,
+                          int64_t rowvec, float* __restrict__ dW, int64_t H, int64_t V, float* __restrict__ head,
                           float* __restrict__ tail) {
   __shared__ uint64_t sk[kRun + 2];
   const int64_t r = blockIdx.x;
   const int64_t p0 = r * kRun;
-  for (int i = threadIdx.x; i < kRun + 2; i += blockDim.x) sk[i] = key_at(keys, n_pad, p0 - 1 + i);
+  for (int i = threadIdx.x; i < kRun + 2; i += blockDim.x) {
+    const uint64_t k = key_at(keys, n_pad, p0 - 1 + i);
+    sk[i] = key_id(k) < V ? k : kSentinel;   // an id outside [0, V) can only be a sentinel; never index dW with it
+  }
   __syncthreads();
   const int64_t v = static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x;
   if (v >= rowvec || key_id(sk[1]) == kNoId) return;
@@ -216,25 +237,46 @@ __global__ void __launch_bounds__(kRedThreads)
 // segment's partials in run order.
 template <int ESIZE>
 __global__ void __launch_bounds__(kRedThreads)
-    embed_bwd_cross_kernel(const uint64_t* __restrict__ keys, int64_t n_pad, int64_t runs, int64_t rowvec,
-                           float* __restrict__ dW, int64_t H, const float* __restrict__ head,
+    embed_bwd_cross_kernel(const uint64_t* __restrict__ keys, int64_t n_pad, int64_t rowvec,
+                           float* __restrict__ dW, int64_t H, int64_t V, int64_t runs, const float* __restrict__ head,
                            const float* __restrict__ tail) {
   const int64_t r = blockIdx.x;
   const int64_t last = (r + 1) * kRun - 1;
   const uint32_t id = key_id(key_at(keys, n_pad, last));
-  if (id == kNoId || key_id(key_at(keys, n_pad, last + 1)) != id) return;   // nothing continues past run r
+  if (id >= V || key_id(key_at(keys, n_pad, last + 1)) != id) return;   // nothing continues past run r
   if (key_id(key_at(keys, n_pad, r * kRun - 1)) == id) return;              // the segment started earlier
   const int64_t v = static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x;
   if (v >= rowvec) return;
+  // the segment's last position: just before the first key with a larger id
+  const uint64_t bound = (static_cast<uint64_t>(id) + 1) << 32;
+  int64_t lo = last + 1, hi = n_pad;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (keys[mid] < bound)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  int64_t end_run = (lo - 1) / kRun;   // the run where the segment ends (its head slot is the last part)
+  if (end_run >= runs) end_run = runs - 1;
   constexpr int kN = Vec<ESIZE>::kN;
   const int64_t col = v * kN;
   float s[kN];
 #pragma unroll
   for (int q = 0; q < kN; ++q) s[q] = tail[r * H + col + q];
-  for (int64_t r2 = r + 1; r2 < runs; ++r2) {
+  // head slots of runs r+1 .. end_run, loaded 8 runs at a time, added in run order
+  for (int64_t r0 = r + 1; r0 <= end_run; r0 += 8) {
+    float h[8][kN];
 #pragma unroll
-    for (int q = 0; q < kN; ++q) s[q] += head[r2 * H + col + q];
-    if (key_id(key_at(keys, n_pad, (r2 + 1) * kRun)) != id) break;   // the segment ends in run r2
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int q = 0; q < kN; ++q) h[u][q] = r0 + u <= end_run ? head[(r0 + u) * H + col + q] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (r0 + u <= end_run) {
+#pragma unroll
+        for (int q = 0; q < kN; ++q) s[q] += h[u][q];
+      }
   }
   Vec<ESIZE> a;
 #pragma unroll
@@ -253,24 +295,22 @@ int64_t pad_pow2(int64_t n) {
 int embed_bwd_kernels(int64_t N) {
   const int64_t n_pad = pad_pow2(N);
   int k = 4;   // keys, chunk sort, run sums, cross-run sums
-  for (int64_t m = 2 * kChunk; m <= n_pad; m <<= 1) {
-    for (int64_t j = m >> 1; j >= kChunk; j >>= 1) ++k;   // global steps
-    ++k;                                                   // the chunk merge
-  }
+  for (int64_t L = n_pad < kChunk ? n_pad : kChunk; L < n_pad; L *= kMergeWays) ++k;   // merge passes
   return k;
 }
 
 size_t embed_bwd_workspace(int64_t N, int64_t H) {
   const int64_t runs = (N + kRun - 1) / kRun;
-  return size_t(pad_pow2(N)) * sizeof(uint64_t) + 2 * size_t(runs) * H * sizeof(float);
+  return 2 * size_t(pad_pow2(N)) * sizeof(uint64_t) + 2 * size_t(runs) * H * sizeof(float);
 }
 
 cudaError_t embed_bwd(const int64_t* ids, const void* dOut, float* dW, int64_t N, int64_t H, int64_t V, int esize,
                       bool accumulate, void* workspace, cudaStream_t stream) {
   const int64_t n_pad = pad_pow2(N);
   const int64_t runs = (N + kRun - 1) / kRun;
-  uint64_t* keys = static_cast<uint64_t*>(workspace);
-  float* head = reinterpret_cast<float*>(keys + n_pad);
+  uint64_t* keys = static_cast<uint64_t*>(workspace);   // two n_pad buffers, sorted in turn
+  uint64_t* spare = keys + n_pad;
+  float* head = reinterpret_cast<float*>(keys + 2 * n_pad);
   float* tail = head + runs * H;
   cudaError_t e = cudaSuccess;
   if (!accumulate) e = cudaMemsetAsync(dW, 0, size_t(V) * H * sizeof(float), stream);
@@ -278,20 +318,23 @@ cudaError_t embed_bwd(const int64_t* ids, const void* dOut, float* dW, int64_t N
   make_keys_kernel<<<static_cast<unsigned>((n_pad + 255) / 256), 256, 0, stream>>>(ids, N, V, keys, n_pad);
   const int len = static_cast<int>(n_pad < kChunk ? n_pad : kChunk);
   bitonic_chunk_sort<<<static_cast<unsigned>(n_pad / len), kSortThreads, 0, stream>>>(keys, len);
-  for (int64_t k = 2 * kChunk; k <= n_pad; k <<= 1) {
-    for (int64_t j = k >> 1; j >= kChunk; j >>= 1)
-      bitonic_global_step<<<static_cast<unsigned>((n_pad / 2 + 255) / 256), 256, 0, stream>>>(keys, n_pad, k, j);
-    bitonic_chunk_merge<<<static_cast<unsigned>(n_pad / kChunk), kSortThreads, 0, stream>>>(keys, k);
+  for (int64_t L = len; L < n_pad;) {
+    const int G = static_cast<int>(n_pad / L < kMergeWays ? n_pad / L : kMergeWays);
+    rank_merge_kernel<<<static_cast<unsigned>((n_pad + 255) / 256), 256, 0, stream>>>(keys, spare, n_pad, L, G);
+    uint64_t* t = keys;
+    keys = spare;
+    spare = t;
+    L *= G;
   }
   const int64_t rowvec = H * esize / 16;
   const dim3 grid(static_cast<unsigned>(runs), static_cast<unsigned>((rowvec + kRedThreads - 1) / kRedThreads));
   const uint4* src = static_cast<const uint4*>(dOut);
   if (esize == 2) {
-    embed_bwd_runs_kernel<2><<<grid, kRedThreads, 0, stream>>>(keys, n_pad, src, rowvec, dW, H, head, tail);
-    embed_bwd_cross_kernel<2><<<grid, kRedThreads, 0, stream>>>(keys, n_pad, runs, rowvec, dW, H, head, tail);
+    embed_bwd_runs_kernel<2><<<grid, kRedThreads, 0, stream>>>(keys, n_pad, src, rowvec, dW, H, V, head, tail);
+    embed_bwd_cross_kernel<2><<<grid, kRedThreads, 0, stream>>>(keys, n_pad, rowvec, dW, H, V, runs, head, tail);
   } else {
-    embed_bwd_runs_kernel<4><<<grid, kRedThreads, 0, stream>>>(keys, n_pad, src, rowvec, dW, H, head, tail);
-    embed_bwd_cross_kernel<4><<<grid, kRedThreads, 0, stream>>>(keys, n_pad, runs, rowvec, dW, H, head, tail);
+    embed_bwd_runs_kernel<4><<<grid, kRedThreads, 0, stream>>>(keys, n_pad, src, rowvec, dW, H, V, head, tail);
+    embed_bwd_cross_kernel<4><<<grid, kRedThreads, 0, stream>>>(keys, n_pad, rowvec, dW, H, V, runs, head, tail);
   }
   return cudaGetLastError();
 }
