@@ -38,6 +38,18 @@ METRIC = "fused LM-head+CE fwd+bwd tokens/s and % of bf16 tensor peak at V=12825
 UNIT = "tokens/s"
 GEMM_STAGES = {"split": ("lse_stats_gemm", "dz_recompute_gemm", "dw_gemm", "dx_gemm"),
                "fused": ("lse_p_gemm", "dw_gemm", "dx_gemm")}
+# library stages of the LM head's forward and backward (the gather is timed apart)
+FWD_STAGES = ("lse_stats_gemm", "lse_p_gemm", "lse_merge", "loss_mean", "upstream_scale", "tile_scale")
+BWD_STAGES = ("dz_recompute_gemm", "dz_from_p", "dw_gemm", "dx_gemm")
+
+
+def fwd_bwd_ms(stages, steps):
+    """(forward ms, backward ms) per step from the library's per-kernel events.
+    In the fused call the upstream scale and the tile factors run with the
+    forward; the p -> dZ pass and the two gradient GEMMs are its backward."""
+    f = sum(stages.get(s, (0.0, 0))[0] for s in FWD_STAGES) / steps
+    b = sum(stages.get(s, (0.0, 0))[0] for s in BWD_STAGES) / steps
+    return round(f, 4), round(b, 4)
 
 
 def parse_args():
@@ -466,15 +478,20 @@ def run_ours(args):
             ostep(X, y)
         torch.cuda.synchronize()
         barrier()
+        vp.stage_timing_enable(16 * args.other_path_steps + 64)
         e0.record()
         for _ in range(args.other_path_steps):
             ostep(X, y)
         e1.record()
         torch.cuda.synchronize()
+        ostages = vp.stage_timing_read()
+        vp.stage_timing_enable(0)
         oms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.other_path_steps
         assert all(vp.read_device_status(w) == 0 for w in ows)
+        ofwd, obwd = fwd_bwd_ms(ostages, args.other_path_steps)
         other = {"path": opath, "steps": args.other_path_steps, "ms_per_step": oms,
-                 "value": job_tokens_per_s(N, world, 1, oms / 1e3), "unit": UNIT}
+                 "value": job_tokens_per_s(N, world, 1, oms / 1e3), "unit": UNIT,
+                 "fwd_ms": ofwd, "bwd_ms": obwd}
         del ostep, ows
 
     if rank != 0:
@@ -545,6 +562,8 @@ def run_ours(args):
             "peak": peaks["hbm_gbs"], "cases": emb_bwd_micro},
         **extra,
         "stages_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in stages.items() if v[1]},
+        "fwd_ms_per_step": fwd_bwd_ms(stages, args.steps)[0],
+        "bwd_ms_per_step": fwd_bwd_ms(stages, args.steps)[1],
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": {"value": job_tokens_per_s(N, world, args.e2e_steps, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
