@@ -61,14 +61,19 @@ def parse_args():
     p.add_argument("--workload", default="v128k")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU work budget of the oracle baseline")
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-steps", type=int, default=0,
+                   help="steps of the end-to-end loop (0: as many as the timed region, so both see the same "
+                        "power-capped clocks)")
     p.add_argument("--path", choices=["fused", "split"], default="fused",
                    help="fused: one fwd+bwd call with saved probabilities; split: fwd, then bwd with recompute")
     p.add_argument("--other-path-steps", type=int, default=5, help="timed steps of the other path (0: skip)")
     p.add_argument("--embed-iters", type=int, default=20, help="launches per case of the gather microbench (0: skip)")
     p.add_argument("--gemm-variant", choices=["pair", "single"], default="single",
                    help="tcgen05 GEMM form: 256x256 tiles on SM pairs, or 128x256 tiles on one SM")
-    return p.parse_args()
+    args = p.parse_args()
+    if args.e2e_steps <= 0:
+        args.e2e_steps = args.steps
+    return args
 
 
 # DRAM bytes (read + write) per launch of the tcgen05 GEMM kernel in the fused
@@ -444,18 +449,37 @@ def run_ours(args):
     ms = max_over_ranks(ms, world, dev)
 
     # ---------------- end to end through host buffers (X, targets in; loss out)
+    # As a training loop would: step i+1's inputs are copied from pinned host
+    # memory on a copy stream into the other of two device buffers while step i
+    # computes; each step's per-token loss and mean are read back to the host.
     Xh = to(inp.X_bits).pin_memory()
     yh = torch.from_numpy(inp.targets).pin_memory()
     loss_h = torch.empty(N, dtype=torch.float32).pin_memory()
     mean_h = torch.empty(1, dtype=torch.float32).pin_memory()
-    Xd, yd = torch.empty_like(X), torch.empty_like(y)
+    Xd = [torch.empty_like(X) for _ in range(2)]
+    yd = [torch.empty_like(y) for _ in range(2)]
+    ready = [torch.cuda.Event() for _ in range(2)]   # inputs of a buffer have landed
+    free = [torch.cuda.Event() for _ in range(2)]    # the step reading a buffer has finished
+    compute, copier = torch.cuda.current_stream(dev), torch.cuda.Stream(dev)
+
+    def copy_in(b):
+        with torch.cuda.stream(copier):
+            copier.wait_event(free[b])
+            Xd[b].copy_(Xh, non_blocking=True)
+            yd[b].copy_(yh, non_blocking=True)
+            ready[b].record(copier)
+
     torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        Xd.copy_(Xh, non_blocking=True)
-        yd.copy_(yh, non_blocking=True)
-        step(Xd, yd)
+    copy_in(0)
+    for i in range(args.e2e_steps):
+        b = i % 2
+        compute.wait_event(ready[b])
+        step(Xd[b], yd[b])
+        free[b].record(compute)
+        if i + 1 < args.e2e_steps:
+            copy_in(1 - b)
         loss_h.copy_(fo["loss"], non_blocking=True)
         mean_h.copy_(fo["mean"], non_blocking=True)
     torch.cuda.synchronize()
@@ -568,8 +592,9 @@ def run_ours(args):
         "clocks": clk,
         "e2e": {"value": job_tokens_per_s(N, world, args.e2e_steps, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "note": "X and targets copied from pinned host memory and loss read back every step; "
-                        "the weight W is model state resident in HBM"},
+                "note": "X and targets copied from pinned host memory every step (on a copy stream, into the "
+                        "other of two device buffers while the previous step computes) and the loss read back "
+                        "every step; the weight W is model state resident in HBM"},
         "other_path": other,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -82,3 +82,16 @@ def test_v32k_shape_full_gradients(path):
     b = ref.lmhead_ce_backward(inp.X, inp.W, inp.targets, wl.V)
     ex, ew = rel_fro(np64(dX), b["dX"]), rel_fro(np64(dW), b["dW"])
     assert ex <= 2e-2 and ew <= 2e-2, (ex, ew)
+
+
+def test_fused_full_size_repeatable():
+    """Two fused calls at the V32k shape (all tokens) give bit-identical loss,
+    dX and dW: no atomics in any reduction of the path."""
+    inp = synth.make_inputs("v32k")
+    wl = inp.wl
+    X, W, y = dev_inputs(inp)
+    a = vp.lmhead_ce_fwd_bwd(X, W, y, wl.T)
+    b = vp.lmhead_ce_fwd_bwd(X, W, y, wl.T)
+    torch.cuda.synchronize()
+    for k in ("loss", "lse", "mean", "dX", "dW"):
+        assert torch.equal(a[k], b[k]), k
