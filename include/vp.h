@@ -142,6 +142,9 @@ vp_status vp_embed_bwd(const int64_t* ids, const void* dOut, float* dW,
  *           `vocab_chunk` ids (<= 0 or >= V: one chunk, the fastest).  Any
  *           workspace at least this large for some chunk works; the backward
  *           derives its chunk from the bytes it is given.
+ *   pass 3: the `saved` buffer of vp_lmhead_ce_fwd_keep / vp_lmhead_ce_bwd_saved
+ *           (VP_BF16: about N * (2*round8(V) + 20*V/256) bytes, all N tokens;
+ *           VP_F32: as pass 2).
  *   pass 2: vp_lmhead_ce_fwd_bwd.  VP_BF16: the last argument is a TOKEN
  *           chunk (rounded down to a multiple of 128; <= 0 or >= N: all N
  *           tokens at once, the fastest), about N_c * (2*round8(V) + 20*V/256)
@@ -285,6 +288,42 @@ vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int64_t* targ
                                float* shard_stats, int32_t* n_bad,
                                void* dX, float* dW,
                                void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * vp_lmhead_ce_fwd_keep / vp_lmhead_ce_bwd_saved -- the forward and backward
+ * of vp_lmhead_ce_fwd_bwd as two calls, for when the upstream gradient is
+ * only known later (an autograd backward).
+ *
+ * "Vocab Parallelism" sec. 5.3.2 saves each shard's softmax in the forward
+ * for the local p - onehot of the backward.  vp_lmhead_ce_fwd_keep computes
+ * what vp_lmhead_ce_fwd computes (same kernels, same bits) and leaves, in the
+ * caller's `saved` buffer, p = exp(z - m_tile) in fp16 and the tile maxima
+ * m_tile of every 256-wide vocab tile.  vp_lmhead_ce_bwd_saved then forms
+ * c = g exp(m_tile - lse), dZ = c p - g 1[j=y] in place and runs dW = dZ^T X,
+ * dX = dZ W: 6NHV flops in all, as in the one-call form, against 8NHV for
+ * vp_lmhead_ce_fwd + vp_lmhead_ce_bwd.  The results equal vp_lmhead_ce_fwd_bwd's
+ * bit for bit.
+ *
+ *   saved  device buffer >= vp_lmhead_ce_workspace_size(..., pass 3, 0) bytes,
+ *          16-byte aligned, owned by the caller; it must stay untouched from
+ *          the forward to the backward, and the backward consumes it (one
+ *          backward per forward).
+ *   the other arguments as in vp_lmhead_ce_fwd and vp_lmhead_ce_bwd (lse
+ *   from the forward; dloss / dmean the upstream gradient).
+ * VP_F32 runs vp_lmhead_ce_fwd and the recompute backward in `saved`.
+ */
+vp_status vp_lmhead_ce_fwd_keep(const void* X, const void* W, const int64_t* targets,
+                                int64_t N, int64_t H, int64_t V, int T,
+                                int64_t ignore_index, vp_dtype dtype,
+                                float* loss, float* lse, float* loss_mean,
+                                float* shard_stats, int32_t* n_bad,
+                                void* saved, size_t saved_bytes, void* stream);
+vp_status vp_lmhead_ce_bwd_saved(const void* X, const void* W, const int64_t* targets,
+                                 const float* lse, const float* dloss, const float* dmean,
+                                 int64_t N, int64_t H, int64_t V, int T,
+                                 int64_t ignore_index, vp_dtype dtype,
+                                 void* dX, float* dW,
+                                 void* saved, size_t saved_bytes, void* stream);
 
 /*
  * vp_read_device_status -- synchronise `stream` and copy the device status

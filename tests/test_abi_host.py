@@ -92,7 +92,7 @@ def test_workspace_sizes(lib):
     c = vp.workspace_size(N, H, V, T, vp.VP_BF16, 1, 16032)
     assert c >= N * 15872 * 2 + N * H * 4                              # chunk rounded to 256, + fp32 dX partial
     assert vp.workspace_size(N, H, V, 7, vp.VP_BF16, 1) == 0           # V % T != 0
-    assert vp.workspace_size(6, 64, 16, 4, vp.VP_F32, 3) == 0          # unknown pass
+    assert vp.workspace_size(6, 64, 16, 4, vp.VP_F32, 4) == 0          # unknown pass
 
 
 def test_fused_workspace_sizes(lib):
@@ -156,3 +156,21 @@ def test_rejects_tile_counts_beyond_int32(lib):
     N, V = (1 << 31) - 1, (1 << 31) - 2          # 2^24 x 2^23 logits tiles
     assert lib.vp_lmhead_ce_fwd(X, W, y, N, 64, V, 2, -100, vp.VP_BF16, loss, lse, None, None, None, ws, 1 << 40,
                                 None) == 2
+
+
+def test_keep_saved_rejects_bad_arguments(lib):
+    X, W, y, sv = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
+    loss, lse, dX, dW = P(0x50000), P(0x60000), P(0x70000), P(0x80000)
+    N, H, V, T = 16384, 4096, 128256, 8
+    full = vp.workspace_size(N, H, V, T, vp.VP_BF16, 3)
+    assert full == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2)     # the whole batch's fused state
+    fk, bs = lib.vp_lmhead_ce_fwd_keep, lib.vp_lmhead_ce_bwd_saved
+    assert fk(X, W, y, 300, 64, 1000, 3, -100, vp.VP_BF16, loss, lse, None, None, None, sv, 1 << 30, None) == 1
+    assert fk(X, W, y, 300, 64, 1000, 4, -100, vp.VP_BF16, None, lse, None, None, None, sv, 1 << 30, None) == 1
+    assert fk(X, W, y, 300, 64, 1000, 4, -100, vp.VP_BF16, loss, lse, None, None, None, P(0x40008), 1 << 30,
+              None) == 2
+    assert fk(X, W, y, 300, 64, 1000, 4, -100, vp.VP_BF16, loss, lse, None, None, None, sv, 4096, None) == 3
+    assert bs(X, W, y, lse, None, None, 300, 64, 1000, 4, -100, vp.VP_BF16, None, dW, sv, 1 << 30, None) == 1
+    assert bs(X, W, y, lse, None, None, 300, 64, 1000, 4, -100, vp.VP_BF16, P(0x70008), dW, sv, 1 << 30,
+              None) == 2
+    assert bs(X, W, y, lse, None, None, 300, 64, 1000, 4, -100, vp.VP_BF16, dX, dW, sv, 4096, None) == 3

@@ -143,3 +143,35 @@ def test_fused_loss_scale_dmean():
     b = ref.lmhead_ce_backward(inp.X, inp.W, inp.targets, inp.wl.V)
     assert rel_fro(np64(o["dX"]), 1024.0 * b["dX"]) <= 2e-2
     assert rel_fro(np64(o["dW"]), 1024.0 * b["dW"]) <= 2e-2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_keep_and_saved_backward_match_the_fused_call(dtype):
+    """vp_lmhead_ce_fwd_keep + vp_lmhead_ce_bwd_saved: the oracle's results,
+    and (bf16) the one-call form's bits, with a per-token upstream gradient."""
+    inp = synth.small_case(520, 192, 2000, 4, dtype, seed=41, ignore_frac=0.1)
+    X, W, y = dev_inputs(inp)
+    dloss = np.random.default_rng(3).standard_normal(520)
+    dl = torch.from_numpy(dloss.astype(np.float32)).cuda()
+    f = vp.lmhead_ce_fwd(X, W, y, 4, shard_stats=True, keep=True)
+    dX, dW = vp.lmhead_ce_bwd(X, W, y, f["lse"], 4, dloss=dl, saved=f["saved"])
+    torch.cuda.synchronize()
+    assert vp.read_device_status(f["saved"]) == 0
+    _check(inp, 4, f, dX, dW, dloss=dloss)
+    if dtype == "bf16":
+        o = vp.lmhead_ce_fwd_bwd(X, W, y, 4, dloss=dl, shard_stats=True)
+        torch.cuda.synchronize()
+        for k in ("loss", "lse", "shard_stats", "mean", "n_bad"):
+            assert torch.equal(f[k], o[k]), k
+        assert torch.equal(dX, o["dX"]) and torch.equal(dW, o["dW"])
+
+
+def test_autograd_with_saved_probabilities():
+    inp = synth.small_case(300, 128, 1000, 4, "bf16", seed=42, ignore_frac=0.1)
+    X, W, y = dev_inputs(inp)
+    X.requires_grad_(True)
+    W.requires_grad_(True)
+    (2.0 * vp.lmhead_ce(X, W, y, 4, save_probs=True)).backward()
+    b = ref.lmhead_ce_backward(inp.X, inp.W, inp.targets, inp.wl.V)
+    assert rel_fro(np64(X.grad), 2.0 * b["dX"]) <= 2e-2
+    assert rel_fro(np64(W.grad), 2.0 * b["dW"]) <= 2e-2

@@ -67,6 +67,10 @@ def _load():
     L.vp_lmhead_ce_bwd.argtypes = [P, P, P, P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, SZ, P]
     L.vp_lmhead_ce_fwd_bwd.restype = I32
     L.vp_lmhead_ce_fwd_bwd.argtypes = [P, P, P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, P, P, P, P, P, SZ, P]
+    L.vp_lmhead_ce_fwd_keep.restype = I32
+    L.vp_lmhead_ce_fwd_keep.argtypes = [P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, P, P, P, SZ, P]
+    L.vp_lmhead_ce_bwd_saved.restype = I32
+    L.vp_lmhead_ce_bwd_saved.argtypes = [P, P, P, P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, SZ, P]
     L.vp_read_device_status.restype = I32
     L.vp_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     L.vp_test_gemm_bf16.restype = I32
@@ -184,9 +188,12 @@ def embed_bwd(ids: torch.Tensor, dOut: torch.Tensor, V: int, T: int, dW: torch.T
 
 
 def lmhead_ce_fwd(X, W, targets, T, ignore_index=IGNORE_INDEX, shard_stats=False, workspace=None,
-                  out=None) -> dict:
+                  out=None, keep=False) -> dict:
     """Fused LM head + vocab-parallel CE forward.  Returns loss [N], lse [N],
-    mean [1], n_bad [1] (int32) and, if asked, shard_stats [T,3,N]."""
+    mean [1], n_bad [1] (int32) and, if asked, shard_stats [T,3,N].  With
+    keep=True the tile probabilities stay in out["saved"] (about 2*N*V bytes)
+    for lmhead_ce_bwd(..., saved=out["saved"]), which then skips the logit
+    recompute."""
     _need(X, "X")
     _need(W, "W", X.dtype, X.device)
     _need(targets, "targets", torch.int64, X.device)
@@ -200,23 +207,28 @@ def lmhead_ce_fwd(X, W, targets, T, ignore_index=IGNORE_INDEX, shard_stats=False
                "n_bad": torch.empty(1, dtype=torch.int32, device=dev)}
         if shard_stats:
             out["shard_stats"] = torch.empty((T, 3, N), dtype=torch.float32, device=dev)
-    ws_bytes = workspace_size(N, H, V, T, _dtype_code(X), 0)
+    ws_bytes = workspace_size(N, H, V, T, _dtype_code(X), 3 if keep else 0)
     if ws_bytes == 0:
         raise VpError("vp_lmhead_ce_workspace_size", 1)
     ws = _workspace(ws_bytes, dev, workspace)
-    code = _load().vp_lmhead_ce_fwd(
+    fn = _load().vp_lmhead_ce_fwd_keep if keep else _load().vp_lmhead_ce_fwd
+    code = fn(
         _ptr(X), _ptr(W), _ptr(targets), N, H, V, T, ignore_index, _dtype_code(X), _ptr(out["loss"]),
         _ptr(out["lse"]), _ptr(out.get("mean")), _ptr(out.get("shard_stats")), _ptr(out.get("n_bad")),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(dev))
-    _check("vp_lmhead_ce_fwd", code)
+    _check("vp_lmhead_ce_fwd_keep" if keep else "vp_lmhead_ce_fwd", code)
     out["workspace"] = ws
+    if keep:
+        out["saved"] = ws
     return out
 
 
 def lmhead_ce_bwd(X, W, targets, lse, T, ignore_index=IGNORE_INDEX, dloss=None, vocab_chunk=None,
-                  workspace=None, dX=None, dW=None, dmean=None):
+                  workspace=None, dX=None, dW=None, dmean=None, saved=None):
     """Backward of dmean * loss_mean (dmean: a 1-element device tensor, default
-    1) or of sum_n dloss[n] * loss[n]: (dX in X's dtype, dW in fp32)."""
+    1) or of sum_n dloss[n] * loss[n]: (dX in X's dtype, dW in fp32).  With
+    `saved` (from lmhead_ce_fwd(..., keep=True)) it uses the kept tile
+    probabilities instead of recomputing the logits; the buffer is consumed."""
     _need(X, "X")
     _need(W, "W", X.dtype, X.device)
     _need(targets, "targets", torch.int64, X.device)
@@ -234,6 +246,11 @@ def lmhead_ce_bwd(X, W, targets, lse, T, ignore_index=IGNORE_INDEX, dloss=None, 
         dW = torch.empty((V, H), dtype=torch.float32, device=dev)
     _need(dX, "dX", X.dtype, dev)
     _need(dW, "dW", torch.float32, dev)
+    if saved is not None:
+        _check("vp_lmhead_ce_bwd_saved", _load().vp_lmhead_ce_bwd_saved(
+            _ptr(X), _ptr(W), _ptr(targets), _ptr(lse), _ptr(dloss), _ptr(dmean), N, H, V, T, ignore_index,
+            _dtype_code(X), _ptr(dX), _ptr(dW), _ptr(saved), saved.numel() * saved.element_size(), _stream(dev)))
+        return dX, dW
     ws_bytes = workspace_size(N, H, V, T, _dtype_code(X), 1, vocab_chunk or 0)
     if ws_bytes == 0:
         raise VpError("vp_lmhead_ce_workspace_size", 1)
@@ -341,10 +358,11 @@ def stage_timing_read() -> dict:
 
 class _LMHeadCE(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, X, W, targets, T, ignore_index):
-        out = lmhead_ce_fwd(X, W, targets, T, ignore_index)
+    def forward(ctx, X, W, targets, T, ignore_index, save_probs):
+        out = lmhead_ce_fwd(X, W, targets, T, ignore_index, keep=save_probs)
         ctx.save_for_backward(X, W, targets, out["lse"])
         ctx.T, ctx.ignore_index = T, ignore_index
+        ctx.saved_probs = out.get("saved")
         return out["mean"][0]
 
     @staticmethod
@@ -354,11 +372,15 @@ class _LMHeadCE(torch.autograd.Function):
         dmean = grad.reshape(1)
         if dmean.dtype != torch.float32 or not dmean.is_contiguous():
             dmean = dmean.to(torch.float32).contiguous()
-        dX, dW = lmhead_ce_bwd(X, W, targets, lse, ctx.T, ctx.ignore_index, dmean=dmean)
-        return dX, dW.to(W.dtype), None, None, None
+        dX, dW = lmhead_ce_bwd(X, W, targets, lse, ctx.T, ctx.ignore_index, dmean=dmean, saved=ctx.saved_probs)
+        ctx.saved_probs = None
+        return dX, dW.to(W.dtype), None, None, None, None
 
 
-def lmhead_ce(X, W, targets, T, ignore_index=IGNORE_INDEX):
+def lmhead_ce(X, W, targets, T, ignore_index=IGNORE_INDEX, save_probs=False):
     """Mean cross-entropy of the tied LM head over valid tokens, differentiable
-    in X and W (autograd wrapper of lmhead_ce_fwd / lmhead_ce_bwd)."""
-    return _LMHeadCE.apply(X, W, targets, T, ignore_index)
+    in X and W (autograd wrapper of lmhead_ce_fwd / lmhead_ce_bwd).
+    save_probs=True keeps the tile probabilities (about 2*N*V bytes) from the
+    forward to the backward, which then skips the logit recompute (6NHV flops
+    instead of 8NHV); the default keeps only lse."""
+    return _LMHeadCE.apply(X, W, targets, T, ignore_index, bool(save_probs))

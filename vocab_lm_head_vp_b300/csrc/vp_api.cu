@@ -242,7 +242,8 @@ VP_EXPORT size_t vp_lmhead_ce_workspace_size(int64_t N, int64_t H, int64_t V, in
     }
     return fused_layout(N, V, T, nc).total;
   }
-  if (pass == 2) {   // fp32: the forward, then the recompute backward in the same bytes
+  if (pass == 3 && dtype == VP_BF16) return fused_layout(N, V, T, N).total;   // kept forward state, all N
+  if (pass == 2 || pass == 3) {   // fp32: the forward, then the recompute backward in the same bytes
     const size_t f = fwd_layout(N, V, T, dtype).total;
     const size_t b = vp_lmhead_ce_workspace_size(N, H, V, T, dtype, 1, vocab_chunk);
     return f > b ? f : b;
@@ -422,6 +423,75 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int
   }
   if (e == cudaSuccess && (loss_mean || n_bad))
     e = timed(kMean, s, [&] { return loss_mean_and_bad(loss, targets, N, V, ignore_index, loss_mean, n_bad, s); });
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+VP_EXPORT vp_status vp_lmhead_ce_fwd_keep(const void* X, const void* W, const int64_t* targets, int64_t N,
+                                          int64_t H, int64_t V, int T, int64_t ignore_index, vp_dtype dtype,
+                                          float* loss, float* lse, float* loss_mean, float* shard_stats,
+                                          int32_t* n_bad, void* saved, size_t saved_bytes, void* stream) {
+  if (!loss || !lse) return VP_ERR_INVALID_ARG;
+  vp_status st = check_args(X, W, targets, N, H, V, T, dtype, saved);
+  if (st != VP_OK) return st;
+  if (dtype == VP_F32)   // fp32: nothing is kept; the backward recomputes in the same bytes
+    return vp_lmhead_ce_fwd(X, W, targets, N, H, V, T, ignore_index, dtype, loss, lse, loss_mean, shard_stats, n_bad,
+                            saved, saved_bytes, stream);
+  const FusedLayout L = fused_layout(N, V, T, N);
+  if (saved_bytes < L.total) return VP_ERR_WORKSPACE;
+  if (!tensor_map_encoder()) return VP_ERR_CUDA;
+  cudaStream_t s = as_stream(stream);
+  uint8_t* ws = static_cast<uint8_t*>(saved);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  float2* partial = reinterpret_cast<float2*>(ws + L.off_partial);
+  float* zy = reinterpret_cast<float*>(ws + L.off_zy);
+  float* tmax = reinterpret_cast<float*>(ws + L.off_tmax);
+  void* P = ws + L.off_p;
+  const int64_t Vs = V / T;
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess)
+    e = timed(kLsePGemm, s, [&] {
+      return bf16_lse_stats_p(X, W, targets, N, H, V, Vs, partial, L.maxseg, zy, tmax, P, L.ldp, status, s);
+    });
+  if (e == cudaSuccess)
+    e = timed(kMerge, s, [&] {
+      return lse_merge(partial, zy, targets, N, V, Vs, T, kBf16TileV, L.maxseg, ignore_index, loss, lse, shard_stats,
+                       s);
+    }, kMergeKernels);
+  if (e == cudaSuccess && (loss_mean || n_bad))
+    e = timed(kMean, s, [&] { return loss_mean_and_bad(loss, targets, N, V, ignore_index, loss_mean, n_bad, s); });
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+VP_EXPORT vp_status vp_lmhead_ce_bwd_saved(const void* X, const void* W, const int64_t* targets, const float* lse,
+                                           const float* dloss, const float* dmean, int64_t N, int64_t H, int64_t V,
+                                           int T, int64_t ignore_index, vp_dtype dtype, void* dX, float* dW,
+                                           void* saved, size_t saved_bytes, void* stream) {
+  if (!lse || !dX || !dW) return VP_ERR_INVALID_ARG;
+  vp_status st = check_args(X, W, targets, N, H, V, T, dtype, saved);
+  if (st != VP_OK) return st;
+  if (!aligned16(dX) || !aligned16(dW)) return VP_ERR_UNSUPPORTED;
+  if (dtype == VP_F32)
+    return vp_lmhead_ce_bwd(X, W, targets, lse, dloss, dmean, N, H, V, T, ignore_index, dtype, dX, dW, saved,
+                            saved_bytes, stream);
+  const FusedLayout L = fused_layout(N, V, T, N);
+  if (saved_bytes < L.total) return VP_ERR_WORKSPACE;
+  if (!tensor_map_encoder()) return VP_ERR_CUDA;
+  cudaStream_t s = as_stream(stream);
+  uint8_t* ws = static_cast<uint8_t*>(saved);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  float* g = reinterpret_cast<float*>(ws + L.off_g);
+  float* tmax = reinterpret_cast<float*>(ws + L.off_tmax);
+  void* P = ws + L.off_p;
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess)
+    e = timed(kScale, s, [&] { return upstream_scale(targets, dloss, dmean, N, V, ignore_index, g, s); });
+  // the kept tile maxima become the factors c = g exp(tmax - lse); p becomes dZ in place
+  if (e == cudaSuccess) e = timed(kTileScale, s, [&] { return tile_scale(tmax, lse, g, N, V, s); });
+  if (e == cudaSuccess) e = timed(kDzFromP, s, [&] { return dz_from_p(P, L.ldp, tmax, g, targets, N, V, s); });
+  if (e == cudaSuccess)
+    e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(P, L.ldp, X, N, H, 0, V, dW, false, status, s); });
+  if (e == cudaSuccess)
+    e = timed(kDxGemm, s, [&] { return bf16_dx_chunk(P, L.ldp, W, N, H, 0, V, dX, nullptr, 3, status, s); });
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
 }
 
