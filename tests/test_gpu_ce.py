@@ -150,6 +150,7 @@ CASES = [  # N, H, V, T, dtype: several tiles, ragged tails, shard edges inside 
     (257, 136, 770, 7, "bf16"),     # V/T = 110 < 256: one tile spans up to 4 shards
     (64, 512, 6400, 16, "bf16"),
     (50, 8, 48, 3, "bf16"),         # H = 8 (one 16-byte row), V < 64: a tile spans all 3 shards
+    (40, 64, 512, 512, "bf16"),     # T = V: every shard one id, 256 shard records per tile
     (77, 40, 99, 3, "f32"),
     (200, 96, 640, 10, "f32"),
 ]
