@@ -283,11 +283,12 @@ def lmhead_ce_backward(X, W, y, V: int, ignore_index: int = IGNORE_INDEX,
 
 
 def lmhead_ce_rows(X, W, y, rows, n_valid: int, ignore_index: int = IGNORE_INDEX,
-                   w_chunk: int = 16384) -> dict:
+                   w_chunk: int = 16384, with_dx: bool = True) -> dict:
     """Loss, lse and dX for selected token rows only, one row's logits at a time
     over vocab chunks (for workloads too large for the dense form).  ``n_valid``
     is the number of valid targets in the whole batch (it sets g = 1/n_valid).
-    W may be float32 holding bf16 values; chunks are widened to float64."""
+    W may be float32 holding bf16 values; chunks are widened to float64.
+    with_dx=False skips dX (the rows' loss and lse only)."""
     W = np.asarray(W)
     V, H = W.shape
     rows = np.asarray(rows, dtype=np.int64)
@@ -297,6 +298,8 @@ def lmhead_ce_rows(X, W, y, rows, n_valid: int, ignore_index: int = IGNORE_INDEX
     for a in range(0, V, w_chunk):
         Zr[:, a:a + w_chunk] = Xr @ np.asarray(W[a:a + w_chunk], dtype=np.float64).T
     ce = cross_entropy(Zr, yr, ignore_index)
+    if not with_dx:
+        return {"loss": ce["loss"], "lse": ce["lse"], "z_y": ce["z_y"]}
     valid, _ = target_masks(yr, V, ignore_index)
     g = valid / max(1, n_valid)
     dZ = grad_logits(Zr, yr, ce["lse"], g)
@@ -304,3 +307,22 @@ def lmhead_ce_rows(X, W, y, rows, n_valid: int, ignore_index: int = IGNORE_INDEX
     for a in range(0, V, w_chunk):
         dX += dZ[:, a:a + w_chunk] @ np.asarray(W[a:a + w_chunk], dtype=np.float64)
     return {"loss": ce["loss"], "lse": ce["lse"], "dX": dX, "z_y": ce["z_y"]}
+
+
+def lmhead_ce_dw_rows(X, W, y, lse, vocab_rows, n_valid: int, ignore_index: int = IGNORE_INDEX) -> np.ndarray:
+    """dW rows for selected vocab ids only ([VP-book] sec. 5.3.2): the logit
+    gradient's columns dZ[:, v] = g (exp(Z[:, v] - lse) - 1[y = v]) for those
+    ids, then dW[v, :] = sum_n dZ[n, v] X[n, :].  ``lse`` is every token's
+    log-sum-exp, from this oracle (lmhead_ce_rows over all rows); ``n_valid``
+    sets g = 1/n_valid on valid targets, 0 elsewhere."""
+    W = np.asarray(W)
+    V = W.shape[0]
+    vr = np.asarray(vocab_rows, dtype=np.int64)
+    X64 = np.asarray(X, dtype=np.float64)
+    y = np.asarray(y, dtype=np.int64)
+    Zv = X64 @ np.asarray(W[vr], dtype=np.float64).T                  # [N, len(vr)]
+    valid, _ = target_masks(y, V, ignore_index)
+    g = valid / max(1, n_valid)
+    onehot = (y[:, None] == vr[None, :]) & valid[:, None]
+    dZv = g[:, None] * (np.exp(Zv - np.asarray(lse, dtype=np.float64)[:, None]) - onehot)
+    return dZv.T @ X64

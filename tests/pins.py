@@ -256,6 +256,25 @@ def pin_rows_variant(o):
     np.testing.assert_allclose(r["dX"], b["dX"][rows], rtol=1e-12, atol=1e-15)
 
 
+def pin_dw_rows_variant(o):
+    """dW rows for selected vocab ids (used at full size) equal torch's autograd
+    of the mean cross-entropy (float64, CPU), ignored and repeated targets in."""
+    rng = np.random.default_rng(9)
+    n, H, V = 20, 6, 40
+    X = rng.standard_normal((n, H))
+    W = (rng.standard_normal((V, H)) * 0.5).astype(np.float32)
+    y = rng.integers(0, V, n)
+    y[:4] = [IGN, 7, 7, 7]
+    Wt = torch.from_numpy(W.astype(np.float64)).requires_grad_(True)
+    Z = torch.from_numpy(X) @ Wt.T
+    torch.nn.functional.cross_entropy(Z, torch.from_numpy(y), ignore_index=IGN).backward()
+    nv = int((y != IGN).sum())
+    lse = o.lmhead_ce_rows(X, W, y, np.arange(n), nv, IGN, with_dx=False)["lse"]
+    rows = np.array([0, 7, 13, V - 1])
+    np.testing.assert_allclose(o.lmhead_ce_dw_rows(X, W, y, lse, rows, nv, IGN), Wt.grad.numpy()[rows],
+                               rtol=1e-10, atol=1e-14)
+
+
 def pin_embed_sp(o):
     """SP on (sec. 5.2.1, reduce-scatter): with the V=8, T=2, ids [1,6] table,
     rank 0 keeps token 1's row E1 and rank 1 token 6's row E6; in general the
@@ -362,4 +381,4 @@ ALL_PINS = [pin_embed_worked_table, pin_embed_figure1, pin_embed_brute_force,
             pin_embed_bwd_finite_differences,
             pin_ce_library, pin_ce_closed_form, pin_ce_ignore_and_bad,
             pin_shard_invariance, pin_page_t4_simulation,
-            pin_grad_library, pin_grad_finite_differences, pin_rows_variant]
+            pin_grad_library, pin_grad_finite_differences, pin_rows_variant, pin_dw_rows_variant]

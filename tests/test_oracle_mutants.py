@@ -103,6 +103,16 @@ def _embed_sp_wrong_slice(ids, W, V, T, rank):
     return ref.embed(ids, W, V, T)[(T - 1 - rank) * rows:(T - rank) * rows]   # ranks reversed
 
 
+def _dw_rows_no_onehot(X, W, y, lse, vocab_rows, n_valid, ignore_index=-100):
+    W = np.asarray(W)
+    vr = np.asarray(vocab_rows, dtype=np.int64)
+    X64 = np.asarray(X, dtype=np.float64)
+    Zv = X64 @ np.asarray(W[vr], dtype=np.float64).T
+    valid = (np.asarray(y) >= 0) & (np.asarray(y) < W.shape[0]) & (np.asarray(y) != ignore_index)
+    g = valid / max(1, n_valid)
+    return (g[:, None] * np.exp(Zv - np.asarray(lse)[:, None])).T @ X64      # the -1[y = v] term dropped
+
+
 _ORIG = {k: getattr(ref, k) for k in ("cross_entropy", "merge_local_stats")}
 
 MUTANTS = {
@@ -117,6 +127,7 @@ MUTANTS = {
     "embed_bwd_assign_not_add": ("embed_shard_grad", _embed_bwd_assign),
     "embed_bwd_global_row": ("embed_shard_grad", _embed_bwd_global_row),
     "embed_sp_wrong_slice": ("embed_sp", _embed_sp_wrong_slice),
+    "dw_rows_no_onehot": ("lmhead_ce_dw_rows", _dw_rows_no_onehot),
 }
 
 
