@@ -95,3 +95,38 @@ def test_fused_full_size_repeatable():
     torch.cuda.synchronize()
     for k in ("loss", "lse", "mean", "dX", "dW"):
         assert torch.equal(a[k], b[k]), k
+
+
+def test_v128k_fused_every_token_and_sampled_dw_rows():
+    """The bench's workload through the fused call it times: every token's loss
+    and lse against the oracle's (all 16384 rows in float64, row batches), and
+    dW rows of sampled vocab ids -- the most frequent Zipf targets, random ids,
+    never-targeted ones -- against the oracle's own columns of the logit
+    gradient."""
+    inp = synth.make_inputs("v128k")
+    wl = inp.wl
+    X, W, y = dev_inputs(inp)
+    o = vp.lmhead_ce_fwd_bwd(X, W, y, wl.T)
+    torch.cuda.synchronize()
+    assert vp.read_device_status(o["workspace"]) == 0
+    valid = (inp.targets >= 0) & (inp.targets < wl.V)
+    n_valid = int(valid.sum())
+    parts = [ref.lmhead_ce_rows(inp.X, inp.W, inp.targets, np.arange(a, min(a + 2048, wl.N)), n_valid,
+                                with_dx=False) for a in range(0, wl.N, 2048)]
+    lse = np.concatenate([p["lse"] for p in parts])
+    loss = np.concatenate([p["loss"] for p in parts])
+    assert_loss_close(np64(o["lse"]), lse, "bf16", what="lse")
+    assert_loss_close(np64(o["loss"]), loss, "bf16", scale=lse, what="loss")
+    rng = np.random.default_rng(123)
+    counts = np.bincount(inp.targets[valid], minlength=wl.V)
+    never = np.flatnonzero(counts == 0)
+    rows = np.unique(np.concatenate([np.arange(8), rng.choice(wl.V, 32, replace=False),
+                                     rng.choice(never, 8, replace=False)]))
+    want = ref.lmhead_ce_dw_rows(inp.X, inp.W, inp.targets, lse, rows, n_valid)
+    got = np64(o["dW"][torch.from_numpy(rows).cuda()])
+    e = rel_fro(got, want)
+    assert e <= 2e-2, f"dW sampled rows rel Frobenius {e:.3e}"
+    # the frequent ids' rows carry the one-hot term: each is checked on its own too
+    for k in range(8):
+        ek = rel_fro(got[k], want[k])
+        assert ek <= 2e-2, (int(rows[k]), ek)
