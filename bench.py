@@ -375,8 +375,18 @@ def run_ours(args):
 
     import synth
     import vocab_lm_head_vp_b300 as vp
+    from vocab_lm_head_vp_b300 import build
 
     rank, world, local = rank_env()
+    if rank == 0:
+        build.build()   # libvp.so is a build product: make it if missing or stale (no-op otherwise)
+    if world > 1:
+        # the other ranks wait (bounded) until rank 0's build is in place
+        t_wait = time.time()
+        while not build.up_to_date():
+            if time.time() - t_wait > 900:
+                raise RuntimeError("libvp.so was not built by rank 0 within 900 s")
+            time.sleep(1.0)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     vp.set_gemm_variant(args.gemm_variant == "pair")

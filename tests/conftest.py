@@ -8,3 +8,7 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (B300, sm_103a) and the built libvp.so")
+    # libvp.so is a build product, not checked in: (re)build it when missing or older
+    # than its sources (nvcc cross-compiles for sm_103a; a no-op when up to date)
+    from vocab_lm_head_vp_b300 import build
+    build.build()
