@@ -47,16 +47,20 @@ vp_status vp_test_set_gemm_variant(int pair);
  *
  * vp_stage_timing_enable(max_launches): max_launches > 0 creates the events
  *   (2 per launch) and starts recording from empty; 0 stops and frees them.
- *   Launches beyond max_launches are not recorded (see the count returned).
+ *   Timed regions beyond max_launches are not recorded; they are counted
+ *   (vp_stage_timing_dropped), so a harness can reject partial totals.
  * vp_stage_timing_read(ms, counts, n): waits for the recorded events and
  *   writes, for stage s < n, the summed milliseconds and the number of
  *   kernels launched in the stage's timed regions (lse_merge is two kernels
  *   per region, embed_bwd several); returns the number of stages, or -1 on a
  *   CUDA error.
+ * vp_stage_timing_dropped(): timed regions not recorded since the last
+ *   vp_stage_timing_enable because all max_launches slots were in use.
  * vp_stage_name(s): the stage's name (static storage), NULL past the end.
  */
 vp_status vp_stage_timing_enable(int max_launches);
 int vp_stage_timing_read(float* ms, int32_t* counts, int n);
+int vp_stage_timing_dropped(void);
 const char* vp_stage_name(int stage);
 
 #ifdef __cplusplus

@@ -174,3 +174,14 @@ def test_keep_saved_rejects_bad_arguments(lib):
     assert bs(X, W, y, lse, None, None, 300, 64, 1000, 4, -100, vp.VP_BF16, P(0x70008), dW, sv, 1 << 30,
               None) == 2
     assert bs(X, W, y, lse, None, None, 300, 64, 1000, 4, -100, vp.VP_BF16, dX, dW, sv, 4096, None) == 3
+
+
+def test_stage_timing_off_records_nothing(lib):
+    # Disabled (the default), no region is recorded or counted as dropped;
+    # disabling again resets the dropped count.
+    assert lib.vp_stage_timing_enable(0) == 0
+    assert lib.vp_stage_timing_dropped() == 0
+    ms = (ctypes.c_float * 16)()
+    k = lib.vp_stage_timing_read(ms, None, 16)
+    assert k > 0 and lib.vp_stage_name(k - 1) and not lib.vp_stage_name(k)
+    assert all(x == 0.0 for x in ms)

@@ -81,6 +81,8 @@ def _load():
     L.vp_stage_timing_enable.argtypes = [I32]
     L.vp_stage_timing_read.restype = I32
     L.vp_stage_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32), I32]
+    L.vp_stage_timing_dropped.restype = I32
+    L.vp_stage_timing_dropped.argtypes = []
     L.vp_stage_name.restype = ctypes.c_char_p
     L.vp_stage_name.argtypes = [I32]
     _lib = L
@@ -345,8 +347,15 @@ def stage_timing_enable(max_launches: int) -> None:
 
 
 def stage_timing_read() -> dict:
-    """{stage name: (milliseconds, launches)} accumulated since enabling."""
+    """{stage name: (milliseconds, launches)} accumulated since enabling.
+
+    Raises if some timed regions found every slot in use: the totals would be
+    partial.
+    """
     L = _load()
+    dropped = L.vp_stage_timing_dropped()
+    if dropped:
+        raise RuntimeError(f"stage timing: {dropped} timed regions were not recorded (enable more slots)")
     n = 16
     ms = (ctypes.c_float * n)()
     cnt = (ctypes.c_int32 * n)()

@@ -146,6 +146,7 @@ const char* const kStageNames[kNumStages] = {"embed_gather",   "lse_stats_gemm",
                                              "lse_p_gemm",     "dz_from_p",         "embed_bwd", "tile_scale"};
 struct StageTimer {
   int cap = 0, used = 0;
+  int dropped = 0;            // timed regions past `cap`, not recorded
   cudaEvent_t* ev = nullptr;  // 2 per launch
   int* stage = nullptr;
   int* kernels = nullptr;   // kernels launched inside each timed region
@@ -154,6 +155,7 @@ struct StageTimer {
 template <class F>
 cudaError_t timed(Stage st, cudaStream_t s, F&& launch, int kernels = 1) {
   int slot = -1;
+  if (g_timer.cap > 0 && g_timer.used >= g_timer.cap) ++g_timer.dropped;
   if (g_timer.cap > 0 && g_timer.used < g_timer.cap) {
     slot = g_timer.used++;
     g_timer.stage[slot] = st;
@@ -528,6 +530,7 @@ VP_EXPORT vp_status vp_stage_timing_enable(int max_launches) {
   }
   t.cap = 0;
   t.used = 0;
+  t.dropped = 0;
   if (max_launches <= 0) return VP_OK;
   t.ev = new cudaEvent_t[2 * max_launches];
   t.stage = new int[max_launches];
@@ -566,6 +569,8 @@ VP_EXPORT int vp_stage_timing_read(float* ms, int32_t* counts, int n) {
   }
   return kNumStages;
 }
+
+VP_EXPORT int vp_stage_timing_dropped(void) { return g_timer.dropped; }
 
 VP_EXPORT const char* vp_stage_name(int stage) {
   return (stage >= 0 && stage < kNumStages) ? kStageNames[stage] : nullptr;
