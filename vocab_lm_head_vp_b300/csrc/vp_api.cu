@@ -138,12 +138,12 @@ constexpr int kMergeKernels = 2;   // lse_merge: the per-shard pass, then the pe
 
 // ---------------- optional per-launch event timing (vp_stage_timing_enable)
 enum Stage {
-  kEmbed, kLseGemm, kMerge, kMean, kScale, kDzGemm, kDwGemm, kDxGemm, kLsePGemm, kDzFromP, kEmbedBwd, kTileScale,
+  kEmbed, kLseGemm, kMerge, kMean, kScale, kDzGemm, kDwGemm, kDxGemm, kLsePGemm, kDzFromP, kEmbedBwd,
   kNumStages
 };
 const char* const kStageNames[kNumStages] = {"embed_gather",   "lse_stats_gemm",    "lse_merge", "loss_mean",
                                              "upstream_scale", "dz_recompute_gemm", "dw_gemm",   "dx_gemm",
-                                             "lse_p_gemm",     "dz_from_p",         "embed_bwd", "tile_scale"};
+                                             "lse_p_gemm",     "dz_from_p",         "embed_bwd"};
 struct StageTimer {
   int cap = 0, used = 0;
   int dropped = 0;            // timed regions past `cap`, not recorded
@@ -413,11 +413,10 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int
         return lse_merge_ld(partial, zy, yc, nc, V, Vs, T, kBf16TileV, L.maxseg, ignore_index, loss + n0, lse + n0,
                             shard_stats ? shard_stats + n0 : nullptr, N, s);
       }, kMergeKernels);
-    // tmax -> c = g exp(tmax - lse): the per-row, per-tile factor turning p into the softmax gradient
-    if (e == cudaSuccess) e = timed(kTileScale, s, [&] { return tile_scale(tmax, lse + n0, g + n0, nc, V, s); });
     void* dXc = static_cast<uint8_t*>(dX) + n0 * H * 2;
     // p -> dZ in place, then dW = sum over token chunks of dZ_c^T X_c; dX rows of this chunk are complete
-    if (e == cudaSuccess) e = timed(kDzFromP, s, [&] { return dz_from_p(P, L.ldp, tmax, g + n0, yc, nc, V, s); });
+    if (e == cudaSuccess)
+      e = timed(kDzFromP, s, [&] { return dz_from_p(P, L.ldp, tmax, lse + n0, g + n0, yc, nc, V, s); });
     if (e == cudaSuccess)
       e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(P, L.ldp, Xc, nc, H, 0, V, dW, n0 > 0, status, s); });
     if (e == cudaSuccess)
@@ -487,9 +486,8 @@ VP_EXPORT vp_status vp_lmhead_ce_bwd_saved(const void* X, const void* W, const i
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess)
     e = timed(kScale, s, [&] { return upstream_scale(targets, dloss, dmean, N, V, ignore_index, g, s); });
-  // the kept tile maxima become the factors c = g exp(tmax - lse); p becomes dZ in place
-  if (e == cudaSuccess) e = timed(kTileScale, s, [&] { return tile_scale(tmax, lse, g, N, V, s); });
-  if (e == cudaSuccess) e = timed(kDzFromP, s, [&] { return dz_from_p(P, L.ldp, tmax, g, targets, N, V, s); });
+  // p becomes dZ in place, scaled per row and tile by c = g exp(tmax - lse) from the kept tile maxima
+  if (e == cudaSuccess) e = timed(kDzFromP, s, [&] { return dz_from_p(P, L.ldp, tmax, lse, g, targets, N, V, s); });
   if (e == cudaSuccess)
     e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(P, L.ldp, X, N, H, 0, V, dW, false, status, s); });
   if (e == cudaSuccess)

@@ -57,13 +57,10 @@ cudaError_t lse_merge(float2* partial, const float* zy, const int64_t* targets, 
 cudaError_t lse_merge_ld(float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
                          int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
                          float* shard_stats, int64_t ss_ld, cudaStream_t stream);
-// In place: tmax [ceil(V/256)][N] -> c = g exp(tmax - lse), the per-row, per-tile
-// factor of the saved-probability backward.
-cudaError_t tile_scale(float* tmax_c, const float* lse, const float* g, int64_t N, int64_t V, cudaStream_t stream);
-// In place: P [N][ldp] fp16 probabilities relative to the tile row maxima ->
-// dZ bf16 = c p - g 1[j = y].
-cudaError_t dz_from_p(void* P, int64_t ldp, const float* cscale, const float* g, const int64_t* targets, int64_t N,
-                      int64_t V, cudaStream_t stream);
+// In place: P [N][ldp] fp16 probabilities relative to the tile row maxima
+// tmax [ceil(V/256)][N] -> dZ bf16 = c p - g 1[j = y], c = g exp(tmax - lse).
+cudaError_t dz_from_p(void* P, int64_t ldp, const float* tmax, const float* lse, const float* g,
+                      const int64_t* targets, int64_t N, int64_t V, cudaStream_t stream);
 
 cudaError_t loss_mean_and_bad(const float* loss, const int64_t* targets, int64_t N, int64_t V, int64_t ignore_index,
                               float* loss_mean, int32_t* n_bad, cudaStream_t stream);
