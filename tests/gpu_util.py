@@ -50,3 +50,38 @@ def grad_tol(dtype):
 
 def np64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def assert_grads_elementwise(inp, dX, dW, b):
+    """dX and dW element by element against a bound derived from the arithmetic.
+
+    b is the oracle's backward (dZ, g, dX, dW).  With M[n, j] = |g_n| (p_nj +
+    1[j = y_n]) >= |dZ[n, j]|, the size of the terms that form the logit
+    gradient ("Vocab Parallelism" sec. 5.3.2),
+
+        |dX_gpu - dX| <= u (M |W|),      |dW_gpu - dW| <= u (M^T |X|)
+
+    elementwise.  For bf16, u = 2^-7 covers the bf16 rounding of dZ (2^-9), the
+    bf16 rounding of dX itself (2^-9), the fp16 rounding of saved probabilities
+    (2^-11) and the fp32 error of the logits and of the sums; for fp32 inputs
+    u = 1e-4.  A mistake confined to a few small entries (a ragged tail tile, a
+    rarely targeted vocab row) fails this although the tensor's relative
+    Frobenius error stays small.
+    """
+    dZ, g = b["dZ"], b["g"]
+    M = np.abs(dZ)
+    rows = np.nonzero(g != 0)[0]
+    y = np.asarray(inp.targets)[rows]
+    # at the target |dZ| = |g| (1 - p_y), while the terms are |g| p_y and |g|
+    M[rows, y] += 2.0 * np.abs(g[rows]) * (dZ[rows, y] / g[rows] + 1.0)
+    X = np.abs(np.asarray(inp.X, dtype=np.float64))
+    W = np.abs(np.asarray(inp.W, dtype=np.float64))
+    u = 2.0 ** -7 if inp.wl.dtype == "bf16" else 1e-4
+    for name, got, want, bound in (("dX", np64(dX), b["dX"], u * (M @ W)),
+                                   ("dW", np64(dW), b["dW"], u * (M.T @ X))):
+        err = np.abs(got - want)
+        bad = err > bound
+        if bad.any():
+            i = np.unravel_index(int(np.argmax(err - bound)), err.shape)
+            raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} entries outside the elementwise bound; "
+                                 f"worst at {i}: err {err[i]:.3e}, bound {bound[i]:.3e}, ref {want[i]:.3e}")

@@ -9,7 +9,7 @@ import oracle.ref as ref
 import synth
 import vocab_lm_head_vp_b300 as vp
 from golden_io import read
-from gpu_util import assert_loss_close, dev_inputs, grad_tol, np64, rel_fro
+from gpu_util import assert_grads_elementwise, assert_loss_close, dev_inputs, grad_tol, np64, rel_fro
 
 pytestmark = pytest.mark.gpu
 IGN = -100
@@ -121,6 +121,7 @@ def _check(inp, T, f, dX, dW, ignore_index=IGN, dloss=None, check_stats=True):
     ex, ew = rel_fro(np64(dX), b["dX"]), rel_fro(np64(dW), b["dW"])
     tol = grad_tol(wl.dtype)
     assert ex <= tol and ew <= tol, f"rel Frobenius dX {ex:.2e} dW {ew:.2e} (tol {tol})"
+    assert_grads_elementwise(inp, dX, dW, b)
     return ex, ew
 
 

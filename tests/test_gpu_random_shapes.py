@@ -1,0 +1,42 @@
+"""Seeded random shapes through both LM-head paths (the split calls and the
+one-call fused form) against the float64 oracle: loss, lse, shard statistics,
+and dX / dW both per tensor and element by element (the bound of
+gpu_util.assert_grads_elementwise, applied inside _check)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from test_gpu_ce import _check, _run
+from test_gpu_fused import _fused
+
+pytestmark = pytest.mark.gpu
+IGN = -100
+NCASES = 24
+
+
+def _draw(k):
+    rng = np.random.default_rng(7000 + k)
+    T = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 16]))
+    V = T * int(rng.integers(1, 401))
+    N = int(rng.integers(1, 601))
+    H = 8 * int(rng.integers(1, 49))
+    dtype = "f32" if k % 4 == 0 else "bf16"
+    ignore_frac = float(rng.choice([0.0, 0.1, 0.5]))
+    targets = "zipf" if rng.random() < 0.5 else "uniform"
+    # fp32-representable, so the oracle and the kernels see the same upstream gradient
+    dloss = rng.standard_normal(N).astype(np.float32).astype(np.float64) if k % 3 == 0 else None
+    vocab_chunk = int(rng.choice([256, 512, 1000])) if rng.random() < 0.5 else None
+    token_chunk = int(rng.choice([128, 256])) if rng.random() < 0.5 else None
+    inp = synth.small_case(N, H, V, T, dtype, seed=8000 + k, targets=targets, ignore_frac=ignore_frac)
+    return inp, T, dloss, vocab_chunk, token_chunk
+
+
+@pytest.mark.parametrize("k", range(NCASES))
+def test_random_shape_split_and_fused(k):
+    inp, T, dloss, vocab_chunk, token_chunk = _draw(k)
+    f, dX, dW = _run(inp, T, IGN, dloss=dloss, vocab_chunk=vocab_chunk)
+    _check(inp, T, f, dX, dW, IGN, dloss)
+    o, dX2, dW2 = _fused(inp, T, IGN, dloss=dloss, token_chunk=token_chunk)
+    _check(inp, T, o, dX2, dW2, IGN, dloss)
+    torch.cuda.synchronize()
