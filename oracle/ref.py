@@ -306,15 +306,17 @@ def lmhead_ce_rows(X, W, y, rows, n_valid: int, ignore_index: int = IGNORE_INDEX
     dX = np.zeros((len(rows), H))
     for a in range(0, V, w_chunk):
         dX += dZ[:, a:a + w_chunk] @ np.asarray(W[a:a + w_chunk], dtype=np.float64)
-    return {"loss": ce["loss"], "lse": ce["lse"], "dX": dX, "z_y": ce["z_y"]}
+    return {"loss": ce["loss"], "lse": ce["lse"], "dX": dX, "z_y": ce["z_y"], "dZ": dZ, "g": g}
 
 
-def lmhead_ce_dw_rows(X, W, y, lse, vocab_rows, n_valid: int, ignore_index: int = IGNORE_INDEX) -> np.ndarray:
+def lmhead_ce_dw_rows(X, W, y, lse, vocab_rows, n_valid: int, ignore_index: int = IGNORE_INDEX,
+                      return_dz: bool = False):
     """dW rows for selected vocab ids only ([VP-book] sec. 5.3.2): the logit
     gradient's columns dZ[:, v] = g (exp(Z[:, v] - lse) - 1[y = v]) for those
     ids, then dW[v, :] = sum_n dZ[n, v] X[n, :].  ``lse`` is every token's
     log-sum-exp, from this oracle (lmhead_ce_rows over all rows); ``n_valid``
-    sets g = 1/n_valid on valid targets, 0 elsewhere."""
+    sets g = 1/n_valid on valid targets, 0 elsewhere.  return_dz=True returns
+    (dW rows, those dZ columns [N, len(vocab_rows)], g) instead of dW rows."""
     W = np.asarray(W)
     V = W.shape[0]
     vr = np.asarray(vocab_rows, dtype=np.int64)
@@ -325,4 +327,5 @@ def lmhead_ce_dw_rows(X, W, y, lse, vocab_rows, n_valid: int, ignore_index: int 
     g = valid / max(1, n_valid)
     onehot = (y[:, None] == vr[None, :]) & valid[:, None]
     dZv = g[:, None] * (np.exp(Zv - np.asarray(lse, dtype=np.float64)[:, None]) - onehot)
-    return dZv.T @ X64
+    dW_rows = dZv.T @ X64
+    return (dW_rows, dZv, g) if return_dz else dW_rows

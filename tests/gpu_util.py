@@ -52,36 +52,59 @@ def np64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def assert_grads_elementwise(inp, dX, dW, b):
-    """dX and dW element by element against a bound derived from the arithmetic.
+def term_magnitudes(dZ, g, y, cols=None):
+    """M[n, c] = |g_n| (p_nc + 1[c = y_n]) >= |dZ[n, c]|: the size of the terms
+    that form each logit-gradient entry (softmax minus one-hot, "Vocab
+    Parallelism" sec. 5.3.2), from the oracle's dZ block.  Rows are tokens with
+    targets y; cols are the block's vocab ids (all of them when None)."""
+    M = np.abs(dZ)
+    g = np.asarray(g, dtype=np.float64)
+    y = np.asarray(y)
+    cols = np.arange(dZ.shape[1]) if cols is None else np.asarray(cols)
+    pos = {int(c): k for k, c in enumerate(cols)}
+    for n in np.nonzero(g != 0)[0]:
+        k = pos.get(int(y[n]))
+        if k is not None:
+            # at the target |dZ| = |g| (1 - p_y), while the terms are |g| p_y and |g|
+            M[n, k] += 2.0 * abs(g[n]) * (dZ[n, k] / g[n] + 1.0)
+    return M
 
-    b is the oracle's backward (dZ, g, dX, dW).  With M[n, j] = |g_n| (p_nj +
-    1[j = y_n]) >= |dZ[n, j]|, the size of the terms that form the logit
-    gradient ("Vocab Parallelism" sec. 5.3.2),
+
+def elementwise_u(dtype):
+    """The bound's factor: for bf16, 2^-7 covers the bf16 rounding of dZ
+    (2^-9), the bf16 rounding of dX itself (2^-9), the fp16 rounding of saved
+    probabilities (2^-11) and the fp32 error of the logits and of the sums;
+    1e-4 for fp32 inputs."""
+    return 2.0 ** -7 if dtype == "bf16" else 1e-4
+
+
+def abs_matmul(A, B, chunk=16384):
+    """|A| @ |B| in float64, B taken in row chunks (B may be a large float32 array)."""
+    out = np.zeros((A.shape[0], B.shape[1]))
+    for a in range(0, B.shape[0], chunk):
+        out += np.abs(A[:, a:a + chunk]) @ np.abs(np.asarray(B[a:a + chunk], dtype=np.float64))
+    return out
+
+
+def assert_within(name, got, want, bound):
+    err = np.abs(np.asarray(got, dtype=np.float64) - want)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(int(np.argmax(err - bound)), err.shape)
+        raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} entries outside the elementwise bound; "
+                             f"worst at {i}: err {err[i]:.3e}, bound {bound[i]:.3e}, ref {want[i]:.3e}")
+
+
+def assert_grads_elementwise(inp, dX, dW, b):
+    """dX and dW element by element against a bound derived from the arithmetic:
 
         |dX_gpu - dX| <= u (M |W|),      |dW_gpu - dW| <= u (M^T |X|)
 
-    elementwise.  For bf16, u = 2^-7 covers the bf16 rounding of dZ (2^-9), the
-    bf16 rounding of dX itself (2^-9), the fp16 rounding of saved probabilities
-    (2^-11) and the fp32 error of the logits and of the sums; for fp32 inputs
-    u = 1e-4.  A mistake confined to a few small entries (a ragged tail tile, a
-    rarely targeted vocab row) fails this although the tensor's relative
-    Frobenius error stays small.
-    """
-    dZ, g = b["dZ"], b["g"]
-    M = np.abs(dZ)
-    rows = np.nonzero(g != 0)[0]
-    y = np.asarray(inp.targets)[rows]
-    # at the target |dZ| = |g| (1 - p_y), while the terms are |g| p_y and |g|
-    M[rows, y] += 2.0 * np.abs(g[rows]) * (dZ[rows, y] / g[rows] + 1.0)
-    X = np.abs(np.asarray(inp.X, dtype=np.float64))
-    W = np.abs(np.asarray(inp.W, dtype=np.float64))
-    u = 2.0 ** -7 if inp.wl.dtype == "bf16" else 1e-4
-    for name, got, want, bound in (("dX", np64(dX), b["dX"], u * (M @ W)),
-                                   ("dW", np64(dW), b["dW"], u * (M.T @ X))):
-        err = np.abs(got - want)
-        bad = err > bound
-        if bad.any():
-            i = np.unravel_index(int(np.argmax(err - bound)), err.shape)
-            raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} entries outside the elementwise bound; "
-                                 f"worst at {i}: err {err[i]:.3e}, bound {bound[i]:.3e}, ref {want[i]:.3e}")
+    with M from term_magnitudes and u from elementwise_u.  b is the oracle's
+    backward (dZ, g, dX, dW).  A mistake confined to a few small entries (a
+    ragged tail tile, a rarely targeted vocab row) fails this although the
+    tensor's relative Frobenius error stays small."""
+    M = term_magnitudes(b["dZ"], b["g"], inp.targets)
+    u = elementwise_u(inp.wl.dtype)
+    assert_within("dX", np64(dX), b["dX"], u * abs_matmul(M, inp.W))
+    assert_within("dW", np64(dW), b["dW"], u * abs_matmul(M.T, inp.X))

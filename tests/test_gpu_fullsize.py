@@ -1,7 +1,9 @@
 """Parity at the full workload sizes, in the launch configuration the bench
 times (one vocab chunk): the oracle recomputes sampled token rows one at a
-time (loss, lse, dX rows); dW is checked through identities that hold at any
-size, and in full at the V32k shape with fewer tokens."""
+time (loss, lse, dX rows) and sampled vocab rows of dW; dW is also checked
+through identities that hold at any size, and in full at the V32k shape with
+fewer tokens.  Gradient entries are compared one by one against the bound of
+gpu_util.assert_grads_elementwise, besides the per-tensor tolerance."""
 import gc
 
 import numpy as np
@@ -11,7 +13,8 @@ import torch
 import oracle.ref as ref
 import synth
 import vocab_lm_head_vp_b300 as vp
-from gpu_util import assert_loss_close, dev_inputs, np64, rel_fro
+from gpu_util import (abs_matmul, assert_grads_elementwise, assert_loss_close, assert_within, dev_inputs,
+                      elementwise_u, np64, rel_fro, term_magnitudes)
 
 pytestmark = pytest.mark.gpu
 
@@ -50,6 +53,8 @@ def test_fullsize_sampled_rows(name, path):
     assert_loss_close(np64(f["loss"][rt]), o["loss"], "bf16", scale=o["lse"], what="loss")
     e = rel_fro(np64(dX[rt]), o["dX"])
     assert e <= 2e-2, f"dX sampled rows rel Frobenius {e:.3e}"
+    M = term_magnitudes(o["dZ"], o["g"], inp.targets[rows])
+    assert_within("dX rows", np64(dX[rt]), o["dX"], elementwise_u("bf16") * abs_matmul(M, inp.W))
     # mean over valid tokens is the mean of the per-token losses
     loss = np64(f["loss"])
     assert abs(float(f["mean"].item()) - loss.sum() / n_valid) <= 1e-5 * abs(loss.sum() / n_valid)
@@ -82,6 +87,7 @@ def test_v32k_shape_full_gradients(path):
     b = ref.lmhead_ce_backward(inp.X, inp.W, inp.targets, wl.V)
     ex, ew = rel_fro(np64(dX), b["dX"]), rel_fro(np64(dW), b["dW"])
     assert ex <= 2e-2 and ew <= 2e-2, (ex, ew)
+    assert_grads_elementwise(inp, dX, dW, b)
 
 
 def test_fused_full_size_repeatable():
@@ -122,8 +128,10 @@ def test_v128k_fused_every_token_and_sampled_dw_rows():
     never = np.flatnonzero(counts == 0)
     rows = np.unique(np.concatenate([np.arange(8), rng.choice(wl.V, 32, replace=False),
                                      rng.choice(never, 8, replace=False)]))
-    want = ref.lmhead_ce_dw_rows(inp.X, inp.W, inp.targets, lse, rows, n_valid)
+    want, dZv, g = ref.lmhead_ce_dw_rows(inp.X, inp.W, inp.targets, lse, rows, n_valid, return_dz=True)
     got = np64(o["dW"][torch.from_numpy(rows).cuda()])
+    M = term_magnitudes(dZv, g, inp.targets, cols=rows)
+    assert_within("dW rows", got, want, elementwise_u("bf16") * abs_matmul(M.T, inp.X))
     e = rel_fro(got, want)
     assert e <= 2e-2, f"dW sampled rows rel Frobenius {e:.3e}"
     # the frequent ids' rows carry the one-hot term: each is checked on its own too
