@@ -53,10 +53,10 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 // ------------------------------------------------------------------ forward
 // kStoreP = false: statistics only (the split forward; logits never stored).
-// kStoreP = true (the fused forward + backward): after the statistics pass the
-// epilogue reads the accumulator row a second time and writes
+// kStoreP = true (the fused forward + backward): the epilogue also writes
 // p = exp(z - m_tile) in fp16 through TMA, where m_tile is the row's maximum
-// over the tile's valid columns (stored in tmax).  p lies in (0, 1], where fp16
+// over the tile's valid columns (stored in tmax).  Both forms take the same
+// branches and sums, so their statistics are bit-identical.  p lies in (0, 1], where fp16
 // carries 11 significant bits, so the later gradient
 // exp(z - lse) = p * exp(m_tile - lse) keeps a relative error near 2^-11.
 template <bool kStoreP>
@@ -70,6 +70,73 @@ struct EpiLseStatsT {
     int maxseg;               // record slots per vocab tile
     float* tmax;              // [num_vtiles][N] row maximum of each tile (kStoreP)
   };
+  // A tile of 256 valid columns inside one shard (all but the tiles holding a
+  // shard edge or the vocabulary's end): one pass for the row maximum m over
+  // the tile, then one exp per logit, e = exp(z - m), summed into the tile's
+  // single (m, S) record and, with kStoreP, stored as p = e in fp16.
+  __device__ static void run_whole(const Params& p, const CUtensorMap* tm, uint32_t taddr, int64_t n, int nb,
+                                   int64_t v0, int64_t yl, bool row_ok, EpiCtx& ctx) {
+    float mx = -INFINITY, zyv = 0.f;
+    bool have_zy = false;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      uint32_t r[32];
+      __syncwarp();
+      tmem_ld32(taddr + c * 32, r);
+      tmem_ld_wait();
+      const int64_t j = yl - c * 32;
+      if (j >= 0 && j < 32) {
+        float v = 0.f;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v = (q == j) ? as_f(r[q]) : v;
+        zyv = v;
+        have_zy = true;
+      }
+      float cm = as_f(r[0]);
+#pragma unroll
+      for (int q = 1; q < 32; ++q) cm = fmaxf(cm, as_f(r[q]));
+      mx = fmaxf(mx, cm);
+    }
+    const float nt = -mx * kLog2e;
+    const bool warp_live = ctx.row0 < p.N;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 1
+    for (int b = 0; b < kBN / 64; ++b) {
+      uint32_t w[kStoreP ? 32 : 1];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(taddr + b * 64 + h * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 32; q += 4) {
+          const float e0 = ex2_approx(fmaf(as_f(r[q + 0]), kLog2e, nt));
+          const float e1 = ex2_approx(fmaf(as_f(r[q + 1]), kLog2e, nt));
+          const float e2 = ex2_approx(fmaf(as_f(r[q + 2]), kLog2e, nt));
+          const float e3 = ex2_approx(fmaf(as_f(r[q + 3]), kLog2e, nt));
+          a0 += e0;
+          a1 += e1;
+          a2 += e2;
+          a3 += e3;
+          if constexpr (kStoreP) {
+            w[h * 16 + q / 2] = pack_f16x2(e0, e1);
+            w[h * 16 + q / 2 + 1] = pack_f16x2(e2, e3);
+          }
+        }
+      }
+      // rows >= N are clipped by the tensor map
+      if constexpr (kStoreP) {
+        if (warp_live) stage_and_store(ctx, tm, w, static_cast<int32_t>(v0 + b * 64));
+      }
+    }
+    if (row_ok) {
+      p.partial[(static_cast<int64_t>(nb) * p.maxseg) * p.N + n] = make_float2(mx, (a0 + a1) + (a2 + a3));
+      if (have_zy) p.zy[n] = zyv;
+      if constexpr (kStoreP) p.tmax[static_cast<int64_t>(nb) * p.N + n] = mx;
+    }
+  }
+
   __device__ static void run(const Params& p, const CUtensorMap* tm, uint32_t taddr, int64_t n, int nb,
                              EpiCtx& ctx) {
     const int64_t v0 = static_cast<int64_t>(nb) * kBN;
@@ -79,6 +146,10 @@ struct EpiLseStatsT {
     const int64_t yl = y - v0;
     int64_t t = v0 / p.Vs;
     int64_t seg_end = min((t + 1) * p.Vs, vend);
+    if (vend - v0 == kBN && seg_end == vend) {
+      run_whole(p, tm, taddr, n, nb, v0, yl, row_ok, ctx);
+      return;
+    }
     int k = 0;
     float m = -INFINITY, s = 0.f, zyv = 0.f, tmx = -INFINITY;
     bool have_zy = false;
