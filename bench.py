@@ -68,8 +68,19 @@ def parse_args():
                    help="fused: one fwd+bwd call with saved probabilities; split: fwd, then bwd with recompute")
     p.add_argument("--other-path-steps", type=int, default=5, help="timed steps of the other path (0: skip)")
     p.add_argument("--embed-iters", type=int, default=20, help="launches per case of the gather microbench (0: skip)")
-    p.add_argument("--gemm-variant", choices=["pair", "single"], default="single",
-                   help="tcgen05 GEMM form: 256x256 tiles on SM pairs, or 128x256 tiles on one SM")
+    p.add_argument("--gemm-variant", choices=["single", "pair", "single128"], default="single",
+                   help="tcgen05 GEMM form: one SM per tile with dX in 256x256 tiles (default), 256x256 tiles on "
+                        "SM pairs, or 128x256 tiles on one SM for every GEMM")
+    p.add_argument("--token-chunk", type=int, default=0,
+                   help="fused path: token rows per chunk the workspace is sized for (0: the library's bounded "
+                        "default, saved probabilities <= 1 GiB; N: all tokens at once)")
+    p.add_argument("--vocab-chunk", type=int, default=0,
+                   help="split path: vocab ids per backward chunk (0: the library's default, one shard V/T; "
+                        "V: the whole vocabulary at once)")
+    p.add_argument("--unbounded-steps", type=int, default=5,
+                   help="timed steps of each path with one chunk (all N tokens / all V ids) for comparison (0: skip)")
+    p.add_argument("--configs", default="minimind,v32k,v128k,v152k",
+                   help="workloads of the per-config throughput table ('' to skip)")
     args = p.parse_args()
     if args.e2e_steps <= 0:
         args.e2e_steps = args.steps
@@ -368,6 +379,79 @@ def embed_bwd_microbench(vp, dev, iters=20):
     return out
 
 
+# ------------------------------------------------------------------ every config's throughput
+def config_table(vp, dev, names, rank, world, barrier):
+    """Both LM-head paths at each named workload's shape with the library's
+    default (bounded) workspaces: tokens/s, algorithmic (6NHV) and executed
+    TFLOP/s, % of the measured bf16 burst peak.  X and W are drawn on the device
+    from a seeded generator (N(0,1) and N(0,0.02^2), rounded to bf16), targets on
+    the host (uniform or Zipf(1.1), ignored positions) -- the workloads'
+    distributions; parity of these shapes is the tests' business.  Each case runs
+    about half a second of steps."""
+    import torch
+    import synth
+    if not names:
+        return None
+    peaks = load_peaks()
+    rows = []
+    for name in names:
+        wl = synth.WORKLOADS[name]
+        N, H, V, T = wl.N, wl.H, wl.V, wl.T
+        g = torch.Generator(device=dev).manual_seed(wl.seed + rank)
+        X = torch.randn(N, H, generator=g, device=dev).to(torch.bfloat16)
+        W = (torch.randn(V, H, generator=g, device=dev) * wl.w_std).to(torch.bfloat16)
+        rng = np.random.default_rng(wl.seed + rank)
+        yn = synth.zipf_ids(rng, N, V, wl.zipf_s) if wl.targets == "zipf" else rng.integers(0, V, N)
+        if wl.ignore_frac:
+            yn[rng.choice(N, int(wl.ignore_frac * N), replace=False)] = synth.IGNORE_INDEX
+        y = torch.from_numpy(yn.astype(np.int64)).to(dev)
+        o = {"loss": torch.empty(N, device=dev), "lse": torch.empty(N, device=dev),
+             "mean": torch.empty(1, device=dev), "n_bad": torch.empty(1, dtype=torch.int32, device=dev),
+             "dX": torch.empty_like(X), "dW": torch.empty((V, H), device=dev)}
+        for path in ("fused", "split"):
+            if path == "fused":
+                ws = [torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 2), dtype=torch.uint8, device=dev)]
+                run = lambda: vp.lmhead_ce_fwd_bwd(X, W, y, T, workspace=ws[0], out=o)
+            else:
+                ws = [torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 0), dtype=torch.uint8, device=dev),
+                      torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 1), dtype=torch.uint8, device=dev)]
+
+                def run():
+                    vp.lmhead_ce_fwd(X, W, y, T, workspace=ws[0], out=o)
+                    vp.lmhead_ce_bwd(X, W, y, o["lse"], T, workspace=ws[1], dX=o["dX"], dW=o["dW"])
+            for _ in range(3):
+                run()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            run()
+            e1.record()
+            torch.cuda.synchronize()
+            steps = int(min(200, max(3, 500.0 / max(e0.elapsed_time(e1), 1e-3))))
+            barrier()
+            e0.record()
+            for _ in range(steps):
+                run()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
+            assert all(vp.read_device_status(w) == 0 for w in ws)
+            alg = 6.0 * N * H * V / (ms / 1e3) / 1e12
+            exe = (6.0 if path == "fused" else 8.0) * N * H * V / (ms / 1e3) / 1e12
+            rows.append({"workload": name, "path": path, "N": N, "H": H, "V": V, "T": T, "steps": steps,
+                         "ms_per_step": ms, "tokens_per_s": job_tokens_per_s(N, world, 1, ms / 1e3),
+                         "tflops_algorithmic": alg, "tflops_executed": exe,
+                         "pct_bf16_burst_algorithmic": 100.0 * alg / peaks["bf16_tflops"],
+                         "pct_bf16_burst_executed": 100.0 * exe / peaks["bf16_tflops"],
+                         "workspace_bytes": int(sum(w.numel() for w in ws)),
+                         "l2": "inputs fit in L2" if (N + V) * H * 2 < 100e6 else "inputs larger than L2"})
+            del ws, run
+        del X, W, y, o
+        torch.cuda.empty_cache()
+    return {"note": "library default workspaces (fused: saved probabilities <= 1 GiB; split: one shard's dZ); "
+                    "X, W drawn on the device; no L2 flush (MiniMind's inputs stay in L2)", "rows": rows}
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args):
     import torch
@@ -389,7 +473,7 @@ def run_ours(args):
             time.sleep(1.0)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    vp.set_gemm_variant(args.gemm_variant == "pair")
+    vp.set_gemm_variant({"single": 0, "pair": 1, "single128": 2}[args.gemm_variant])
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
@@ -413,17 +497,21 @@ def run_ours(args):
     dW = torch.empty((V, H), dtype=torch.float32, device=dev)
     fo["dX"], fo["dW"] = dX, dW
 
-    def make_step(path):
-        """One step of the given path and the workspaces it uses."""
+    def make_step(path, chunk=None):
+        """One step of the given path and the workspaces it uses.  chunk: token
+        rows (fused) or vocab ids (split) the workspace is sized for; None takes
+        the command line's, 0 the library's bounded default."""
         if path == "fused":
-            ws = torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 2), dtype=torch.uint8, device=dev)
+            tc = args.token_chunk if chunk is None else chunk
+            ws = torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, tc), dtype=torch.uint8, device=dev)
 
             def step(Xs, ys):
                 vp.embed_fwd(ys, W, T, out=emb)
                 vp.lmhead_ce_fwd_bwd(Xs, W, ys, T, workspace=ws, out=fo)
             return step, [ws]
+        vc = args.vocab_chunk if chunk is None else chunk
         wsf = torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 0), dtype=torch.uint8, device=dev)
-        wsb = torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 1), dtype=torch.uint8, device=dev)
+        wsb = torch.empty(vp.workspace_size(N, H, V, T, vp.VP_BF16, 1, vc), dtype=torch.uint8, device=dev)
 
         def step(Xs, ys):
             vp.embed_fwd(ys, W, T, out=emb)
@@ -431,7 +519,35 @@ def run_ours(args):
             vp.lmhead_ce_bwd(Xs, W, ys, fo["lse"], T, workspace=wsb, dX=dX, dW=dW)
         return step, [wsf, wsb]
 
+    def time_path(path, chunk, steps):
+        """Brief timing of one path: ms per step, forward / backward ms, GEMM
+        chunks per step, workspace bytes."""
+        ostep, ows = make_step(path, chunk)
+        for _ in range(2):
+            ostep(X, y)
+        torch.cuda.synchronize()
+        barrier()
+        vp.stage_timing_enable(256 * steps + 64)
+        e0.record()
+        for _ in range(steps):
+            ostep(X, y)
+        e1.record()
+        torch.cuda.synchronize()
+        ost = vp.stage_timing_read()
+        vp.stage_timing_enable(0)
+        oms = max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
+        assert all(vp.read_device_status(w) == 0 for w in ows)
+        ofwd, obwd = fwd_bwd_ms(ost, steps)
+        r = {"path": path, "steps": steps, "ms_per_step": oms, "value": job_tokens_per_s(N, world, 1, oms / 1e3),
+             "unit": UNIT, "fwd_ms": ofwd, "bwd_ms": obwd, "chunks": ost.get("dw_gemm", (0, 0))[1] / steps,
+             "workspace_bytes": int(sum(w.numel() for w in ows)),
+             "pct_bf16_burst_algorithmic": 100.0 * 6.0 * N * H * V / (oms / 1e3) / 1e12 / load_peaks()["bf16_tflops"]}
+        del ostep, ows
+        torch.cuda.empty_cache()
+        return r
+
     step, workspaces = make_step(args.path)
+    ws_bytes = int(sum(w.numel() for w in workspaces))
     for _ in range(args.warmup):
         step(X, y)
     torch.cuda.synchronize()
@@ -440,7 +556,7 @@ def run_ours(args):
     # ---------------- timed region
     uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
     clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else None)
-    vp.stage_timing_enable(16 * args.steps + 64)
+    vp.stage_timing_enable(256 * args.steps + 64)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks.start()
     time.sleep(0.3)
@@ -498,7 +614,6 @@ def run_ours(args):
     h2d = Xh.numel() * 2 + yh.numel() * 8
     d2h = loss_h.numel() * 4 + 4
     assert all(vp.read_device_status(w) == 0 for w in workspaces)
-    del workspaces, step
 
     emb_micro = embed_microbench(vp, dev) if args.embed_iters > 0 else None
     emb_bwd_micro = embed_bwd_microbench(vp, dev) if args.embed_iters > 0 else None
@@ -507,26 +622,15 @@ def run_ours(args):
     other = None
     if args.other_path_steps > 0:
         opath = "split" if args.path == "fused" else "fused"
-        ostep, ows = make_step(opath)
-        for _ in range(2):
-            ostep(X, y)
-        torch.cuda.synchronize()
-        barrier()
-        vp.stage_timing_enable(16 * args.other_path_steps + 64)
-        e0.record()
-        for _ in range(args.other_path_steps):
-            ostep(X, y)
-        e1.record()
-        torch.cuda.synchronize()
-        ostages = vp.stage_timing_read()
-        vp.stage_timing_enable(0)
-        oms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.other_path_steps
-        assert all(vp.read_device_status(w) == 0 for w in ows)
-        ofwd, obwd = fwd_bwd_ms(ostages, args.other_path_steps)
-        other = {"path": opath, "steps": args.other_path_steps, "ms_per_step": oms,
-                 "value": job_tokens_per_s(N, world, 1, oms / 1e3), "unit": UNIT,
-                 "fwd_ms": ofwd, "bwd_ms": obwd}
-        del ostep, ows
+        other = time_path(opath, 0, args.other_path_steps)
+    # ---------------- both paths with one chunk (all N tokens, all V ids): the memory bound's cost
+    unbounded = None
+    if args.unbounded_steps > 0:
+        unbounded = {"fused": time_path("fused", N, args.unbounded_steps),
+                     "split": time_path("split", V, args.unbounded_steps)}
+    del step, workspaces
+    torch.cuda.empty_cache()
+    table = config_table(vp, dev, [c for c in args.configs.split(",") if c], rank, world, barrier)
 
     if rank != 0:
         if world > 1:
@@ -572,7 +676,10 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) X, N(0,0.02^2) W, Zipf targets)",
         "config": dict(workload_config(wl), parallelism=f"replicas x{world}, no data-path collective",
-                       path=args.path, chunks=1, gemm_variant=args.gemm_variant),
+                       path=args.path, gemm_variant=args.gemm_variant, workspace_bytes=ws_bytes,
+                       chunks_per_step=gemm_launches_per_stage,
+                       chunking=("token chunks; saved fp16 probabilities bounded by the workspace"
+                                 if args.path == "fused" else "vocab chunks; bf16 dZ of one chunk at a time")),
         "tflops_algorithmic": alg * args.steps / sec / 1e12,
         "tflops_executed": exe * args.steps / sec / 1e12,
         "pct_bf16_peak_algorithmic": 100.0 * alg * args.steps / sec / 1e12 / peaks["bf16_tflops"],
@@ -580,10 +687,11 @@ def run_ours(args):
         "roofline": {"kernel": ("umma_gemm_kernel (tcgen05; 3 launches/step: lse stats + saved p, dW, dX)"
                                 if args.path == "fused" else
                                 "umma_gemm_kernel (tcgen05; 4 launches/step: lse stats, dZ recompute, dW, dX)"),
-                     "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
-                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops_sustained"],
-                     "peak_kind": f"bf16 sustained ({peaks['source']})",
-                     "frac_of_burst": achieved / peaks["bf16_tflops"],
+                     "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "peak_kind": f"bf16 burst ({peaks['source']})",
+                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                     "peak_sustained": peaks["bf16_tflops_sustained"],
                      "traffic": gemm_traffic(wl.name, args.path, args.gemm_variant),
                      "launches_per_gemm_stage": gemm_launches_per_stage,
                      "traffic_unit": "bytes per GEMM stage (one 2NHV contraction; ncu dram read + write, "
@@ -607,6 +715,8 @@ def run_ours(args):
                         "other of two device buffers while the previous step computes) and the loss read back "
                         "every step; the weight W is model state resident in HBM"},
         "other_path": other,
+        "unbounded": unbounded,
+        "configs": table,
     }
     if world == 1 and not args.no_cpu_baseline:
         v, n, t = oracle_tokens_per_s(inp, args.cpu_seconds)

@@ -30,7 +30,8 @@
  *     nothing has been launched or written, except for VP_ERR_CUDA.
  *   - Every wait inside a kernel is bounded in time.  A wait that runs out
  *     sets a bit in the workspace's device status word (vp_read_device_status)
- *     and the kernel returns early; outputs are then undefined.
+ *     and the kernel returns early; outputs are then undefined, and a forward
+ *     whose GEMM gave up writes NaN to loss, lse and the shard statistics.
  */
 #ifndef VP_H
 #define VP_H
@@ -164,8 +165,12 @@ size_t vp_lmhead_ce_workspace_size(int64_t N, int64_t H, int64_t V, int T,
  * m_t, the local sum S_t = sum exp(z - m_t) and the local target logit
  * z_y^(t) (0 off-shard); an on-device merge gives
  *     m = max_t m_t,  S = sum_t S_t e^(m_t - m),  lse = m + log S,
- *     loss[n] = lse - z_y                      (0 for ignored targets),
+ *     loss[n] = log S - (z_y - m)              (0 for ignored targets),
  *     loss_mean = sum_n loss[n] / max(1, N_valid)   (sec. 5.3.3).
+ * S is carried as S = 1 + R, R the sum without one maximal term, and the loss
+ * is formed as log1p(R) + (m - z_y): two non-negative terms, so a loss far
+ * below lse (the target is the row's maximum by a wide margin) keeps its
+ * relative accuracy instead of cancelling.
  * A target equal to ignore_index, or outside [0,V), is ignored; the latter
  * kind is counted in n_bad.
  *
@@ -213,7 +218,11 @@ vp_status vp_lmhead_ce_fwd(const void* X, const void* W, const int64_t* targets,
  *     Calls whose executions overlap on the GPU (different streams, or
  *     different host threads on one device) race on it: serialise them.
  *   - The device status word lives in the shared array and is not readable
- *     through vp_read_device_status.
+ *     through vp_read_device_status; if a kernel gives up a wait, loss, lse,
+ *     loss_mean and shard_stats come out NaN instead.
+ *   - The array's device address is looked up on a device's first successful
+ *     call and kept; cudaDeviceReset unloads the library's device code, so do
+ *     not call this function on a device after resetting it in this process.
  */
 vp_status vp_lmhead_ce_fwd_noalloc(const void* X, const void* W, const int64_t* targets,
                                    int64_t N, int64_t H, int64_t V, int T,
@@ -324,6 +333,66 @@ vp_status vp_lmhead_ce_bwd_saved(const void* X, const void* W, const int64_t* ta
                                  int64_t ignore_index, vp_dtype dtype,
                                  void* dX, float* dW,
                                  void* saved, size_t saved_bytes, void* stream);
+
+/*
+ * One shard per rank: the building blocks of the T-GPU form.
+ *
+ * "Vocab Parallelism" sec. 5.3.1 and the interview note's figure 2: each of T
+ * ranks holds only its shard W_t = W[t*V/T, (t+1)*V/T) and computes, for every
+ * token, three scalars of its logits slice; three all-reduces of [B,S]
+ * tensors (MAX, SUM, SUM) combine them.  Sec. 5.3.2 and the key formulas: the
+ * logit gradient is local to each rank, dW_t stays local, and the LM head's dX
+ * is all-reduced over ranks.  A rank runs
+ *     vp_lmhead_ce_shard_fwd  -> stats_t [3][N]
+ *     (all-gather of stats_t over the T ranks: [T][3][N]; the caller's collective)
+ *     vp_lmhead_ce_merge_stats -> loss, lse (every rank the same)
+ *     vp_lmhead_ce_shard_bwd  -> dX_t (fp32), dW_t
+ *     (all-reduce SUM of dX_t over the ranks: dX; the caller's collective)
+ * One all-gather of 3 floats per token replaces the three all-reduces (m_t is
+ * kept local, so the sums need no second round).  On one GPU these calls run
+ * the ranks one after another; the library itself never talks to another GPU.
+ *
+ * vp_lmhead_ce_shard_fwd -- shard t's statistics.
+ *   X        dtype [N,H];   W_t  dtype [V/T,H], the shard's rows of the weight
+ *   targets  int64 [N]      ids of the whole vocabulary [0,V)
+ *   stats    f32 [3][N]     written: m_t (the shard's max logit), R_t = S_t - 1
+ *                           (sum of exp(z - m_t) over the shard except one
+ *                           maximal term, kept apart from the 1 for accuracy),
+ *                           z_y^(t) (the target logit if the valid target lies
+ *                           in the shard, else 0)
+ *   workspace >= vp_lmhead_ce_workspace_size(N, H, V/T, 1, dtype, 0, 0) bytes
+ *   0 <= t < T, V % T == 0 (else VP_ERR_INVALID_ARG); other rules as vp_lmhead_ce_fwd.
+ *
+ * vp_lmhead_ce_merge_stats -- the merge of the gathered statistics.
+ *   stats    f32 [T][3][N]  shard t's stats_t at [t] (device memory)
+ *   writes loss [N], lse [N] as vp_lmhead_ce_fwd does (m = max_t m_t,
+ *   1 + R = sum_t (1 + R_t) e^(m_t - m), z_y = sum_t z_y^(t),
+ *   loss = log1p(R) + (m - z_y), lse = m + log1p(R)), and loss_mean / n_bad
+ *   when not NULL.
+ *
+ * vp_lmhead_ce_shard_bwd -- shard t's backward, recomputing its logits.
+ *   lse      f32 [N]        from vp_lmhead_ce_merge_stats
+ *   dloss / dmean           as in vp_lmhead_ce_bwd (N_valid counts the whole batch)
+ *   dX_t     f32 [N,H]      overwritten: dZ_t W_t, this shard's part of dX (sum
+ *                           over t, then round to the training dtype)
+ *   dW_t     f32 [V/T,H]    overwritten: dZ_t^T X, complete for the shard
+ *   workspace >= vp_lmhead_ce_workspace_size(N, H, V/T, 1, dtype, 1, chunk)
+ *             for some vocab chunk (the call derives it from the bytes)
+ */
+vp_status vp_lmhead_ce_shard_fwd(const void* X, const void* W_t, const int64_t* targets,
+                                 int64_t N, int64_t H, int64_t V, int T, int t,
+                                 int64_t ignore_index, vp_dtype dtype, float* stats,
+                                 void* workspace, size_t ws_bytes, void* stream);
+vp_status vp_lmhead_ce_merge_stats(const float* stats, const int64_t* targets,
+                                   int64_t N, int64_t V, int T, int64_t ignore_index,
+                                   float* loss, float* lse, float* loss_mean, int32_t* n_bad,
+                                   void* stream);
+vp_status vp_lmhead_ce_shard_bwd(const void* X, const void* W_t, const int64_t* targets,
+                                 const float* lse, const float* dloss, const float* dmean,
+                                 int64_t N, int64_t H, int64_t V, int T, int t,
+                                 int64_t ignore_index, vp_dtype dtype,
+                                 float* dX_t, float* dW_t,
+                                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * vp_read_device_status -- synchronise `stream` and copy the device status

@@ -31,12 +31,36 @@ vp_status vp_test_gemm_bf16(const void* A, const void* B, float* D, int64_t M, i
 
 /*
  * vp_test_set_gemm_variant -- select the tcgen05 GEMM form used by every
- * later bf16 call in this process: 1 runs each 256 x 256 tile on a pair of
- * SMs (cta_group::2, a cluster of 2 CTAs), 0 (default) runs each 128 x 256
- * tile on one SM.  Both compute the same results; this exists to compare them
- * (under a sustained power cap the one-SM form has measured faster).
+ * later bf16 call in this process:
+ *   0 (default): one SM per tile; the dX contraction in 256 x 256 tiles (two
+ *      128-row blocks sharing each B stage, B streamed half as often), the
+ *      other GEMMs in 128 x 256 tiles with the epilogue overlapping the MMAs;
+ *   1: each 256 x 256 tile on a pair of SMs (cta_group::2, a cluster of 2 CTAs);
+ *   2: one SM per 128 x 256 tile for every GEMM, dX included.
+ * All compute the same results; this exists to compare them.  Other values:
+ * VP_ERR_INVALID_ARG.
  */
-vp_status vp_test_set_gemm_variant(int pair);
+vp_status vp_test_set_gemm_variant(int variant);
+
+/*
+ * vp_test_set_wait_fault -- exercise the bounded waits of the tcgen05 GEMMs.
+ * Applies to every later bf16 GEMM launch of this process (one-SM form):
+ *   mode 0: normal operation (the default);
+ *   mode 1: the TMA producer issues no load, so the MMA issuer's wait for
+ *           data runs out (VP_DEV_TIMEOUT_MMA) and the epilogue's wait for an
+ *           accumulator ends with it (VP_DEV_TIMEOUT_EPILOGUE);
+ *   mode 2: the MMA issuer issues no MMA, so the producer's wait for a free
+ *           stage runs out with its loads in flight (VP_DEV_TIMEOUT_PRODUCER;
+ *           it first waits for those loads to land) and the epilogue's wait
+ *           ends with it.
+ *   wait_ns: the limit of every mbarrier wait in those launches; 0 restores
+ *           the default (1 s).
+ * A CTA that gives up drains what it issued, frees its tensor memory and
+ * exits; the call's forward outputs (loss, lse, shard statistics) come out NaN
+ * and the workspace's status word holds the bits.  The SM-pair GEMM form
+ * honours wait_ns but not mode.  Process-global, not thread-safe.
+ */
+vp_status vp_test_set_wait_fault(int mode, uint64_t wait_ns);
 
 /*
  * Stage timing for measurement harnesses.  While enabled, every libvp call

@@ -85,25 +85,33 @@ def test_ce_rejects_bad_arguments(lib):
 def test_workspace_sizes(lib):
     N, H, V, T = 16384, 4096, 128256, 8
     fwd = vp.workspace_size(N, H, V, T, vp.VP_BF16, 0)
-    # records: ceil(V/256) tiles x 2 segment slots x N tokens x (m, S) fp32, plus z_y
+    # records: ceil(V/256) tiles x 2 segment slots x N tokens x (m, R) fp32, plus z_y
     assert fwd >= 501 * 2 * N * 8 + N * 4 and fwd < 501 * 2 * N * 8 + N * 4 + 4096
-    one = vp.workspace_size(N, H, V, T, vp.VP_BF16, 1)
+    one = vp.workspace_size(N, H, V, T, vp.VP_BF16, 1, V)
     assert one >= N * V * 2 and one < N * V * 2 + N * 4 + 4096       # one chunk: bf16 dZ, no fp32 dX partial
-    c = vp.workspace_size(N, H, V, T, vp.VP_BF16, 1, 16032)
-    assert c >= N * 15872 * 2 + N * H * 4                              # chunk rounded to 256, + fp32 dX partial
+    # default: one shard's dZ (V/T = 16032 rounded up to 16128) plus the fp32 dX partial
+    d = vp.workspace_size(N, H, V, T, vp.VP_BF16, 1)
+    assert N * 16128 * 2 + N * H * 4 <= d < N * 16128 * 2 + N * H * 4 + N * 4 + 4096
+    assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 1, 16032) == d
+    assert vp.workspace_size(N, H, V, 1, vp.VP_BF16, 1) == one          # T = 1: the shard is all of V
     assert vp.workspace_size(N, H, V, 7, vp.VP_BF16, 1) == 0           # V % T != 0
     assert vp.workspace_size(6, 64, 16, 4, vp.VP_F32, 4) == 0          # unknown pass
 
 
 def test_fused_workspace_sizes(lib):
     N, H, V, T = 16384, 4096, 128256, 8
-    full = vp.workspace_size(N, H, V, T, vp.VP_BF16, 2)
-    # fp16 p / bf16 dZ [N, V] + per tile and token: 2 (m, S) slots, the tile max; + z_y, g
+    full = vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, N)
+    # fp16 p / bf16 dZ [N, V] + per tile and token: 2 (m, R) slots, the tile max; + z_y, g
     body = N * V * 2 + 501 * N * (2 * 8 + 4) + 2 * N * 4
     assert body <= full < body + 8192
     half = vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 8192)
     assert half < full / 2 + N * 8 and half > full / 2 - N * V
     assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 100) == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 128)
+    # default: saved probabilities of at most 1 GiB (4096 token rows of V = 128256)
+    assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 2) == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 4096)
+    # small problems fit in one chunk by default
+    assert vp.workspace_size(4096, 512, 6400, 2, vp.VP_BF16, 2) == vp.workspace_size(4096, 512, 6400, 2,
+                                                                                        vp.VP_BF16, 2, 4096)
     # fp32: the larger of the split forward and backward
     f32 = vp.workspace_size(6, 64, 16, 4, vp.VP_F32, 2)
     assert f32 == max(vp.workspace_size(6, 64, 16, 4, vp.VP_F32, 0), vp.workspace_size(6, 64, 16, 4, vp.VP_F32, 1))
@@ -163,7 +171,7 @@ def test_keep_saved_rejects_bad_arguments(lib):
     loss, lse, dX, dW = P(0x50000), P(0x60000), P(0x70000), P(0x80000)
     N, H, V, T = 16384, 4096, 128256, 8
     full = vp.workspace_size(N, H, V, T, vp.VP_BF16, 3)
-    assert full == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2)     # the whole batch's fused state
+    assert full == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, N)  # the whole batch's fused state
     fk, bs = lib.vp_lmhead_ce_fwd_keep, lib.vp_lmhead_ce_bwd_saved
     assert fk(X, W, y, 300, 64, 1000, 3, -100, vp.VP_BF16, loss, lse, None, None, None, sv, 1 << 30, None) == 1
     assert fk(X, W, y, 300, 64, 1000, 4, -100, vp.VP_BF16, None, lse, None, None, None, sv, 1 << 30, None) == 1

@@ -63,8 +63,10 @@ CASES = [  # N, H, V, T, dtype, ids
     (300, 136, 1000, 8, "bf16", "uniform"),
     (300, 64, 50, 5, "bf16", "uniform"),          # ids repeat ~6 times: segments cross runs
     (1000, 256, 5000, 4, "bf16", "zipf"),         # id 0 spans many runs
-    (4097, 64, 2048, 2, "bf16", "zipf"),          # n_pad 8192: 16 sorted chunks, 8-way then 2-way merges
-    (9000, 128, 4000, 8, "f32", "zipf"),          # n_pad 16384: 32 sorted chunks, 8-way then 4-way merges
+    (513, 64, 700, 2, "bf16", "uniform"),         # n_pad 1024: 2 sorted chunks, one rank placement
+    (4097, 64, 2048, 2, "bf16", "zipf"),          # n_pad 8192: 16 sorted chunks, one rank placement
+    (9000, 128, 4000, 8, "f32", "zipf"),          # n_pad 16384: 32 sorted chunks, one rank placement
+    (16384, 64, 128256, 8, "bf16", "uniform"),    # the V128k id count, uniform: mostly one token per id
     (20000, 64, 3000, 4, "bf16", "zipf"),         # n_pad 32768: 64 sorted chunks, two 8-way merges
 ]
 

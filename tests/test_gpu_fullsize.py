@@ -1,9 +1,18 @@
-"""Parity at the full workload sizes, in the launch configuration the bench
-times (one vocab chunk): the oracle recomputes sampled token rows one at a
-time (loss, lse, dX rows) and sampled vocab rows of dW; dW is also checked
-through identities that hold at any size, and in full at the V32k shape with
-fewer tokens.  Gradient entries are compared one by one against the bound of
-gpu_util.assert_grads_elementwise, besides the per-tensor tolerance."""
+"""Parity at every workload's full size, for both LM-head paths and for every
+shard count T in {1, 2, the workload's T, 16} (each divides V), in the launch
+configuration the bench times (the library's default, bounded workspaces).
+
+- MiniMind (N=4096, H=512, V=6400) and V32k (N=8192, H=4096, V=32000): every
+  token's loss and lse, every shard statistic, and every dX and dW entry.
+- V128k (N=16384, H=4096, V=128256) and V152k (N=32768, H=5120, V=151936, 10%
+  of positions ignore_index): every token's loss and lse (float64 oracle over
+  all rows, in row batches), 256 sampled dX rows, and dW rows of the 8 most
+  frequent, 32 random and 8 never-targeted vocab ids; ignored positions give a
+  zero loss and zero dX rows; dW identities that hold at any size.
+
+The oracle is computed once per workload (it does not depend on T or on the
+path).  Gradient entries are held to the elementwise bound of
+gpu_util.assert_grads_elementwise as well as the per-tensor tolerance."""
 import gc
 
 import numpy as np
@@ -13,10 +22,17 @@ import torch
 import oracle.ref as ref
 import synth
 import vocab_lm_head_vp_b300 as vp
-from gpu_util import (abs_matmul, assert_grads_elementwise, assert_loss_close, assert_within, dev_inputs,
-                      elementwise_u, np64, rel_fro, term_magnitudes)
+from gpu_util import (abs_matmul, assert_loss_close, assert_stats_close, assert_within, dev_inputs, elementwise_u,
+                      np64, rel_fro, term_magnitudes)
 
 pytestmark = pytest.mark.gpu
+IGN = -100
+SHARDS = {"minimind": (1, 2, 16), "v32k": (1, 2, 4, 16), "v128k": (1, 2, 8, 16), "v152k": (1, 2, 8, 16)}
+# "_all": one chunk (all N tokens' probabilities, or all V ids' dZ, held at once), at the workload's own T
+CASES = [(name, T, path) for name, ts in SHARDS.items() for T in ts for path in ("fused", "split")]
+CASES = CASES[:CASES.index(("v128k", 16, "split")) + 1] + [("v128k", 8, "fused_all"), ("v128k", 8, "split_all")] \
+    + CASES[CASES.index(("v128k", 16, "split")) + 1:]
+_CACHE = {}
 
 
 @pytest.fixture(autouse=True)
@@ -26,68 +42,116 @@ def _free():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("path", ["split", "fused"])
-@pytest.mark.parametrize("name", ["v32k", "v128k", "v152k"])
-def test_fullsize_sampled_rows(name, path):
-    """``split``: vp_lmhead_ce_fwd + vp_lmhead_ce_bwd; ``fused``:
-    vp_lmhead_ce_fwd_bwd (the call the bench times), all tokens in one chunk."""
+def _dense(name):
+    """MiniMind / V32k: the whole oracle, and the elementwise gradient bounds."""
     inp = synth.make_inputs(name)
     wl = inp.wl
-    X, W, y = dev_inputs(inp)
-    if path == "split":
-        f = vp.lmhead_ce_fwd(X, W, y, wl.T)
-        dX, dW = vp.lmhead_ce_bwd(X, W, y, f["lse"], wl.T)
-    else:
-        f = vp.lmhead_ce_fwd_bwd(X, W, y, wl.T)
-        dX, dW = f["dX"], f["dW"]
-    torch.cuda.synchronize()
-    assert vp.read_device_status(f["workspace"]) == 0
-    valid = (inp.targets >= 0) & (inp.targets < wl.V)
+    Z = ref.logits(inp.X, inp.W)
+    fwd = ref.cross_entropy(Z, inp.targets)
+    stats = {T: ref.shard_local_stats(Z, inp.targets, wl.V, T) for T in SHARDS[name]}
+    g = ref.upstream_scale(inp.targets, wl.V)
+    dZ = ref.grad_logits(Z, inp.targets, fwd["lse"], g)
+    del Z
+    dX, dW = ref.lmhead_grads(inp.X, inp.W, dZ)
+    M = term_magnitudes(dZ, g, inp.targets)
+    del dZ
+    u = elementwise_u("bf16")
+    bx, bw = u * abs_matmul(M, inp.W), u * abs_matmul(M.T, inp.X)
+    return {"inp": inp, "fwd": fwd, "stats": stats, "dX": dX, "dW": dW, "bx": bx, "bw": bw}
+
+
+def _sampled(name):
+    """V128k / V152k: every token's loss and lse; sampled dX and dW rows."""
+    inp = synth.make_inputs(name)
+    wl = inp.wl
+    valid, _ = ref.target_masks(inp.targets, wl.V)
     n_valid = int(valid.sum())
-    assert int(f["n_bad"].item()) == 0
+    parts = [ref.lmhead_ce_rows(inp.X, inp.W, inp.targets, np.arange(a, min(a + 2048, wl.N)), n_valid,
+                                with_dx=False) for a in range(0, wl.N, 2048)]
+    lse = np.concatenate([p["lse"] for p in parts])
+    loss = np.concatenate([p["loss"] for p in parts])
     rng = np.random.default_rng(99)
-    rows = np.sort(rng.choice(wl.N, 24, replace=False))
+    rows = np.sort(rng.choice(wl.N, 256, replace=False))
     o = ref.lmhead_ce_rows(inp.X, inp.W, inp.targets, rows, n_valid)
-    rt = torch.from_numpy(rows).cuda()
-    assert_loss_close(np64(f["lse"][rt]), o["lse"], "bf16", what="lse")
-    assert_loss_close(np64(f["loss"][rt]), o["loss"], "bf16", scale=o["lse"], what="loss")
-    e = rel_fro(np64(dX[rt]), o["dX"])
-    assert e <= 2e-2, f"dX sampled rows rel Frobenius {e:.3e}"
-    M = term_magnitudes(o["dZ"], o["g"], inp.targets[rows])
-    assert_within("dX rows", np64(dX[rt]), o["dX"], elementwise_u("bf16") * abs_matmul(M, inp.W))
-    # mean over valid tokens is the mean of the per-token losses
-    loss = np64(f["loss"])
-    assert abs(float(f["mean"].item()) - loss.sum() / n_valid) <= 1e-5 * abs(loss.sum() / n_valid)
+    u = elementwise_u("bf16")
+    Mx = term_magnitudes(o["dZ"], o["g"], inp.targets[rows])
+    counts = np.bincount(inp.targets[valid], minlength=wl.V)
+    never = np.flatnonzero(counts == 0)
+    vrows = np.unique(np.concatenate([np.argsort(-counts, kind="stable")[:8], rng.choice(wl.V, 32, replace=False),
+                                      rng.choice(never, 8, replace=False)]))
+    want_w, dZv, g = ref.lmhead_ce_dw_rows(inp.X, inp.W, inp.targets, lse, vrows, n_valid, return_dz=True)
+    Mw = term_magnitudes(dZv, g, inp.targets, cols=vrows)
+    return {"inp": inp, "lse": lse, "loss": loss, "mean": float(loss.sum()) / max(1, n_valid),
+            "n_valid": n_valid, "rows": rows, "dX_rows": o["dX"], "bx": u * abs_matmul(Mx, inp.W),
+            "vrows": vrows, "dW_rows": want_w, "bw": u * abs_matmul(Mw.T, inp.X), "top8": np.argsort(-counts)[:8]}
+
+
+def _oracle(name):
+    if name not in _CACHE:
+        _CACHE.clear()   # one workload's oracle at a time (the cases run grouped by workload)
+        _CACHE[name] = _dense(name) if name in ("minimind", "v32k") else _sampled(name)
+    return _CACHE[name]
+
+
+def _run(inp, T, path, stats):
+    X, W, y = dev_inputs(inp)
+    wl = inp.wl
+    if path.startswith("split"):
+        f = vp.lmhead_ce_fwd(X, W, y, T, shard_stats=stats)
+        dX, dW = vp.lmhead_ce_bwd(X, W, y, f["lse"], T, vocab_chunk=wl.V if path.endswith("_all") else None)
+        ws = f["workspace"]
+    else:
+        f = vp.lmhead_ce_fwd_bwd(X, W, y, T, shard_stats=stats, token_chunk=wl.N if path.endswith("_all") else None)
+        dX, dW, ws = f["dX"], f["dW"], f["workspace"]
+    torch.cuda.synchronize()
+    assert vp.read_device_status(ws) == 0
+    return X, W, f, dX, dW
+
+
+@pytest.mark.parametrize("name,T,path", CASES)
+def test_config_parity(name, T, path):
+    o = _oracle(name)
+    inp = o["inp"]
+    wl = inp.wl
+    dense = "fwd" in o
+    X, W, f, dX, dW = _run(inp, T, path, stats=dense)
+    assert int(f["n_bad"].item()) == 0
+    if dense:
+        assert_loss_close(np64(f["lse"]), o["fwd"]["lse"], "bf16", what="lse")
+        assert_loss_close(np64(f["loss"]), o["fwd"]["loss"], "bf16", what="loss")
+        assert_loss_close(np64(f["mean"]), [o["fwd"]["mean"]], "bf16", what="mean")
+        assert_stats_close(np64(f["shard_stats"]), o["stats"][T], inp, T)
+        ex, ew = rel_fro(np64(dX), o["dX"]), rel_fro(np64(dW), o["dW"])
+        assert ex <= 2e-2 and ew <= 2e-2, (ex, ew)
+        assert_within("dX", np64(dX), o["dX"], o["bx"])
+        assert_within("dW", np64(dW), o["dW"], o["bw"])
+        return
+    assert_loss_close(np64(f["lse"]), o["lse"], "bf16", what="lse")
+    assert_loss_close(np64(f["loss"]), o["loss"], "bf16", what="loss")
+    assert_loss_close(np64(f["mean"]), [o["mean"]], "bf16", what="mean")
+    rt = torch.from_numpy(o["rows"]).cuda()
+    got = np64(dX[rt])
+    assert rel_fro(got, o["dX_rows"]) <= 2e-2
+    assert_within("dX rows", got, o["dX_rows"], o["bx"])
+    vt = torch.from_numpy(o["vrows"]).cuda()
+    gw = np64(dW[vt])
+    assert rel_fro(gw, o["dW_rows"]) <= 2e-2
+    assert_within("dW rows", gw, o["dW_rows"], o["bw"])
+    for k, v in enumerate(o["vrows"]):   # the frequent ids' rows carry the one-hot term: each on its own too
+        if v in o["top8"]:
+            assert rel_fro(gw[k], o["dW_rows"][k]) <= 2e-2, int(v)
+    ign = np.flatnonzero(inp.targets == IGN)
+    if len(ign):
+        it = torch.from_numpy(ign).cuda()
+        assert bool((f["loss"][it] == 0).all()) and bool((dX[it] == 0).all())
     # dW identities: sum_v dW[v,:] = 0 (dZ rows sum to 0); <dW, W> = <dX, X> (= <dZ, Z>)
     dWd = dW.double()
     # bf16 rounding of dZ leaves |sum_v dZ[n,v]| ~ 2^-9 |dZ[n]|, i.e. a column-sum
     # norm ~ 2e-3 |dW|; a dropped or misplaced onehot term gives ~ |dW|
-    colsum = dWd.sum(0).norm().item()
-    assert colsum <= 1e-2 * dWd.norm().item(), (colsum, dWd.norm().item())
+    assert dWd.sum(0).norm().item() <= 1e-2 * dWd.norm().item()
     a = (dWd * W.double()).sum().item()
     b = (dX.double() * X.double()).sum().item()
     assert abs(a - b) <= 2e-2 * max(abs(a), abs(b)) + 1e-6, (a, b)
-
-
-@pytest.mark.parametrize("path", ["split", "fused"])
-def test_v32k_shape_full_gradients(path):
-    """H=4096, V=32000, T=4 with 512 tokens: every loss and every dX/dW entry."""
-    inp = synth.make_inputs("v32k", N=512)
-    wl = inp.wl
-    X, W, y = dev_inputs(inp)
-    if path == "split":
-        f = vp.lmhead_ce_fwd(X, W, y, wl.T, shard_stats=True)
-        dX, dW = vp.lmhead_ce_bwd(X, W, y, f["lse"], wl.T)
-    else:
-        f = vp.lmhead_ce_fwd_bwd(X, W, y, wl.T, shard_stats=True)
-        dX, dW = f["dX"], f["dW"]
-    torch.cuda.synchronize()
-    o = ref.lmhead_ce_forward(inp.X, inp.W, inp.targets, wl.V, wl.T)
-    assert_loss_close(np64(f["loss"]), o["loss"], "bf16", scale=o["lse"])
-    b = ref.lmhead_ce_backward(inp.X, inp.W, inp.targets, wl.V)
-    ex, ew = rel_fro(np64(dX), b["dX"]), rel_fro(np64(dW), b["dW"])
-    assert ex <= 2e-2 and ew <= 2e-2, (ex, ew)
-    assert_grads_elementwise(inp, dX, dW, b)
 
 
 def test_fused_full_size_repeatable():
@@ -101,40 +165,3 @@ def test_fused_full_size_repeatable():
     torch.cuda.synchronize()
     for k in ("loss", "lse", "mean", "dX", "dW"):
         assert torch.equal(a[k], b[k]), k
-
-
-def test_v128k_fused_every_token_and_sampled_dw_rows():
-    """The bench's workload through the fused call it times: every token's loss
-    and lse against the oracle's (all 16384 rows in float64, row batches), and
-    dW rows of sampled vocab ids -- the most frequent Zipf targets, random ids,
-    never-targeted ones -- against the oracle's own columns of the logit
-    gradient."""
-    inp = synth.make_inputs("v128k")
-    wl = inp.wl
-    X, W, y = dev_inputs(inp)
-    o = vp.lmhead_ce_fwd_bwd(X, W, y, wl.T)
-    torch.cuda.synchronize()
-    assert vp.read_device_status(o["workspace"]) == 0
-    valid = (inp.targets >= 0) & (inp.targets < wl.V)
-    n_valid = int(valid.sum())
-    parts = [ref.lmhead_ce_rows(inp.X, inp.W, inp.targets, np.arange(a, min(a + 2048, wl.N)), n_valid,
-                                with_dx=False) for a in range(0, wl.N, 2048)]
-    lse = np.concatenate([p["lse"] for p in parts])
-    loss = np.concatenate([p["loss"] for p in parts])
-    assert_loss_close(np64(o["lse"]), lse, "bf16", what="lse")
-    assert_loss_close(np64(o["loss"]), loss, "bf16", scale=lse, what="loss")
-    rng = np.random.default_rng(123)
-    counts = np.bincount(inp.targets[valid], minlength=wl.V)
-    never = np.flatnonzero(counts == 0)
-    rows = np.unique(np.concatenate([np.arange(8), rng.choice(wl.V, 32, replace=False),
-                                     rng.choice(never, 8, replace=False)]))
-    want, dZv, g = ref.lmhead_ce_dw_rows(inp.X, inp.W, inp.targets, lse, rows, n_valid, return_dz=True)
-    got = np64(o["dW"][torch.from_numpy(rows).cuda()])
-    M = term_magnitudes(dZv, g, inp.targets, cols=rows)
-    assert_within("dW rows", got, want, elementwise_u("bf16") * abs_matmul(M.T, inp.X))
-    e = rel_fro(got, want)
-    assert e <= 2e-2, f"dW sampled rows rel Frobenius {e:.3e}"
-    # the frequent ids' rows carry the one-hot term: each is checked on its own too
-    for k in range(8):
-        ek = rel_fro(got[k], want[k])
-        assert ek <= 2e-2, (int(rows[k]), ek)

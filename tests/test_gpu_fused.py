@@ -122,15 +122,15 @@ def test_fused_tiny_config_and_repeatable():
     assert torch.equal(a[0]["loss"], b[0]["loss"]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
 
 
-@pytest.mark.parametrize("pair", [True, False])
-def test_fused_gemm_forms(pair):
-    vp.set_gemm_variant(pair)
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_fused_gemm_forms(variant):
+    vp.set_gemm_variant(variant)
     try:
         inp = synth.small_case(333, 264, 1800, 6, "bf16", seed=77, ignore_frac=0.1)
         o, dX, dW = _fused(inp, 6, token_chunk=256)
         _check(inp, 6, o, dX, dW)
     finally:
-        vp.set_gemm_variant(False)
+        vp.set_gemm_variant(0)
 
 
 def test_fused_loss_scale_dmean():

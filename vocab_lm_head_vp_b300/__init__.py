@@ -18,8 +18,9 @@ import os
 
 import torch
 
-__all__ = ["embed_fwd", "embed_fwd_sp", "embed_bwd", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce_fwd_bwd", "lmhead_ce", "workspace_size", "read_device_status",
-           "test_gemm_bf16", "set_gemm_variant", "stage_timing_enable", "stage_timing_read", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
+__all__ = ["embed_fwd", "embed_fwd_sp", "embed_bwd", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce_fwd_bwd", "lmhead_ce",
+           "lmhead_ce_shard_fwd", "lmhead_ce_merge_stats", "lmhead_ce_shard_bwd", "vocab_parallel_lmhead_ce", "workspace_size", "read_device_status",
+           "test_gemm_bf16", "set_gemm_variant", "set_wait_fault", "stage_timing_enable", "stage_timing_read", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
 
 VP_F32, VP_BF16 = 0, 1
 IGNORE_INDEX = -100
@@ -71,12 +72,22 @@ def _load():
     L.vp_lmhead_ce_fwd_keep.argtypes = [P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, P, P, P, SZ, P]
     L.vp_lmhead_ce_bwd_saved.restype = I32
     L.vp_lmhead_ce_bwd_saved.argtypes = [P, P, P, P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, SZ, P]
+    L.vp_lmhead_ce_shard_fwd.restype = I32
+    L.vp_lmhead_ce_shard_fwd.argtypes = [P, P, P, I64, I64, I64, I32, I32, I64, I32, P, P, SZ, P]
+    L.vp_lmhead_ce_merge_stats.restype = I32
+    L.vp_lmhead_ce_merge_stats.argtypes = [P, P, I64, I64, I32, I64, P, P, P, P, P]
+    L.vp_lmhead_ce_shard_bwd.restype = I32
+    L.vp_lmhead_ce_shard_bwd.argtypes = [P, P, P, P, P, P, I64, I64, I64, I32, I32, I64, I32, P, P, P, SZ, P]
     L.vp_read_device_status.restype = I32
     L.vp_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     L.vp_test_gemm_bf16.restype = I32
     L.vp_test_gemm_bf16.argtypes = [P, P, P, I64, I64, I64, U, U, P, P]
     L.vp_test_set_gemm_variant.restype = I32
     L.vp_test_set_gemm_variant.argtypes = [I32]
+    L.vp_test_set_wait_fault.restype = I32
+    L.vp_test_set_wait_fault.argtypes = [I32, ctypes.c_uint64]
+    L.vp_lmhead_ce_fwd_noalloc.restype = I32
+    L.vp_lmhead_ce_fwd_noalloc.argtypes = [P, P, P, I64, I64, I64, I32, I64, I32, P, P, P, P, P, P]
     L.vp_stage_timing_enable.restype = I32
     L.vp_stage_timing_enable.argtypes = [I32]
     L.vp_stage_timing_read.restype = I32
@@ -312,6 +323,92 @@ def lmhead_ce_fwd_bwd(X, W, targets, T, ignore_index=IGNORE_INDEX, dloss=None, s
     return out
 
 
+def lmhead_ce_shard_fwd(X, W_t, targets, V, T, t, ignore_index=IGNORE_INDEX, workspace=None, stats=None):
+    """Shard t's statistics [3, N] = (m_t, R_t = S_t - 1, z_y^(t)) from its own
+    rows W_t = W[t V/T, (t+1) V/T) (the rank of a T-rank vocabulary)."""
+    _need(X, "X")
+    _need(W_t, "W_t", X.dtype, X.device)
+    _need(targets, "targets", torch.int64, X.device)
+    N, H = X.shape
+    dev = X.device
+    if stats is None:
+        stats = torch.empty((3, N), dtype=torch.float32, device=dev)
+    _need(stats, "stats", torch.float32, dev)
+    nb = workspace_size(N, H, V // T, 1, _dtype_code(X), 0)
+    if nb == 0:
+        raise VpError("vp_lmhead_ce_workspace_size", 1)
+    ws = _workspace(nb, dev, workspace)
+    _check("vp_lmhead_ce_shard_fwd", _load().vp_lmhead_ce_shard_fwd(
+        _ptr(X), _ptr(W_t), _ptr(targets), N, H, V, T, t, ignore_index, _dtype_code(X), _ptr(stats), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(dev)))
+    return stats
+
+
+def lmhead_ce_merge_stats(stats, targets, V, T, ignore_index=IGNORE_INDEX, out=None) -> dict:
+    """Merge of the T shards' gathered statistics [T, 3, N] into loss, lse,
+    mean and n_bad (the result vp_lmhead_ce_fwd gives for the whole W)."""
+    _need(stats, "stats", torch.float32)
+    _need(targets, "targets", torch.int64, stats.device)
+    N = targets.numel()
+    if tuple(stats.shape) != (T, 3, N):
+        raise ValueError(f"stats must be [T, 3, N] = [{T}, 3, {N}], got {tuple(stats.shape)}")
+    dev = stats.device
+    if out is None:
+        out = {"loss": torch.empty(N, dtype=torch.float32, device=dev),
+               "lse": torch.empty(N, dtype=torch.float32, device=dev),
+               "mean": torch.empty(1, dtype=torch.float32, device=dev),
+               "n_bad": torch.empty(1, dtype=torch.int32, device=dev)}
+    _check("vp_lmhead_ce_merge_stats", _load().vp_lmhead_ce_merge_stats(
+        _ptr(stats), _ptr(targets), N, V, T, ignore_index, _ptr(out["loss"]), _ptr(out["lse"]), _ptr(out.get("mean")),
+        _ptr(out.get("n_bad")), _stream(dev)))
+    return out
+
+
+def lmhead_ce_shard_bwd(X, W_t, targets, lse, V, T, t, ignore_index=IGNORE_INDEX, dloss=None, dmean=None,
+                        vocab_chunk=None, workspace=None, dX_t=None, dW_t=None):
+    """Shard t's backward: (dX_t, dW_t), both fp32.  dX_t is this shard's part of
+    dX (sum it over the T shards); dW_t is complete for the shard's rows."""
+    _need(X, "X")
+    _need(W_t, "W_t", X.dtype, X.device)
+    _need(targets, "targets", torch.int64, X.device)
+    _need(lse, "lse", torch.float32, X.device)
+    N, H = X.shape
+    Vt = W_t.shape[0]
+    dev = X.device
+    if dX_t is None:
+        dX_t = torch.empty((N, H), dtype=torch.float32, device=dev)
+    if dW_t is None:
+        dW_t = torch.empty((Vt, H), dtype=torch.float32, device=dev)
+    _need(dX_t, "dX_t", torch.float32, dev)
+    _need(dW_t, "dW_t", torch.float32, dev)
+    nb = workspace_size(N, H, V // T, 1, _dtype_code(X), 1, vocab_chunk or 0)
+    if nb == 0:
+        raise VpError("vp_lmhead_ce_workspace_size", 1)
+    ws = _workspace(nb, dev, workspace)
+    _check("vp_lmhead_ce_shard_bwd", _load().vp_lmhead_ce_shard_bwd(
+        _ptr(X), _ptr(W_t), _ptr(targets), _ptr(lse), _ptr(dloss), _ptr(dmean), N, H, V, T, t, ignore_index,
+        _dtype_code(X), _ptr(dX_t), _ptr(dW_t), _ptr(ws), ws.numel() * ws.element_size(), _stream(dev)))
+    return dX_t, dW_t
+
+
+def vocab_parallel_lmhead_ce(X, W_t, targets, V, T, rank, group=None, ignore_index=IGNORE_INDEX, dmean=None):
+    """One rank's step of the T-rank form ("Vocab Parallelism" sec. 5.3; the
+    interview note's figure 2): the shard's statistics, one all-gather of them
+    ([T, 3, N], rank order), the merge (every rank gets the same loss and lse),
+    the shard's backward, and an all-reduce (SUM) of the fp32 dX parts.
+    Returns (forward dict, dX fp32 [N, H], dW_t fp32 [V/T, H]).  The two
+    collectives go through torch.distributed on `group`; everything else is
+    libvp's kernels on this rank's device."""
+    import torch.distributed as dist
+    stats = lmhead_ce_shard_fwd(X, W_t, targets, V, T, rank, ignore_index)
+    parts = [torch.empty_like(stats) for _ in range(T)]
+    dist.all_gather(parts, stats, group=group)
+    fwd = lmhead_ce_merge_stats(torch.stack(parts), targets, V, T, ignore_index)
+    dX, dW_t = lmhead_ce_shard_bwd(X, W_t, targets, fwd["lse"], V, T, rank, ignore_index, dmean=dmean)
+    dist.all_reduce(dX, group=group)
+    return fwd, dX, dW_t
+
+
 def read_device_status(workspace: torch.Tensor) -> int:
     """Synchronise the current stream and return the workspace's device status
     word (0 = no kernel gave up waiting)."""
@@ -336,9 +433,17 @@ def test_gemm_bf16(A, B, a_mn_major=False, b_mn_major=False):
     return D, ws
 
 
-def set_gemm_variant(pair: bool) -> None:
-    """Run the tcgen05 GEMMs on SM pairs (True) or one SM per tile (False, default)."""
-    _check("vp_test_set_gemm_variant", _load().vp_test_set_gemm_variant(int(bool(pair))))
+def set_gemm_variant(variant) -> None:
+    """tcgen05 GEMM form: 0 / False (default) one SM per tile, dX in 256 x 256
+    tiles; 1 / True SM pairs; 2 one SM per 128 x 256 tile everywhere."""
+    _check("vp_test_set_gemm_variant", _load().vp_test_set_gemm_variant(int(variant)))
+
+
+def set_wait_fault(mode: int, wait_ns: int = 0) -> None:
+    """Diagnostic of the bounded waits in the tcgen05 GEMMs: mode 1 holds the
+    TMA producer back, mode 2 the MMA issuer, 0 restores normal operation;
+    wait_ns limits every wait (0: the default 1 s)."""
+    _check("vp_test_set_wait_fault", _load().vp_test_set_wait_fault(int(mode), int(wait_ns)))
 
 
 def stage_timing_enable(max_launches: int) -> None:

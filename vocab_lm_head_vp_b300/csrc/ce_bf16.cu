@@ -2,7 +2,9 @@
 // the three epilogues that ride on the tcgen05 GEMM core and their launchers.
 //
 //   EpiLseStats  forward: per token row and per shard segment of a 256-wide
-//                vocab tile, the local max m and sum exp(z - m), plus the
+//                vocab tile, the local max m and R = sum exp(z - m) over the
+//                segment's logits except one maximal one (S = 1 + R, kept
+//                apart from the 1 so that a tiny R survives), plus the
 //                target logit when the tile owns the target ("Vocab
 //                Parallelism" sec. 5.3.1; interview note figure 2).
 //   EpiLseStatsP the same statistics, plus the tile's probabilities relative
@@ -63,17 +65,19 @@ template <bool kStoreP>
 struct EpiLseStatsT {
   static constexpr uint32_t kStagingBytes = kStoreP ? kStoreStagingBytes : 0;
   struct Params {
-    float2* partial;          // [num_vtiles * maxseg][N] (m, S)
+    float2* partial;          // [num_vtiles * maxseg][N] (m, R), R = S - 1
     float* zy;                // [N] target logit, written by the owning tile
     const int64_t* targets;   // [N]
     int64_t N, V, Vs;         // tokens, vocab, shard width V/T
     int maxseg;               // record slots per vocab tile
     float* tmax;              // [num_vtiles][N] row maximum of each tile (kStoreP)
+    int64_t y_off;            // vocab id of W's first row (targets are ids of the whole vocabulary)
   };
   // A tile of 256 valid columns inside one shard (all but the tiles holding a
   // shard edge or the vocabulary's end): one pass for the row maximum m over
-  // the tile, then one exp per logit, e = exp(z - m), summed into the tile's
-  // single (m, S) record and, with kStoreP, stored as p = e in fp16.
+  // the tile, then one exp per logit, e = exp(z - m), stored as p = e in fp16
+  // with kStoreP and summed into the tile's single (m, R) record.  Logits
+  // equal to m are counted instead of summed: R = (sum over z < m) + (ties - 1).
   __device__ static void run_whole(const Params& p, const CUtensorMap* tm, uint32_t taddr, int64_t n, int nb,
                                    int64_t v0, int64_t yl, bool row_ok, EpiCtx& ctx) {
     float mx = -INFINITY, zyv = 0.f;
@@ -100,6 +104,7 @@ struct EpiLseStatsT {
     const float nt = -mx * kLog2e;
     const bool warp_live = ctx.row0 < p.N;
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int ties = 0;
 #pragma unroll 1
     for (int b = 0; b < kBN / 64; ++b) {
       uint32_t w[kStoreP ? 32 : 1];
@@ -115,10 +120,13 @@ struct EpiLseStatsT {
           const float e1 = ex2_approx(fmaf(as_f(r[q + 1]), kLog2e, nt));
           const float e2 = ex2_approx(fmaf(as_f(r[q + 2]), kLog2e, nt));
           const float e3 = ex2_approx(fmaf(as_f(r[q + 3]), kLog2e, nt));
-          a0 += e0;
-          a1 += e1;
-          a2 += e2;
-          a3 += e3;
+          const bool t0 = as_f(r[q + 0]) == mx, t1 = as_f(r[q + 1]) == mx;
+          const bool t2 = as_f(r[q + 2]) == mx, t3 = as_f(r[q + 3]) == mx;
+          a0 += t0 ? 0.f : e0;
+          a1 += t1 ? 0.f : e1;
+          a2 += t2 ? 0.f : e2;
+          a3 += t3 ? 0.f : e3;
+          ties += (t0 + t1) + (t2 + t3);
           if constexpr (kStoreP) {
             w[h * 16 + q / 2] = pack_f16x2(e0, e1);
             w[h * 16 + q / 2 + 1] = pack_f16x2(e2, e3);
@@ -131,7 +139,9 @@ struct EpiLseStatsT {
       }
     }
     if (row_ok) {
-      p.partial[(static_cast<int64_t>(nb) * p.maxseg) * p.N + n] = make_float2(mx, (a0 + a1) + (a2 + a3));
+      // ties >= 1 (m is one of the logits); further ties are whole terms exp(0) = 1
+      p.partial[(static_cast<int64_t>(nb) * p.maxseg) * p.N + n] =
+          make_float2(mx, ((a0 + a1) + (a2 + a3)) + static_cast<float>(ties - 1));
       if (have_zy) p.zy[n] = zyv;
       if constexpr (kStoreP) p.tmax[static_cast<int64_t>(nb) * p.N + n] = mx;
     }
@@ -142,8 +152,7 @@ struct EpiLseStatsT {
     const int64_t v0 = static_cast<int64_t>(nb) * kBN;
     const int64_t vend = min(v0 + kBN, p.V);
     const bool row_ok = n < p.N;
-    const int64_t y = row_ok ? p.targets[n] : -1;
-    const int64_t yl = y - v0;
+    const int64_t yl = row_ok ? p.targets[n] - p.y_off - v0 : -1;
     int64_t t = v0 / p.Vs;
     int64_t seg_end = min((t + 1) * p.Vs, vend);
     if (vend - v0 == kBN && seg_end == vend) {
@@ -176,20 +185,28 @@ struct EpiLseStatsT {
 #pragma unroll
         for (int q = 1; q < 32; ++q) cm = fmaxf(cm, as_f(r[q]));
         if (kStoreP) tmx = fmaxf(tmx, cm);
+        // a new maximum turns the old one into an ordinary term, and one of
+        // this chunk's logits equal to it is the segment's excluded maximum
+        int skip = 0;
         if (cm > m) {
-          s *= ex2_approx((m - cm) * kLog2e);
+          s = (s + 1.f) * ex2_approx((m - cm) * kLog2e);
           m = cm;
+          skip = 1;
         }
         const float mL = m * kLog2e;
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        int ties = 0;
 #pragma unroll
         for (int q = 0; q < 32; q += 4) {
-          a0 += ex2_approx(fmaf(as_f(r[q + 0]), kLog2e, -mL));
-          a1 += ex2_approx(fmaf(as_f(r[q + 1]), kLog2e, -mL));
-          a2 += ex2_approx(fmaf(as_f(r[q + 2]), kLog2e, -mL));
-          a3 += ex2_approx(fmaf(as_f(r[q + 3]), kLog2e, -mL));
+          const bool t0 = as_f(r[q + 0]) == m, t1 = as_f(r[q + 1]) == m;
+          const bool t2 = as_f(r[q + 2]) == m, t3 = as_f(r[q + 3]) == m;
+          a0 += t0 ? 0.f : ex2_approx(fmaf(as_f(r[q + 0]), kLog2e, -mL));
+          a1 += t1 ? 0.f : ex2_approx(fmaf(as_f(r[q + 1]), kLog2e, -mL));
+          a2 += t2 ? 0.f : ex2_approx(fmaf(as_f(r[q + 2]), kLog2e, -mL));
+          a3 += t3 ? 0.f : ex2_approx(fmaf(as_f(r[q + 3]), kLog2e, -mL));
+          ties += (t0 + t1) + (t2 + t3);
         }
-        s += (a0 + a1) + (a2 + a3);
+        s += ((a0 + a1) + (a2 + a3)) + static_cast<float>(ties - skip);
       } else {
         // a shard edge or the vocab end falls inside this chunk
 #pragma unroll
@@ -207,10 +224,10 @@ struct EpiLseStatsT {
           const float z = as_f(r[q]);
           if (kStoreP) tmx = fmaxf(tmx, z);
           if (z > m) {
-            s = s * ex2_approx((m - z) * kLog2e) + 1.f;
+            s = (s + 1.f) * ex2_approx((m - z) * kLog2e);   // the old maximum joins the sum
             m = z;
           } else {
-            s += ex2_approx((z - m) * kLog2e);
+            s += ex2_approx((z - m) * kLog2e);   // a tie adds exp(0) = 1
           }
         }
       }
@@ -258,7 +275,7 @@ struct EpiDZ {
     const float* g;           // [N] upstream scale (0 for ignored rows)
     const int64_t* targets;   // [N]
     int64_t N;
-    int64_t c0, Vc;           // chunk start (global vocab id) and width
+    int64_t c0, Vc;           // chunk start (vocab id of the chunk's first column) and width
   };
   __device__ static void run(const Params& p, const CUtensorMap* tm, uint32_t taddr, int64_t n, int nb,
                              EpiCtx& ctx) {
@@ -425,21 +442,31 @@ cudaError_t ensure_smem(Kern kern, size_t smem, std::atomic<int>* done) {
   return e;
 }
 
-template <bool A_MN, bool B_MN, class Epi>
+// Diagnostic of the bounded waits (vp_test_set_wait_fault): a role of every
+// later one-SM GEMM launch that issues nothing, and the waits' time limit.
+int g_hold = kHoldNone;
+uint64_t g_wait_ns = kWaitTimeoutNs;
+
+// kMB 128-row blocks per CTA tile (1: 128 x 256 tiles, 2: 256 x 256 tiles);
+// group_m_rows: output rows per tile group.
+template <bool A_MN, bool B_MN, class Epi, int kMB = 1>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, int64_t M,
                         int64_t Ncols, int64_t K, const typename Epi::Params& ep, uint32_t* status,
-                        cudaStream_t stream, int group_m) {
-  auto kern = umma_gemm_kernel<A_MN, B_MN, Epi>;
-  constexpr size_t smem = kGemmSmemBytes + Epi::kStagingBytes;
+                        cudaStream_t stream, int group_m_rows) {
+  auto kern = umma_gemm_kernel<A_MN, B_MN, Epi, kMB>;
+  constexpr size_t smem = GemmShape<kMB>::kSmem + Epi::kStagingBytes;
   static std::atomic<int> attr_done[kMaxDevices];
   const cudaError_t e = ensure_smem(kern, smem, attr_done);
   if (e != cudaSuccess) return e;
   GemmArgs a;
-  a.sched.num_m = static_cast<int>((M + kBM - 1) / kBM);
+  a.sched.num_m = static_cast<int>((M + kMB * kBM - 1) / (kMB * kBM));
   a.sched.num_n = static_cast<int>((Ncols + kBN - 1) / kBN);
+  const int group_m = group_m_rows / (kMB * kBM);
   a.sched.group_m = group_m < 1 ? 1 : group_m;
   a.num_k = static_cast<int>((K + kBK - 1) / kBK);
   a.status = status;
+  a.wait_ns = g_wait_ns;
+  a.hold = g_hold;
   const int total = a.sched.num_m * a.sched.num_n;
   const int grid = total < sm_count() ? total : sm_count();
   kern<<<grid, kGemmThreads, smem, stream>>>(ta, tb, tc, a, ep);
@@ -485,29 +512,44 @@ cudaError_t launch_gemm_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const 
   a.sched.group_m = group_m < 1 ? 1 : group_m;
   a.num_k = static_cast<int>((K + kBK - 1) / kBK);
   a.status = status;
+  a.wait_ns = g_wait_ns;
+  a.hold = kHoldNone;   // the hold diagnostic covers the one-SM form only
   const int total = a.sched.num_m * a.sched.num_n;
   const int pairs = total < max_pairs ? total : max_pairs;
   cfg.gridDim = dim3(2 * pairs);
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, a, ep);
 }
 
-bool g_pair_kernels = false;  // one SM per tile by default (faster under the power cap); vp_test_set_gemm_variant switches
+// GEMM form (vp_test_set_gemm_variant): 0 (default) one SM per tile, the dX
+// contraction in 256 x 256 tiles; 1 SM pairs (cta_group::2, 256 x 256 tiles);
+// 2 one SM per 128 x 256 tile everywhere.
+int g_variant = 0;
+bool pair_kernels() { return g_variant == 1; }
 
 // B operand K-major box rows: 256 for one SM, 128 (its half) for a CTA pair.
-int kmajor_b_box_rows() { return g_pair_kernels ? 128 : kBN; }
+int kmajor_b_box_rows() { return pair_kernels() ? 128 : kBN; }
 
-template <bool A_MN, bool B_MN, class Epi>
+template <bool A_MN, bool B_MN, class Epi, int kMB = 1>
 cudaError_t launch_any(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, int64_t M,
                        int64_t Ncols, int64_t K, const typename Epi::Params& ep, uint32_t* status,
                        cudaStream_t stream, int group_m_rows) {
-  if (g_pair_kernels)
+  if (pair_kernels())
     return launch_gemm_2sm<A_MN, B_MN, Epi>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows / kPairBM);
-  return launch_gemm<A_MN, B_MN, Epi>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows / kBM);
+  if (kMB == 2 && g_variant == 2)
+    return launch_gemm<A_MN, B_MN, Epi, 1>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows);
+  return launch_gemm<A_MN, B_MN, Epi, kMB>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows);
 }
 
 }  // namespace
 
-void set_gemm_variant(int pair) { g_pair_kernels = pair != 0; }
+void set_gemm_variant(int variant) { g_variant = (variant == 1 || variant == 2) ? variant : 0; }
+
+int gemm_sm_count() { return sm_count(); }
+
+void set_wait_fault(int hold, uint64_t wait_ns) {
+  g_hold = (hold == kHoldProducer || hold == kHoldMma) ? hold : kHoldNone;
+  g_wait_ns = wait_ns > 0 ? wait_ns : kWaitTimeoutNs;
+}
 
 int lse_maxseg(int64_t V, int64_t Vs, int T) {
   // shard segments one 256-wide tile can touch: at most floor(255 / Vs) + 2, and at most T
@@ -521,11 +563,11 @@ int64_t lse_num_vtiles(int64_t V) { return (V + kBN - 1) / kBN; }
 
 cudaError_t bf16_lse_stats(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H,
                            int64_t V, int64_t Vs, float2* partial, int maxseg, float* zy, uint32_t* status,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, int64_t y_off) {
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, X, N, H, H, kBK, kBM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, W, V, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
-  EpiLseStats::Params p{partial, zy, targets, N, V, Vs, maxseg, nullptr};
+  EpiLseStats::Params p{partial, zy, targets, N, V, Vs, maxseg, nullptr, y_off};
   return launch_any<false, false, EpiLseStats>(ta, tb, ta, N, V, H, p, status, stream, VP_GROUP_ROWS_LOGITS);
 }
 
@@ -537,19 +579,19 @@ cudaError_t bf16_lse_stats_p(const void* X, const void* W, const int64_t* target
   if (!make_tmap_bf16(&tb, W, V, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
   // fp16 boxes of 32 rows x 64 columns (128 bytes), clipped at V columns and N rows
   if (!make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, P, N, V, ldp, 64, 32)) return cudaErrorInvalidValue;
-  EpiLseStatsP::Params p{partial, zy, targets, N, V, Vs, maxseg, tmax};
+  EpiLseStatsP::Params p{partial, zy, targets, N, V, Vs, maxseg, tmax, 0};
   return launch_any<false, false, EpiLseStatsP>(ta, tb, tc, N, V, H, p, status, stream, VP_GROUP_ROWS_LOGITS);
 }
 
 cudaError_t bf16_dz_chunk(const void* X, const void* W, const int64_t* targets, const float* lse, const float* g,
                           int64_t N, int64_t H, int64_t c0, int64_t Vc, void* dz, int64_t ldz, uint32_t* status,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, int64_t y_off) {
   CUtensorMap ta, tb, tc;
   const uint8_t* Wc = static_cast<const uint8_t*>(W) + c0 * H * 2;
   if (!make_tmap_bf16(&ta, X, N, H, H, kBK, kBM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, Wc, Vc, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
   if (!make_store_tmap(&tc, true, dz, N, Vc, ldz)) return cudaErrorInvalidValue;
-  EpiDZ::Params p{lse, g, targets, N, c0, Vc};
+  EpiDZ::Params p{lse, g, targets, N, y_off + c0, Vc};
   return launch_any<false, false, EpiDZ>(ta, tb, tc, N, Vc, H, p, status, stream, VP_GROUP_ROWS_LOGITS);
 }
 
@@ -564,7 +606,9 @@ cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N,
   if (!make_tmap_bf16(&tb, Wc, Vc, H, H, 64, kBK)) return cudaErrorInvalidValue;
   if (!make_store_tmap(&tc, mode >= kStoreBf16AddPartial, out, N, H, H)) return cudaErrorInvalidValue;
   EpiStore::Params p{mode == kAddF32 ? static_cast<const float*>(out) : partial, H, N, H, mode};
-  return launch_any<false, true, EpiStore>(ta, tb, tc, N, H, Vc, p, status, stream, VP_GROUP_ROWS_DX);
+  // 256-row tiles: the K loop runs over the whole vocabulary chunk, so the
+  // accumulator overlap of 128-row tiles matters little and W is streamed half as often
+  return launch_any<false, true, EpiStore, 2>(ta, tb, tc, N, H, Vc, p, status, stream, VP_GROUP_ROWS_DX);
 }
 
 cudaError_t bf16_dw_chunk(const void* dz, int64_t ldz, const void* X, int64_t N, int64_t H, int64_t c0,

@@ -2,7 +2,7 @@
 // FMAs.  fp32 inputs are held to a 1e-5 relative loss tolerance, which TF32
 // tensor cores cannot meet, so these kernels use plain fp32 arithmetic and
 // the accurate expf/logf.  Same structure as the bf16 path: 64 x 64 logit
-// tiles reduced to per-shard-segment (m, S) records (forward) or to dZ
+// tiles reduced to per-shard-segment (m, R) records (forward) or to dZ
 // (backward), then plain GEMMs for dX and dW.
 #include <cuda_runtime.h>
 
@@ -56,11 +56,13 @@ __device__ __forceinline__ void tile_mma(const float* __restrict__ A, int64_t sa
   }
 }
 
-// Forward: Z tile = X[n0:n0+64] W[v0:v0+64]^T -> per-row shard-segment records.
+// Forward: Z tile = X[n0:n0+64] W[v0:v0+64]^T -> per-row shard-segment records
+// (m, R): the segment's maximum and the sum of exp(z - m) over its logits
+// except one maximal one (S = 1 + R).
 __global__ void __launch_bounds__(kThr) f32_lse_kernel(const float* __restrict__ X, const float* __restrict__ W,
                                                        const int64_t* __restrict__ targets, int64_t N, int64_t H,
                                                        int64_t V, int64_t Vs, float2* __restrict__ partial,
-                                                       int maxseg, float* __restrict__ zy) {
+                                                       int maxseg, float* __restrict__ zy, int64_t y_off) {
   __shared__ float As[kK][kT + 4];
   __shared__ float Bs[kK][kT + 4];
   __shared__ float Zs[kT][kT + 1];
@@ -97,12 +99,12 @@ __global__ void __launch_bounds__(kThr) f32_lse_kernel(const float* __restrict__
     }
     const float z = Zs[r][col - v0];
     if (z > m) {
-      s = s * expf(m - z) + 1.f;
+      s = (s + 1.f) * expf(m - z);   // the old maximum joins the sum (expf(-inf) = 0 at the start)
       m = z;
     } else {
-      s += expf(z - m);
+      s += expf(z - m);              // a tie adds exp(0) = 1
     }
-    if (col == y) zy[n] = z;
+    if (col + y_off == y) zy[n] = z;
   }
   rec[static_cast<int64_t>(k) * N] = make_float2(m, s);
 }
@@ -112,7 +114,7 @@ __global__ void __launch_bounds__(kThr) f32_dz_kernel(const float* __restrict__ 
                                                       const int64_t* __restrict__ targets,
                                                       const float* __restrict__ lse, const float* __restrict__ g,
                                                       int64_t N, int64_t H, int64_t c0, int64_t Vc,
-                                                      float* __restrict__ dz, int64_t ldz) {
+                                                      float* __restrict__ dz, int64_t ldz, int64_t y_off) {
   __shared__ float As[kK][kT + 4];
   __shared__ float Bs[kK][kT + 4];
   const int64_t n0 = static_cast<int64_t>(blockIdx.y) * kT;
@@ -125,7 +127,7 @@ __global__ void __launch_bounds__(kThr) f32_dz_kernel(const float* __restrict__ 
     const int64_t n = n0 + ty * 4 + i;
     if (n >= N) continue;
     const float gn = g[n], ln = lse[n];
-    const int64_t yl = targets[n] - c0;
+    const int64_t yl = targets[n] - y_off - c0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int64_t c = v0 + tx * 4 + j;
@@ -176,14 +178,15 @@ int f32_maxseg(int64_t V, int64_t Vs, int T) {
 }
 
 cudaError_t f32_lse_stats(const float* X, const float* W, const int64_t* targets, int64_t N, int64_t H, int64_t V,
-                          int64_t Vs, float2* partial, int maxseg, float* zy, cudaStream_t stream) {
-  f32_lse_kernel<<<tiles(N, V), kThr, 0, stream>>>(X, W, targets, N, H, V, Vs, partial, maxseg, zy);
+                          int64_t Vs, float2* partial, int maxseg, float* zy, cudaStream_t stream, int64_t y_off) {
+  f32_lse_kernel<<<tiles(N, V), kThr, 0, stream>>>(X, W, targets, N, H, V, Vs, partial, maxseg, zy, y_off);
   return cudaGetLastError();
 }
 
 cudaError_t f32_dz_chunk(const float* X, const float* W, const int64_t* targets, const float* lse, const float* g,
-                         int64_t N, int64_t H, int64_t c0, int64_t Vc, float* dz, int64_t ldz, cudaStream_t stream) {
-  f32_dz_kernel<<<tiles(N, Vc), kThr, 0, stream>>>(X, W, targets, lse, g, N, H, c0, Vc, dz, ldz);
+                         int64_t N, int64_t H, int64_t c0, int64_t Vc, float* dz, int64_t ldz, cudaStream_t stream,
+                         int64_t y_off) {
+  f32_dz_kernel<<<tiles(N, Vc), kThr, 0, stream>>>(X, W, targets, lse, g, N, H, c0, Vc, dz, ldz, y_off);
   return cudaGetLastError();
 }
 

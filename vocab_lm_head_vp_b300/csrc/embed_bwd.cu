@@ -12,11 +12,13 @@
 //
 // Deterministic, no atomics:
 //   1. keys (id << 32 | n) for valid ids, all-ones for the rest and the
-//      padding, sorted: blocks bitonic-sort 512-key chunks in shared memory,
-//      then groups of up to 8 sorted runs merge in one pass each, every key
-//      placing itself at its rank (binary searches in the other runs of its
-//      group; the keys are distinct, the all-ones ones tie-broken by run).
-//      The sorted order groups tokens by id, by n within.
+//      padding, sorted: blocks build and bitonic-sort 512-key chunks in shared
+//      memory; then every key places itself at its rank, the count of keys
+//      that precede it in every other chunk (binary searches; the keys are
+//      distinct, the all-ones ones tie-broken by chunk).  Up to 16384 keys this
+//      is one pass with all keys in each block's shared memory; beyond, groups
+//      of up to 8 sorted runs merge in one pass each, the searches in global
+//      memory.  The sorted order groups tokens by id, by n within.
 //   2. runs of kRun sorted positions: one thread per 16-byte column vector of
 //      the row walks the run in order and sums; a segment (one id) that starts
 //      and ends inside the run is added to dW at once, a segment cut by the
@@ -37,23 +39,19 @@ namespace {
 constexpr uint64_t kSentinel = ~0ull;
 constexpr uint32_t kNoId = 0xffffffffu;
 constexpr int kChunk = 512;           // keys sorted per block in shared memory
-constexpr int kMergeWays = 8;         // sorted runs merged per pass
+constexpr int kMergeWays = 8;         // sorted runs merged per pass (beyond kRankAllKeys)
+constexpr int kRankAllKeys = 16384;   // keys the one-pass rank placement holds in shared memory (128 KB)
+constexpr int kRankAllChunks = kRankAllKeys / kChunk;
 constexpr int kSortThreads = 256;
 constexpr int kRun = 32;              // sorted positions per run
 constexpr int kRedThreads = 256;
 
 __device__ __forceinline__ uint32_t key_id(uint64_t k) { return static_cast<uint32_t>(k >> 32); }
 
-__global__ void make_keys_kernel(const int64_t* __restrict__ ids, int64_t N, int64_t V, uint64_t* __restrict__ keys,
-                                 int64_t n_pad) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n_pad) return;
-  uint64_t k = kSentinel;
-  if (i < N) {
-    const int64_t id = ids[i];
-    if (id >= 0 && id < V) k = (static_cast<uint64_t>(id) << 32) | static_cast<uint64_t>(i);
-  }
-  keys[i] = k;
+__device__ __forceinline__ uint64_t make_key(const int64_t* __restrict__ ids, int64_t N, int64_t V, int64_t i) {
+  if (i >= N) return kSentinel;
+  const int64_t id = ids[i];
+  return (id >= 0 && id < V) ? (static_cast<uint64_t>(id) << 32) | static_cast<uint64_t>(i) : kSentinel;
 }
 
 // Compare-exchange step j of merge size k on `len` keys in shared memory.
@@ -73,16 +71,56 @@ __device__ __forceinline__ void smem_step(uint64_t* s, int len, int k, int j) {
   __syncthreads();
 }
 
-// Bitonic sort of each chunk of len = min(kChunk, n_pad) keys into ascending
-// order (merge sizes 2..len), ready for the rank merges.
-__global__ void __launch_bounds__(kSortThreads) bitonic_chunk_sort(uint64_t* __restrict__ keys, int len) {
+// The keys of each chunk of len = min(kChunk, n_pad) positions, bitonic-sorted
+// into ascending order (merge sizes 2..len), ready for the rank placement.
+__global__ void __launch_bounds__(kSortThreads) keys_chunk_sort(const int64_t* __restrict__ ids, int64_t N,
+                                                                int64_t V, uint64_t* __restrict__ keys, int len) {
   __shared__ uint64_t s[kChunk];
   const int64_t gbase = static_cast<int64_t>(blockIdx.x) * len;
-  for (int i = threadIdx.x; i < len; i += blockDim.x) s[i] = keys[gbase + i];
+  for (int i = threadIdx.x; i < len; i += blockDim.x) s[i] = make_key(ids, N, V, gbase + i);
   __syncthreads();
   for (int k = 2; k <= len; k <<= 1)
     for (int j = k >> 1; j > 0; j >>= 1) smem_step(s, len, k, j);
   for (int i = threadIdx.x; i < len; i += blockDim.x) keys[gbase + i] = s[i];
+}
+
+// All n_pad <= kRankAllKeys keys at once, sorted in chunks of kChunk: block c
+// holds every key in shared memory and places each key of chunk c at its
+// index in the chunk plus, for every other chunk, the keys there that precede
+// it (an earlier chunk's equal keys first).  The chunks' binary searches
+// advance in lockstep, one independent shared-memory load per chunk and round.
+__global__ void __launch_bounds__(kChunk) rank_all_kernel(const uint64_t* __restrict__ in,
+                                                          uint64_t* __restrict__ out, int n_pad) {
+  extern __shared__ uint64_t sk_all[];
+  for (int i = threadIdx.x; i < n_pad; i += blockDim.x) sk_all[i] = in[i];
+  __syncthreads();
+  const int chunks = n_pad / kChunk;
+  const int own = blockIdx.x;
+  const int i = own * kChunk + static_cast<int>(threadIdx.x);
+  const uint64_t key = sk_all[i];
+  int lo[kRankAllChunks], hi[kRankAllChunks];
+#pragma unroll
+  for (int c = 0; c < kRankAllChunks; ++c) {
+    lo[c] = 0;
+    hi[c] = (c < chunks && c != own) ? kChunk : 0;   // no search in the own chunk or past the last
+  }
+  for (int span = kChunk; span > 0; span >>= 1) {   // log2(kChunk) + 1 rounds finish every search
+#pragma unroll
+    for (int c = 0; c < kRankAllChunks; ++c) {
+      if (lo[c] < hi[c]) {
+        const int mid = (lo[c] + hi[c]) >> 1;
+        const uint64_t x = sk_all[c * kChunk + mid];
+        if (c < own ? x <= key : x < key)
+          lo[c] = mid + 1;
+        else
+          hi[c] = mid;
+      }
+    }
+  }
+  int pos = static_cast<int>(threadIdx.x);
+#pragma unroll
+  for (int c = 0; c < kRankAllChunks; ++c) pos += lo[c];
+  out[pos] = key;
 }
 
 // Merge each group of G consecutive sorted runs of L keys (G, L, n_pad powers
@@ -294,8 +332,10 @@ int64_t pad_pow2(int64_t n) {
 
 int embed_bwd_kernels(int64_t N) {
   const int64_t n_pad = pad_pow2(N);
-  int k = 4;   // keys, chunk sort, run sums, cross-run sums
-  for (int64_t L = n_pad < kChunk ? n_pad : kChunk; L < n_pad; L *= kMergeWays) ++k;   // merge passes
+  int k = 3;   // keys + chunk sort, run sums, cross-run sums
+  if (n_pad <= kChunk) return k;
+  if (n_pad <= kRankAllKeys) return k + 1;   // one rank placement
+  for (int64_t L = kChunk; L < n_pad; L *= kMergeWays) ++k;   // merge passes
   return k;
 }
 
@@ -315,10 +355,25 @@ cudaError_t embed_bwd(const int64_t* ids, const void* dOut, float* dW, int64_t N
   cudaError_t e = cudaSuccess;
   if (!accumulate) e = cudaMemsetAsync(dW, 0, size_t(V) * H * sizeof(float), stream);
   if (e != cudaSuccess) return e;
-  make_keys_kernel<<<static_cast<unsigned>((n_pad + 255) / 256), 256, 0, stream>>>(ids, N, V, keys, n_pad);
   const int len = static_cast<int>(n_pad < kChunk ? n_pad : kChunk);
-  bitonic_chunk_sort<<<static_cast<unsigned>(n_pad / len), kSortThreads, 0, stream>>>(keys, len);
-  for (int64_t L = len; L < n_pad;) {
+  keys_chunk_sort<<<static_cast<unsigned>(n_pad / len), kSortThreads, 0, stream>>>(ids, N, V, keys, len);
+  if (n_pad > kChunk && n_pad <= kRankAllKeys) {
+    const size_t smem = size_t(n_pad) * sizeof(uint64_t);
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    if (!attr_set[dev]) {
+      e = cudaFuncSetAttribute(rank_all_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kRankAllKeys * static_cast<int>(sizeof(uint64_t)));
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
+    rank_all_kernel<<<static_cast<unsigned>(n_pad / kChunk), kChunk, smem, stream>>>(keys, spare, static_cast<int>(n_pad));
+    uint64_t* t = keys;
+    keys = spare;
+    spare = t;
+  }
+  for (int64_t L = len; n_pad > kRankAllKeys && L < n_pad;) {
     const int G = static_cast<int>(n_pad / L < kMergeWays ? n_pad / L : kMergeWays);
     rank_merge_kernel<<<static_cast<unsigned>((n_pad + 255) / 256), 256, 0, stream>>>(keys, spare, n_pad, L, G);
     uint64_t* t = keys;

@@ -1,12 +1,22 @@
 // Per-token merge of the forward statistics and the small per-batch kernels.
 //
+// If a kernel earlier on the stream gave up a wait (a non-zero device status
+// word), its records are incomplete: the merge then writes NaN to loss, lse
+// and the shard statistics, so the failure shows in the outputs themselves.
+//
 // lse_merge: the on-device form of the pages' cross-shard reductions ("Vocab
 // Parallelism" sec. 5.3.1; "Vocab parallelism: how to split embedding and LM
-// head", figure 2 and key formulas).  For token n, the per-tile records
-// (m, S) of shard t are merged into the shard's (m_t, S_t) (one thread per
-// token and shard); the shards then merge into m = max_t m_t,
-// S = sum_t S_t e^(m_t - m), lse = m + log S, and loss = lse - z_y for a
-// valid target, 0 otherwise (one thread per token, shards in order).
+// head", figure 2 and key formulas).  A record (m, R) stands for a set of
+// logits with maximum m and S = sum exp(z - m) = 1 + R: R sums every term
+// but one maximal one, so the 1 is never added to a small R in fp32.  For
+// token n, the per-tile records of shard t are merged into the shard's
+// (m_t, R_t) (one thread per token and shard); the shards then merge into
+// m = max_t m_t and R with S = 1 + R = sum_t S_t e^(m_t - m) (one thread per
+// token, shards in order), and
+//     loss = log1p(R) + (m - z_y)            (valid target; 0 otherwise),
+//     lse  = m + log1p(R),
+// the pages' l = log sum_j e^(z_j - m) - (z_y - m) as two non-negative
+// terms: no cancellation when the target is the row's maximum and l << lse.
 //
 // loss_mean_and_bad: L = sum_n loss_n / max(1, N_valid) (sec. 5.3.3) and the
 // count of targets that are neither ignore_index nor inside [0, V).
@@ -21,16 +31,19 @@
 namespace vp {
 namespace {
 
-__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
+// (m, r) <- the merge of (m, r) and (m2, r2): the smaller maximum's whole set,
+// 1 + r, is rescaled onto the larger one; the larger one's excluded term stays
+// excluded.
+__device__ __forceinline__ void merge_mr(float& m, float& r, float m2, float r2) {
   if (m2 > m) {
-    s = s * expf(m - m2) + s2;
+    r = r2 + (r + 1.f) * expf(m - m2);
     m = m2;
   } else {
-    s += s2 * expf(m2 - m);
+    r += (r2 + 1.f) * expf(m2 - m);
   }
 }
 
-// Slot of shard t's first tile: where the shard's merged (m_t, S_t) is left.
+// Slot of shard t's first tile: where the shard's merged (m_t, R_t) is left.
 __device__ __forceinline__ int64_t shard_slot(int t, int64_t Vs, int tile_v, int maxseg) {
   const int64_t nb = static_cast<int64_t>(t) * Vs / tile_v;
   const int k = t - static_cast<int>((nb * tile_v) / Vs);
@@ -38,7 +51,7 @@ __device__ __forceinline__ int64_t shard_slot(int t, int64_t Vs, int tile_v, int
 }
 
 // Step 1, one thread per (token, shard): the shard's tile records, in tile
-// order, into (m_t, S_t), written over the record of the shard's first tile
+// order, into (m_t, R_t), written over the record of the shard's first tile
 // (a record slot belongs to exactly one shard, so only this thread touches it).
 __global__ void shard_merge_kernel(float2* __restrict__ partial, int64_t N, int64_t Vs, int T, int tile_v,
                                    int maxseg) {
@@ -47,13 +60,16 @@ __global__ void shard_merge_kernel(float2* __restrict__ partial, int64_t N, int6
   for (int t = blockIdx.y; t < T; t += gridDim.y) {
     const int64_t a = static_cast<int64_t>(t) * Vs;
     const int64_t b = a + Vs;
-    float mt = -INFINITY, st = 0.f;
-    for (int64_t nb = a / tile_v; nb <= (b - 1) / tile_v; ++nb) {
+    const int64_t nb0 = a / tile_v;
+    // every record holds at least one logit: start from the shard's first one
+    const float2 r0 = partial[(nb0 * maxseg + (t - static_cast<int>((nb0 * tile_v) / Vs))) * N + n];
+    float mt = r0.x, rt = r0.y;
+    for (int64_t nb = nb0 + 1; nb <= (b - 1) / tile_v; ++nb) {
       const int k = t - static_cast<int>((nb * tile_v) / Vs);   // slot of shard t inside tile nb
       const float2 r = partial[(nb * maxseg + k) * N + n];
-      merge_ms(mt, st, r.x, r.y);
+      merge_mr(mt, rt, r.x, r.y);
     }
-    partial[shard_slot(t, Vs, tile_v, maxseg) * N + n] = make_float2(mt, st);
+    partial[shard_slot(t, Vs, tile_v, maxseg) * N + n] = make_float2(mt, rt);
   }
 }
 
@@ -61,26 +77,90 @@ __global__ void shard_merge_kernel(float2* __restrict__ partial, int64_t N, int6
 __global__ void lse_merge_kernel(const float2* __restrict__ partial, const float* __restrict__ zy,
                                  const int64_t* __restrict__ targets, int64_t N, int64_t V, int64_t Vs, int T,
                                  int tile_v, int maxseg, int64_t ignore_index, float* __restrict__ loss,
-                                 float* __restrict__ lse, float* __restrict__ shard_stats, int64_t ss_ld) {
+                                 float* __restrict__ lse, float* __restrict__ shard_stats, int64_t ss_ld,
+                                 const uint32_t* __restrict__ status) {
   const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (n >= N) return;
+  if (status && *status != 0u) {
+    const float nan = __int_as_float(0x7fc00000);
+    lse[n] = nan;
+    loss[n] = nan;
+    if (shard_stats)
+      for (int64_t q = 0; q < 3 * static_cast<int64_t>(T); ++q) shard_stats[q * ss_ld + n] = nan;
+    return;
+  }
   const int64_t y = targets[n];
   const bool valid = y >= 0 && y < V && y != ignore_index;
   const float zyn = valid ? zy[n] : 0.f;
-  float m = -INFINITY, s = 0.f;
+  float m = 0.f, r = 0.f;
   for (int t = 0; t < T; ++t) {
-    const float2 r = partial[shard_slot(t, Vs, tile_v, maxseg) * N + n];
+    const float2 rec = partial[shard_slot(t, Vs, tile_v, maxseg) * N + n];
     if (shard_stats) {
       const int64_t a = static_cast<int64_t>(t) * Vs;
-      shard_stats[(static_cast<int64_t>(t) * 3 + 0) * ss_ld + n] = r.x;
-      shard_stats[(static_cast<int64_t>(t) * 3 + 1) * ss_ld + n] = r.y;
+      shard_stats[(static_cast<int64_t>(t) * 3 + 0) * ss_ld + n] = rec.x;
+      shard_stats[(static_cast<int64_t>(t) * 3 + 1) * ss_ld + n] = 1.f + rec.y;   // S_t
       shard_stats[(static_cast<int64_t>(t) * 3 + 2) * ss_ld + n] = (valid && y >= a && y < a + Vs) ? zyn : 0.f;
     }
-    merge_ms(m, s, r.x, r.y);
+    if (t == 0) {
+      m = rec.x;
+      r = rec.y;
+    } else {
+      merge_mr(m, r, rec.x, rec.y);
+    }
   }
-  const float l = m + logf(s);
-  lse[n] = l;
-  loss[n] = valid ? l - zyn : 0.f;
+  const float l1 = log1pf(r);
+  lse[n] = m + l1;
+  // z_y is one of the logits, so m - z_y >= 0: both terms are non-negative
+  loss[n] = valid ? l1 + (m - zyn) : 0.f;
+}
+
+// One shard of a T-shard vocabulary computed by itself (a rank holding only
+// its W_t): its tile records in order into (m_t, R_t), and its target logit
+// z_y^(t) (0 when the target is ignored or in another shard).
+__global__ void shard_stats_kernel(const float2* __restrict__ partial, const float* __restrict__ zy,
+                                   const int64_t* __restrict__ targets, int64_t N, int64_t V, int64_t start,
+                                   int64_t Vs, int64_t ntiles, int64_t ignore_index, float* __restrict__ stats,
+                                   const uint32_t* __restrict__ status) {
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  if (status && *status != 0u) {
+    const float nan = __int_as_float(0x7fc00000);
+    stats[n] = nan;
+    stats[N + n] = nan;
+    stats[2 * N + n] = nan;
+    return;
+  }
+  const float2 r0 = partial[n];
+  float m = r0.x, r = r0.y;
+  for (int64_t nb = 1; nb < ntiles; ++nb) {
+    const float2 rec = partial[nb * N + n];
+    merge_mr(m, r, rec.x, rec.y);
+  }
+  const int64_t y = targets[n];
+  const bool own = y >= start && y < start + Vs && y < V && y != ignore_index;
+  stats[n] = m;
+  stats[N + n] = r;
+  stats[2 * N + n] = own ? zy[n] : 0.f;
+}
+
+// The merge of gathered shard statistics [T][3][N], shards in order: the
+// pages' MAX of m_t, SUM of the rescaled local sums and SUM of z_y^(t).
+__global__ void merge_shard_stats_kernel(const float* __restrict__ stats, const int64_t* __restrict__ targets,
+                                         int64_t N, int64_t V, int T, int64_t ignore_index, float* __restrict__ loss,
+                                         float* __restrict__ lse) {
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  float m = stats[n], r = stats[N + n], z = 0.f + stats[2 * N + n];
+  for (int t = 1; t < T; ++t) {
+    const float* st = stats + static_cast<int64_t>(t) * 3 * N;
+    merge_mr(m, r, st[n], st[N + n]);
+    z += st[2 * N + n];
+  }
+  const int64_t y = targets[n];
+  const bool valid = y >= 0 && y < V && y != ignore_index;
+  const float l1 = log1pf(r);
+  lse[n] = m + l1;
+  loss[n] = valid ? l1 + (m - z) : 0.f;
 }
 
 constexpr int kRedThreads = 1024;
@@ -152,22 +232,39 @@ __global__ void __launch_bounds__(kRedThreads) upstream_scale_kernel(const int64
 
 cudaError_t lse_merge_ld(float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
                          int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
-                         float* shard_stats, int64_t ss_ld, cudaStream_t stream) {
+                         float* shard_stats, int64_t ss_ld, const uint32_t* status, cudaStream_t stream) {
   const int threads = 256;
   const int64_t blocks = (N + threads - 1) / threads;
   const dim3 grid1(static_cast<unsigned>(blocks), static_cast<unsigned>(T < 65535 ? T : 65535));
   // the records are scratch of this call: step 1 leaves each shard's merge in one of them
   shard_merge_kernel<<<grid1, threads, 0, stream>>>(partial, N, Vs, T, tile_v, maxseg);
   lse_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      partial, zy, targets, N, V, Vs, T, tile_v, maxseg, ignore_index, loss, lse, shard_stats, ss_ld);
+      partial, zy, targets, N, V, Vs, T, tile_v, maxseg, ignore_index, loss, lse, shard_stats, ss_ld, status);
   return cudaGetLastError();
 }
 
 cudaError_t lse_merge(float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
                       int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
-                      float* shard_stats, cudaStream_t stream) {
+                      float* shard_stats, const uint32_t* status, cudaStream_t stream) {
   return lse_merge_ld(partial, zy, targets, N, V, Vs, T, tile_v, maxseg, ignore_index, loss, lse, shard_stats, N,
-                      stream);
+                      status, stream);
+}
+
+cudaError_t shard_stats(const float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
+                        int64_t start, int64_t Vs, int64_t ntiles, int64_t ignore_index, float* stats,
+                        const uint32_t* status, cudaStream_t stream) {
+  const int threads = 256;
+  shard_stats_kernel<<<static_cast<unsigned>((N + threads - 1) / threads), threads, 0, stream>>>(
+      partial, zy, targets, N, V, start, Vs, ntiles, ignore_index, stats, status);
+  return cudaGetLastError();
+}
+
+cudaError_t merge_shard_stats(const float* stats, const int64_t* targets, int64_t N, int64_t V, int T,
+                              int64_t ignore_index, float* loss, float* lse, cudaStream_t stream) {
+  const int threads = 256;
+  merge_shard_stats_kernel<<<static_cast<unsigned>((N + threads - 1) / threads), threads, 0, stream>>>(
+      stats, targets, N, V, T, ignore_index, loss, lse);
+  return cudaGetLastError();
 }
 
 cudaError_t loss_mean_and_bad(const float* loss, const int64_t* targets, int64_t N, int64_t V, int64_t ignore_index,

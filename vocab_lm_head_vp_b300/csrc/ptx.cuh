@@ -48,8 +48,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase of `bar` with the given parity to complete.  Returns
-// false if `*abort` becomes non-zero or the time limit passes first.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+// false if `*abort` becomes non-zero or `limit_ns` passes first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
   const uint32_t a = smem_addr(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -57,7 +58,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     if (mbar_try_wait(a, parity)) return true;
     if ((i & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
 }
@@ -218,7 +219,8 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 // mbar_wait for a barrier that peer CTAs arrive on (cluster-scope acquire).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                                  uint64_t limit_ns = kWaitTimeoutNs) {
   const uint32_t a = smem_addr(bar);
   if (mbar_try_wait_cluster(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -226,7 +228,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     if (mbar_try_wait_cluster(a, parity)) return true;
     if ((i & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
 }

@@ -12,6 +12,14 @@
 // Two 128x256 fp32 accumulators (2 x 256 TMEM columns) let the epilogue of
 // tile i overlap the MMAs of tile i+1.
 //
+// kMB = 2 makes each CTA tile 256 x 256: two 128-row A blocks per stage share
+// the stage's B block (two MMAs per 16-deep K step, one per accumulator), so
+// the CTAs running at one time cover twice the output rows per pass over B
+// and B is streamed from L2 / DRAM half as often.  Both 256-column
+// accumulators then belong to one tile (no overlap of epilogue and MMAs: for
+// long K loops, such as dX's over the vocabulary, it does not matter) and the
+// ring has 3 stages of 64 KB instead of 4 of 48 KB.
+//
 // Operand layouts (A is M x K, B is N x K; "MN-major" = M (or N) contiguous):
 //   K-major : one TMA box {64 K, rows} per stage; swizzle atoms of 8 rows x
 //             128 B stacked along the rows (stride 1024 B); the k-th 16-wide
@@ -38,6 +46,19 @@ constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr uint32_t kMnBoxBytes = 64 * kBK * 2;  // one {64 MN, 64 K} box: 8 KB
 constexpr size_t kGemmSmemBytes = 1024 + kStages * kStageBytes + 256;
+
+// Pipeline shape of a kernel whose CTA tile is kMB 128-row blocks by 256 columns.
+template <int kMB>
+struct GemmShape {
+  static_assert(kMB == 1 || kMB == 2, "one or two 128-row blocks per CTA tile");
+  static constexpr int kStg = kMB == 1 ? kStages : 3;    // ring stages
+  static constexpr int kAcc = kMB == 1 ? 2 : 1;          // accumulator sets (2 x 256 TMEM columns in all)
+  static constexpr uint32_t kAStage = kMB * kABytes;
+  static constexpr uint32_t kStage = kAStage + kBBytes;
+  static constexpr size_t kSmem = 1024 + kStg * kStage + 256;
+};
+static_assert(GemmShape<1>::kSmem == kGemmSmemBytes && GemmShape<2>::kSmem <= kGemmSmemBytes,
+              "both tile shapes fit the same shared-memory budget");
 // Epilogues that store through TMA stage one 32-row x 128-byte box per warp,
 // double-buffered: 4 warps x 2 x 4 KB.
 constexpr uint32_t kStoreBoxBytes = 32 * 128;
@@ -86,10 +107,16 @@ struct TileSched {
   }
 };
 
+// Roles that may be told to issue nothing (a diagnostic of the bounded
+// waits: the other roles' waits then run out and the CTA takes its abort path).
+enum GemmHold : int { kHoldNone = 0, kHoldProducer = 1, kHoldMma = 2 };
+
 struct GemmArgs {
   TileSched sched;
   int num_k;           // number of 64-wide K blocks
   uint32_t* status;    // device status word (VP_DEV_* bits)
+  uint64_t wait_ns;    // limit of every mbarrier wait
+  int hold;            // GemmHold (kHoldNone outside diagnostics)
 };
 
 __device__ __forceinline__ void record_failure(uint32_t* status, volatile int* abort, uint32_t bit) {
@@ -97,22 +124,23 @@ __device__ __forceinline__ void record_failure(uint32_t* status, volatile int* a
   if (status) atomicOr(status, bit);
 }
 
-template <bool A_MN, bool B_MN, class Epi>
+template <bool A_MN, bool B_MN, class Epi, int kMB = 1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const GemmArgs args, const typename Epi::Params ep) {
+  using S = GemmShape<kMB>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  uint8_t* sA = smem;                         // kStages x 16 KB
-  uint8_t* sB = smem + kStages * kABytes;     // kStages x 32 KB
-  uint8_t* sC = smem + kStages * kStageBytes; // Epi::kStagingBytes (0 or 32 KB)
+  uint8_t* sA = smem;                           // kStg x kMB x 16 KB
+  uint8_t* sB = smem + S::kStg * S::kAStage;    // kStg x 32 KB
+  uint8_t* sC = smem + S::kStg * S::kStage;     // Epi::kStagingBytes (0 or 32 KB)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sC + Epi::kStagingBytes);
-  uint64_t* full = bars;                      // TMA -> MMA
-  uint64_t* empty = bars + kStages;           // MMA -> TMA
-  uint64_t* tfull = bars + 2 * kStages;       // MMA -> epilogue (2 accumulators)
-  uint64_t* tempty = tfull + 2;               // epilogue -> MMA
-  uint64_t* drain = tempty + 2;               // MMA completion at exit
+  uint64_t* full = bars;                        // TMA -> MMA
+  uint64_t* empty = bars + S::kStg;             // MMA -> TMA
+  uint64_t* tfull = bars + 2 * S::kStg;         // MMA -> epilogue (kAcc accumulator sets)
+  uint64_t* tempty = tfull + S::kAcc;           // epilogue -> MMA
+  uint64_t* drain = tempty + S::kAcc;           // MMA completion at exit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   __shared__ int never_abort;
@@ -121,11 +149,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S::kStg; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < S::kAcc; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4 * 32);
     }
@@ -153,27 +181,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;   // bit s: stage s has a load in flight / its parity
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const int first_tile = args.hold == kHoldProducer ? total : static_cast<int>(blockIdx.x);
+      for (int tile = first_tile; tile < total; tile += gridDim.x) {
         int mb, nb;
         args.sched.tile(tile, mb, nb);
         bool ok = true;
         for (int kb = 0; kb < args.num_k; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort, args.wait_ns)) {
             record_failure(args.status, abort, 0x1u);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          mbar_arrive_expect_tx(&full[stage], S::kStage);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          uint8_t* a = sA + stage * kABytes;
+          uint8_t* a = sA + stage * S::kAStage;
           uint8_t* b = sB + stage * kBBytes;
           const int k0 = kb * kBK;
-          if (!A_MN) {
-            tma_load_2d(a, &tmA, &full[stage], k0, mb * kBM);
-          } else {
-            tma_load_2d(a, &tmA, &full[stage], mb * kBM, k0);
-            tma_load_2d(a + kMnBoxBytes, &tmA, &full[stage], mb * kBM + 64, k0);
+#pragma unroll
+          for (int h = 0; h < kMB; ++h) {
+            const int m0 = (mb * kMB + h) * kBM;
+            if (!A_MN) {
+              tma_load_2d(a + h * kABytes, &tmA, &full[stage], k0, m0);
+            } else {
+              tma_load_2d(a + h * kABytes, &tmA, &full[stage], m0, k0);
+              tma_load_2d(a + h * kABytes + kMnBoxBytes, &tmA, &full[stage], m0 + 64, k0);
+            }
           }
           if (!B_MN) {
             tma_load_2d(b, &tmB, &full[stage], k0, nb * kBN);
@@ -182,7 +215,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int i = 0; i < kBN / 64; ++i)
               tma_load_2d(b + i * kMnBoxBytes, &tmB, &full[stage], nb * kBN + 64 * i, k0);
           }
-          if (++stage == kStages) {
+          if (++stage == S::kStg) {
             stage = 0;
             phase ^= 1u;
           }
@@ -190,8 +223,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!ok) break;
       }
       // Every load this thread issued must land before the CTA can exit.
-      for (int s = 0; s < kStages; ++s)
-        if (armed & (1u << s)) mbar_wait(&full[s], (armed_parity >> s) & 1u, &never_abort);
+      for (int s = 0; s < S::kStg; ++s)
+        if (armed & (1u << s)) mbar_wait(&full[s], (armed_parity >> s) & 1u, &never_abort, args.wait_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -201,45 +234,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort)) {
+      const int first_tile = args.hold == kHoldMma ? total : static_cast<int>(blockIdx.x);
+      for (int tile = first_tile; tile < total; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort, args.wait_ns)) {
           record_failure(args.status, abort, 0x2u);
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        // accumulator set acc: kMB x 256 columns (acc is always 0 when kMB = 2)
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kMB * kBN);
         bool ok = true;
         for (int kb = 0; kb < args.num_k; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort)) {
+          if (!mbar_wait(&full[stage], phase, abort, args.wait_ns)) {
             record_failure(args.status, abort, 0x2u);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_addr(sA + stage * kABytes);
+          const uint32_t a0 = smem_addr(sA + stage * S::kAStage);
           const uint32_t b0 = smem_addr(sB + stage * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, kMnBoxBytes, 1024)
-                                     : sdesc_sw128(a0 + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, kMnBoxBytes, 1024)
                                      : sdesc_sw128(b0 + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int h = 0; h < kMB; ++h) {
+              const uint32_t ah = a0 + h * kABytes;
+              const uint64_t ad = A_MN ? sdesc_sw128(ah + kk * 2048, kMnBoxBytes, 1024)
+                                       : sdesc_sw128(ah + kk * 32, 16, 1024);
+              umma_bf16(d_tmem + h * kBN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit(&empty[stage]);
-          if (++stage == kStages) {
+          if (++stage == S::kStg) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
         umma_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == S::kAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       // All MMAs issued above must finish before TMEM is released.
       umma_commit(drain);
-      mbar_wait(drain, 0, &never_abort);
+      mbar_wait(drain, 0, &never_abort, args.wait_ns);
     }
   } else {
     // -------------------------------------------------- epilogue warps
@@ -250,19 +291,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int mb, nb;
       args.sched.tile(tile, mb, nb);
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort));
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, args.wait_ns));
       if (!ok) {
         if (lane == 0) record_failure(args.status, abort, 0x4u);
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * kBN) + (static_cast<uint32_t>(quad * 32) << 16);
-      ctx.row0 = static_cast<int64_t>(mb) * kBM + quad * 32;
-      Epi::run(ep, &tmC, taddr, ctx.row0 + lane, nb, ctx);
+#pragma unroll 1
+      for (int h = 0; h < kMB; ++h) {
+        const uint32_t taddr = tmem_base + static_cast<uint32_t>((acc * kMB + h) * kBN) +
+                               (static_cast<uint32_t>(quad * 32) << 16);
+        ctx.row0 = static_cast<int64_t>(mb * kMB + h) * kBM + quad * 32;
+        Epi::run(ep, &tmC, taddr, ctx.row0 + lane, nb, ctx);
+      }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == S::kAcc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
     if (Epi::kStagingBytes && lane == 0) bulk_wait_group<0>();   // this warp's stores are complete
   }

@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int n0 = nb * kBN + static_cast<int>(half) * 128;
         bool ok = true;
         for (int kb = 0; kb < args.num_k; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort, args.wait_ns)) {
             record_failure(args.status, abort, 0x1u);
             ok = false;
             break;
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (half == 0) {
         // Both CTAs' loads into every armed stage must land before the pair exits.
         for (int s = 0; s < kStages2; ++s)
-          if (armed & (1u << s)) mbar_wait(&full[s], (armed_parity >> s) & 1u, &never_abort);
+          if (armed & (1u << s)) mbar_wait(&full[s], (armed_parity >> s) & 1u, &never_abort, args.wait_ns);
       } else if (*abort) {
         // The leader stopped consuming: give this CTA's in-flight loads time to land.
         const uint64_t t0 = global_timer_ns();
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       for (int tile = pair; tile < total; tile += npairs) {
-        if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort)) {
+        if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort, args.wait_ns)) {
           record_failure(args.status, abort, 0x2u);
           break;
         }
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
         bool ok = true;
         for (int kb = 0; kb < args.num_k; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort)) {
+          if (!mbar_wait(&full[stage], phase, abort, args.wait_ns)) {
             record_failure(args.status, abort, 0x2u);
             ok = false;
             break;
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (acc == 0) acc_phase ^= 1u;
       }
       umma_commit_pair(drain, static_cast<uint16_t>(1u << leader));
-      mbar_wait(drain, 0, &never_abort);
+      mbar_wait(drain, 0, &never_abort, args.wait_ns);
     }
   } else {
     // -------------------------------------------------- epilogue warps (both CTAs)
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int tile = pair; tile < total; tile += npairs) {
       int mb, nb;
       args.sched.tile(tile, mb, nb);
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort));
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, args.wait_ns));
       if (!ok) {
         if (lane == 0) record_failure(args.status, abort, 0x4u);
         break;

@@ -30,45 +30,6 @@ EncodeTiledFn tensor_map_encoder() {
 
 namespace {
 
-constexpr size_t kAlign = 256;
-constexpr size_t kHeader = 256;  // device status word + reserved
-
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-int esize_of(vp_dtype dt) { return dt == VP_BF16 ? 2 : 4; }
-bool dtype_ok(int dt) { return dt == VP_F32 || dt == VP_BF16; }
-
-bool shape_ok(int64_t N, int64_t H, int64_t V, int T) {
-  return N > 0 && H > 0 && V > 0 && T > 0 && V % T == 0 && N < (int64_t(1) << 31) && V < (int64_t(1) << 31) &&
-         H < (int64_t(1) << 31);
-}
-
-// The persistent GEMMs number their 128 x 256 output tiles with 32-bit ints:
-// logits [N, V], dW [V, H] and dX [N, H] must each have fewer than 2^31 tiles.
-bool tiles_ok(int64_t N, int64_t H, int64_t V) {
-  const auto tiles = [](int64_t m, int64_t n) { return ((m + 127) / 128) * ((n + 255) / 256); };
-  const int64_t lim = int64_t(1) << 31;
-  return tiles(N, V) < lim && tiles(V, H) < lim && tiles(N, H) < lim;
-}
-
-// ---------------- forward workspace: header | partial records | z_y
-struct FwdLayout {
-  int tile_v, maxseg;
-  int64_t ntiles;
-  size_t off_partial, off_zy, total;
-};
-FwdLayout fwd_layout(int64_t N, int64_t V, int T, vp_dtype dt) {
-  FwdLayout L;
-  const int64_t Vs = V / T;
-  L.tile_v = dt == VP_BF16 ? kBf16TileV : kF32TileV;
-  L.maxseg = dt == VP_BF16 ? lse_maxseg(V, Vs, T) : f32_maxseg(V, Vs, T);
-  L.ntiles = (V + L.tile_v - 1) / L.tile_v;
-  L.off_partial = kHeader;
-  L.off_zy = align_up(L.off_partial + size_t(L.ntiles) * L.maxseg * N * sizeof(float2), kAlign);
-  L.total = align_up(L.off_zy + size_t(N) * sizeof(float), kAlign);
-  return L;
-}
-
 // ---------------- backward workspace: header | g | dZ chunk | dX fp32 partial (bf16, >1 chunk)
 struct BwdLayout {
   int64_t Vc, ldz;
@@ -120,6 +81,60 @@ FusedLayout fused_layout(int64_t N, int64_t V, int T, int64_t Nc) {
   return L;
 }
 constexpr int64_t kFusedRowAlign = 128;   // token chunks are whole 128-row GEMM blocks
+
+// Budget of the fused call's saved probabilities when the caller names no
+// token chunk: N_c x round8(V) 2-byte values stay below it (the logits are
+// never held for all N tokens at once).
+constexpr size_t kFusedDefaultSavedBytes = size_t(1) << 30;
+
+int64_t fused_default_chunk(int64_t N, int64_t V) {
+  const size_t per_row = size_t((V + 7) / 8 * 8) * 2;
+  int64_t nc = int64_t(kFusedDefaultSavedBytes / per_row) / kFusedRowAlign * kFusedRowAlign;
+  if (nc < kFusedRowAlign) nc = kFusedRowAlign;
+  return nc >= N ? N : nc;
+}
+
+// Token chunk of the fused call for at most nc_max rows per chunk.  Each
+// chunk's dX GEMM runs ceil(rows/128) * ceil(H/256) tiles on the persistent
+// grid, so equal chunks can leave a mostly idle last wave in every chunk:
+// among chunk sizes from nc_max down to half of it, take the one with the
+// fewest dX waves over all chunks, then the fewest chunks (each chunk after
+// the first adds an fp32 read-modify-write of dW).
+int64_t balanced_token_chunk(int64_t N, int64_t H, int64_t nc_max) {
+  if (nc_max >= N) return N;
+  const int64_t cols = (H + 255) / 256;
+  const int64_t sms = gemm_sm_count();
+  const auto waves = [&](int64_t rows) { return ((rows + 127) / 128 * cols + sms - 1) / sms; };
+  const int64_t mmax = nc_max / kFusedRowAlign;
+  int64_t best = mmax, best_w = -1, best_k = -1;
+  for (int64_t m = mmax; m >= 1 && 2 * m >= mmax; --m) {
+    const int64_t nc = m * kFusedRowAlign, k = (N + nc - 1) / nc;
+    const int64_t w = (k - 1) * waves(nc) + waves(N - (k - 1) * nc);
+    if (best_w < 0 || w < best_w || (w == best_w && k < best_k)) {
+      best = m;
+      best_w = w;
+      best_k = k;
+    }
+  }
+  return best * kFusedRowAlign;
+}
+
+// Vocab chunk of the split backward for at most vc_max ids per chunk: the
+// fewest chunks, as equal as the tile allows.
+int64_t balanced_vocab_chunk(int64_t V, int64_t vc_max, int64_t tile) {
+  if (vc_max >= V) return V;
+  const int64_t k = (V + vc_max - 1) / vc_max;
+  const int64_t vc = ((V + k - 1) / k + tile - 1) / tile * tile;
+  return vc < vc_max ? vc : vc_max;
+}
+
+// Default vocab chunk of the split backward: one shard, V/T ids, rounded up
+// to the tile (the pages' unit: each rank forms dZ for its own shard).
+int64_t bwd_default_chunk(int64_t V, int T, vp_dtype dt) {
+  const int64_t tile = bwd_tile(dt);
+  const int64_t vc = (V / T + tile - 1) / tile * tile;
+  return vc >= V ? V : vc;
+}
 // Largest token chunk that fits in ws bytes: all N, else a multiple of 128 (0 if none fits).
 int64_t fused_chunk_from_ws(int64_t N, int64_t V, int T, size_t ws) {
   if (fused_layout(N, V, T, N).total <= ws) return N;
@@ -232,42 +247,32 @@ VP_EXPORT vp_status vp_embed_bwd(const int64_t* ids, const void* dOut, float* dW
 }
 
 VP_EXPORT size_t vp_lmhead_ce_workspace_size(int64_t N, int64_t H, int64_t V, int T, vp_dtype dtype, int pass,
-                                             int64_t vocab_chunk) {
+                                             int64_t chunk) {
   if (!dtype_ok(dtype) || !shape_ok(N, H, V, T)) return 0;
   if (pass == 0) return fwd_layout(N, V, T, dtype).total;
   if (pass == 2 && dtype == VP_BF16) {
-    int64_t nc = N;
-    if (vocab_chunk > 0 && vocab_chunk < N) {
-      nc = vocab_chunk / kFusedRowAlign * kFusedRowAlign;
+    int64_t nc = chunk <= 0 ? fused_default_chunk(N, V) : chunk;
+    if (nc < N) {
+      nc = nc / kFusedRowAlign * kFusedRowAlign;
       if (nc < kFusedRowAlign) nc = kFusedRowAlign;
-      if (nc > N) nc = N;
     }
+    if (nc > N) nc = N;
     return fused_layout(N, V, T, nc).total;
   }
   if (pass == 3 && dtype == VP_BF16) return fused_layout(N, V, T, N).total;   // kept forward state, all N
   if (pass == 2 || pass == 3) {   // fp32: the forward, then the recompute backward in the same bytes
     const size_t f = fwd_layout(N, V, T, dtype).total;
-    const size_t b = vp_lmhead_ce_workspace_size(N, H, V, T, dtype, 1, vocab_chunk);
+    const size_t b = vp_lmhead_ce_workspace_size(N, H, V, T, dtype, 1, chunk);
     return f > b ? f : b;
   }
   if (pass != 1) return 0;
-  int64_t vc = V;
-  if (vocab_chunk > 0 && vocab_chunk < V) {
+  int64_t vc = chunk <= 0 ? bwd_default_chunk(V, T, dtype) : chunk;
+  if (vc < V) {
     const int64_t tile = bwd_tile(dtype);
-    vc = vocab_chunk / tile * tile;
-    if (vc < tile) vc = tile;
-    if (vc > V) vc = V;
+    vc = (vc + tile - 1) / tile * tile;
   }
+  if (vc > V) vc = V;
   return bwd_layout_for_chunk(N, H, V, dtype, vc).total;
-}
-
-static vp_status check_args(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H, int64_t V,
-                            int T, vp_dtype dtype, const void* ws) {
-  if (!X || !W || !targets || !ws || !dtype_ok(dtype) || !shape_ok(N, H, V, T)) return VP_ERR_INVALID_ARG;
-  if (!tiles_ok(N, H, V)) return VP_ERR_UNSUPPORTED;
-  if (!aligned16(X) || !aligned16(W) || !aligned16(ws) || (H * esize_of(dtype)) % 16 != 0) return VP_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(targets) & 7u) != 0) return VP_ERR_UNSUPPORTED;
-  return VP_OK;
 }
 
 static vp_status check_common(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H, int64_t V,
@@ -304,7 +309,7 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd(const void* X, const void* W, const int64_t
   if (e == cudaSuccess)
     e = timed(kMerge, s, [&] {
       return lse_merge(partial, zy, targets, N, V, Vs, T, L.tile_v, L.maxseg, ignore_index, loss, lse, shard_stats,
-                       s);
+                       status, s);
     }, kMergeKernels);
   if (e == cudaSuccess && (loss_mean || n_bad))
     e = timed(kMean, s, [&] { return loss_mean_and_bad(loss, targets, N, V, ignore_index, loss_mean, n_bad, s); });
@@ -320,8 +325,9 @@ VP_EXPORT vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t
   vp_status st = check_common(X, W, targets, N, H, V, T, dtype, workspace);
   if (st != VP_OK) return st;
   if (!aligned16(dX) || !aligned16(dW)) return VP_ERR_UNSUPPORTED;
-  const int64_t Vc = bwd_chunk_from_ws(N, H, V, dtype, ws_bytes);
-  if (Vc <= 0) return VP_ERR_WORKSPACE;
+  const int64_t Vc_max = bwd_chunk_from_ws(N, H, V, dtype, ws_bytes);
+  if (Vc_max <= 0) return VP_ERR_WORKSPACE;
+  const int64_t Vc = balanced_vocab_chunk(V, Vc_max, bwd_tile(dtype));
   const BwdLayout L = bwd_layout_for_chunk(N, H, V, dtype, Vc);
   cudaStream_t s = as_stream(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -385,8 +391,9 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int
     return vp_lmhead_ce_bwd(X, W, targets, lse, dloss, dmean, N, H, V, T, ignore_index, dtype, dX, dW, workspace,
                             ws_bytes, stream);
   }
-  const int64_t Nc = fused_chunk_from_ws(N, V, T, ws_bytes);
-  if (Nc <= 0) return VP_ERR_WORKSPACE;
+  const int64_t Nc_max = fused_chunk_from_ws(N, V, T, ws_bytes);
+  if (Nc_max <= 0) return VP_ERR_WORKSPACE;
+  const int64_t Nc = balanced_token_chunk(N, H, Nc_max);
   if (!tensor_map_encoder()) return VP_ERR_CUDA;
   const FusedLayout L = fused_layout(N, V, T, Nc);
   cudaStream_t s = as_stream(stream);
@@ -411,7 +418,7 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int
     if (e == cudaSuccess)
       e = timed(kMerge, s, [&] {
         return lse_merge_ld(partial, zy, yc, nc, V, Vs, T, kBf16TileV, L.maxseg, ignore_index, loss + n0, lse + n0,
-                            shard_stats ? shard_stats + n0 : nullptr, N, s);
+                            shard_stats ? shard_stats + n0 : nullptr, N, status, s);
       }, kMergeKernels);
     void* dXc = static_cast<uint8_t*>(dX) + n0 * H * 2;
     // p -> dZ in place, then dW = sum over token chunks of dZ_c^T X_c; dX rows of this chunk are complete
@@ -456,7 +463,7 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_keep(const void* X, const void* W, const in
   if (e == cudaSuccess)
     e = timed(kMerge, s, [&] {
       return lse_merge(partial, zy, targets, N, V, Vs, T, kBf16TileV, L.maxseg, ignore_index, loss, lse, shard_stats,
-                       s);
+                       status, s);
     }, kMergeKernels);
   if (e == cudaSuccess && (loss_mean || n_bad))
     e = timed(kMean, s, [&] { return loss_mean_and_bad(loss, targets, N, V, ignore_index, loss_mean, n_bad, s); });
@@ -492,6 +499,109 @@ VP_EXPORT vp_status vp_lmhead_ce_bwd_saved(const void* X, const void* W, const i
     e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(P, L.ldp, X, N, H, 0, V, dW, false, status, s); });
   if (e == cudaSuccess)
     e = timed(kDxGemm, s, [&] { return bf16_dx_chunk(P, L.ldp, W, N, H, 0, V, dX, nullptr, 3, status, s); });
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+// ---------------- one shard of a T-rank vocabulary (a rank that holds only W_t)
+static vp_status check_shard(const void* X, const void* W_t, const int64_t* targets, int64_t N, int64_t H, int64_t V,
+                             int T, int t, vp_dtype dtype, const void* ws) {
+  if (!shape_ok(N, H, V, T) || t < 0 || t >= T) return VP_ERR_INVALID_ARG;
+  return check_args(X, W_t, targets, N, H, V / T, 1, dtype, ws);
+}
+
+VP_EXPORT vp_status vp_lmhead_ce_shard_fwd(const void* X, const void* W_t, const int64_t* targets, int64_t N,
+                                           int64_t H, int64_t V, int T, int t, int64_t ignore_index, vp_dtype dtype,
+                                           float* stats, void* workspace, size_t ws_bytes, void* stream) {
+  if (!stats) return VP_ERR_INVALID_ARG;
+  vp_status st = check_shard(X, W_t, targets, N, H, V, T, t, dtype, workspace);
+  if (st != VP_OK) return st;
+  if (dtype == VP_BF16 && !tensor_map_encoder()) return VP_ERR_CUDA;
+  const int64_t Vs = V / T;
+  const FwdLayout L = fwd_layout(N, Vs, 1, dtype);   // the shard alone: one record per tile
+  if (ws_bytes < L.total) return VP_ERR_WORKSPACE;
+  cudaStream_t s = as_stream(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  float2* partial = reinterpret_cast<float2*>(ws + L.off_partial);
+  float* zy = reinterpret_cast<float*>(ws + L.off_zy);
+  const int64_t start = static_cast<int64_t>(t) * Vs;
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess)
+    e = timed(kLseGemm, s, [&] {
+      if (dtype == VP_BF16)
+        return bf16_lse_stats(X, W_t, targets, N, H, Vs, Vs, partial, L.maxseg, zy, status, s, start);
+      return f32_lse_stats(static_cast<const float*>(X), static_cast<const float*>(W_t), targets, N, H, Vs, Vs,
+                           partial, L.maxseg, zy, s, start);
+    });
+  if (e == cudaSuccess)
+    e = timed(kMerge, s, [&] {
+      return shard_stats(partial, zy, targets, N, V, start, Vs, L.ntiles, ignore_index, stats, status, s);
+    });
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+VP_EXPORT vp_status vp_lmhead_ce_merge_stats(const float* stats, const int64_t* targets, int64_t N, int64_t V, int T,
+                                             int64_t ignore_index, float* loss, float* lse, float* loss_mean,
+                                             int32_t* n_bad, void* stream) {
+  if (!stats || !targets || !loss || !lse || N <= 0 || V <= 0 || T <= 0 || V % T != 0 || N >= (int64_t(1) << 31))
+    return VP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(targets) & 7u) != 0) return VP_ERR_UNSUPPORTED;
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e =
+      timed(kMerge, s, [&] { return merge_shard_stats(stats, targets, N, V, T, ignore_index, loss, lse, s); });
+  if (e == cudaSuccess && (loss_mean || n_bad))
+    e = timed(kMean, s, [&] { return loss_mean_and_bad(loss, targets, N, V, ignore_index, loss_mean, n_bad, s); });
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+VP_EXPORT vp_status vp_lmhead_ce_shard_bwd(const void* X, const void* W_t, const int64_t* targets, const float* lse,
+                                           const float* dloss, const float* dmean, int64_t N, int64_t H, int64_t V,
+                                           int T, int t, int64_t ignore_index, vp_dtype dtype, float* dX_t,
+                                           float* dW_t, void* workspace, size_t ws_bytes, void* stream) {
+  if (!lse || !dX_t || !dW_t) return VP_ERR_INVALID_ARG;
+  vp_status st = check_shard(X, W_t, targets, N, H, V, T, t, dtype, workspace);
+  if (st != VP_OK) return st;
+  if (!aligned16(dX_t) || !aligned16(dW_t)) return VP_ERR_UNSUPPORTED;
+  if (dtype == VP_BF16 && !tensor_map_encoder()) return VP_ERR_CUDA;
+  const int64_t Vs = V / T;
+  const int64_t Vc_max = bwd_chunk_from_ws(N, H, Vs, dtype, ws_bytes);
+  if (Vc_max <= 0) return VP_ERR_WORKSPACE;
+  const int64_t Vc = balanced_vocab_chunk(Vs, Vc_max, bwd_tile(dtype));
+  const BwdLayout L = bwd_layout_for_chunk(N, H, Vs, dtype, Vc);
+  cudaStream_t s = as_stream(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  float* g = reinterpret_cast<float*>(ws + L.off_g);
+  void* dz = ws + L.off_dz;
+  const int64_t start = static_cast<int64_t>(t) * Vs;
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess)   // validity against the whole vocabulary: every rank sees the same N_valid
+    e = timed(kScale, s, [&] { return upstream_scale(targets, dloss, dmean, N, V, ignore_index, g, s); });
+  for (int64_t c0 = 0; c0 < Vs && e == cudaSuccess; c0 += Vc) {
+    const int64_t vc = (Vs - c0) < Vc ? (Vs - c0) : Vc;
+    const bool first = c0 == 0;
+    if (dtype == VP_BF16) {
+      e = timed(kDzGemm, s,
+                [&] { return bf16_dz_chunk(X, W_t, targets, lse, g, N, H, c0, vc, dz, L.ldz, status, s, start); });
+      if (e == cudaSuccess)
+        e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(dz, L.ldz, X, N, H, c0, vc, dW_t, false, status, s); });
+      // this shard's part of dX in fp32: stored by the first chunk, added by the others
+      if (e == cudaSuccess)
+        e = timed(kDxGemm, s, [&] {
+          return bf16_dx_chunk(dz, L.ldz, W_t, N, H, c0, vc, dX_t, nullptr, first ? 0 : 1, status, s);
+        });
+    } else {
+      const float* Xf = static_cast<const float*>(X);
+      const float* Wf = static_cast<const float*>(W_t);
+      float* dzf = static_cast<float*>(dz);
+      e = timed(kDzGemm, s,
+                [&] { return f32_dz_chunk(Xf, Wf, targets, lse, g, N, H, c0, vc, dzf, L.ldz, s, start); });
+      if (e == cudaSuccess)
+        e = timed(kDwGemm, s, [&] { return f32_gemm(dzf, 1, L.ldz, Xf, H, 1, dW_t + c0 * H, H, vc, H, N, false, s); });
+      if (e == cudaSuccess)
+        e = timed(kDxGemm, s, [&] { return f32_gemm(dzf, L.ldz, 1, Wf + c0 * H, H, 1, dX_t, H, N, H, vc, !first, s); });
+    }
+  }
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
 }
 
@@ -574,7 +684,14 @@ VP_EXPORT const char* vp_stage_name(int stage) {
   return (stage >= 0 && stage < kNumStages) ? kStageNames[stage] : nullptr;
 }
 
-VP_EXPORT vp_status vp_test_set_gemm_variant(int pair) {
-  set_gemm_variant(pair);
+VP_EXPORT vp_status vp_test_set_gemm_variant(int variant) {
+  if (variant < 0 || variant > 2) return VP_ERR_INVALID_ARG;
+  set_gemm_variant(variant);
+  return VP_OK;
+}
+
+VP_EXPORT vp_status vp_test_set_wait_fault(int mode, uint64_t wait_ns) {
+  if (mode < 0 || mode > 2) return VP_ERR_INVALID_ARG;
+  set_wait_fault(mode, wait_ns);
   return VP_OK;
 }

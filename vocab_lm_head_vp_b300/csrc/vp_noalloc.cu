@@ -29,28 +29,28 @@ constexpr int kNoAllocMaxDevices = 64;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 // In host code `g_noalloc_scratch` only names a host-side stand-in; the
-// device address is looked up once per device, with that device current.
-struct DeviceScratch {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
-};
-DeviceScratch g_scratch[kNoAllocMaxDevices];
+// device address is looked up with the device current, the first time a call
+// runs on that device, and kept for later calls on it.  A failed lookup is not
+// kept: the next call tries again.
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kNoAllocMaxDevices] = {};
 
 cudaError_t scratch_on_current_device(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
-  DeviceScratch& d = g_scratch[dev];
-  std::call_once(d.once, [&d] { d.err = cudaGetSymbolAddress(&d.ptr, g_noalloc_scratch); });
-  if (d.err != cudaSuccess) return d.err;
-  if (!d.ptr) return cudaErrorInvalidSymbol;
-  *out = d.ptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    if (!p) return cudaErrorInvalidSymbol;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
   return cudaSuccess;
 }
-
-size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 }  // namespace vp
@@ -61,47 +61,38 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_noalloc(const void* X, const void* W, const
                                              int64_t H, int64_t V, int T, int64_t ignore_index, vp_dtype dtype,
                                              float* loss, float* lse, float* loss_mean, float* shard_stats,
                                              int32_t* n_bad, void* stream) {
-  if (!X || !W || !targets || !loss || !lse) return VP_ERR_INVALID_ARG;
-  if (dtype != VP_F32 && dtype != VP_BF16) return VP_ERR_INVALID_ARG;
-  if (N <= 0 || H <= 0 || V <= 0 || T <= 0 || V % T != 0 || N >= (int64_t(1) << 31) || V >= (int64_t(1) << 31) ||
-      H >= (int64_t(1) << 31))
-    return VP_ERR_INVALID_ARG;
-  const int es = dtype == VP_BF16 ? 2 : 4;
-  const auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  if (!a16(X) || !a16(W) || (H * es) % 16 != 0 || (reinterpret_cast<uintptr_t>(targets) & 7u) != 0)
-    return VP_ERR_UNSUPPORTED;
-
-  // Scratch layout: status word | (m, S) records per vocab tile and shard slot | z_y.
-  const int64_t Vs = V / T;
-  const int tile_v = dtype == VP_BF16 ? kBf16TileV : kF32TileV;
-  const int maxseg = dtype == VP_BF16 ? lse_maxseg(V, Vs, T) : f32_maxseg(V, Vs, T);
-  const int64_t ntiles = (V + tile_v - 1) / tile_v;
-  const size_t off_partial = 256;
-  const size_t off_zy = up256(off_partial + size_t(ntiles) * maxseg * size_t(N) * sizeof(float2));
-  const size_t need = up256(off_zy + size_t(N) * sizeof(float));
-  if (need > kNoAllocScratchBytes) return VP_ERR_WORKSPACE;   // beyond the fixed 32 MiB scratch
+  if (!loss || !lse) return VP_ERR_INVALID_ARG;
+  const vp_status st = check_inputs(X, W, targets, N, H, V, T, dtype);
+  if (st != VP_OK) return st;
+  // the same scratch layout as vp_lmhead_ce_fwd's workspace
+  const FwdLayout L = fwd_layout(N, V, T, dtype);
+  if (L.total > kNoAllocScratchBytes) return VP_ERR_WORKSPACE;   // beyond the fixed 32 MiB scratch
   if (dtype == VP_BF16 && !tensor_map_encoder()) return VP_ERR_CUDA;
 
   void* base = nullptr;
   if (scratch_on_current_device(&base) != cudaSuccess) return VP_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(base);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
-  float2* partial = reinterpret_cast<float2*>(ws + off_partial);
-  float* zy = reinterpret_cast<float*>(ws + off_zy);
+  float2* partial = reinterpret_cast<float2*>(ws + L.off_partial);
+  float* zy = reinterpret_cast<float*>(ws + L.off_zy);
+  const int64_t Vs = V / T;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   // The array keeps the previous call's contents: the status word must start at
-  // zero; every record the merge reads is rewritten by this call's tiles.
+  // zero; every record the merge reads is rewritten by this call's tiles.  The
+  // status word cannot be read through vp_read_device_status; a kernel that
+  // gives up a wait makes the merge write NaN to loss and lse instead.
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess) {
     if (dtype == VP_BF16)
-      e = bf16_lse_stats(X, W, targets, N, H, V, Vs, partial, maxseg, zy, status, s);
+      e = bf16_lse_stats(X, W, targets, N, H, V, Vs, partial, L.maxseg, zy, status, s);
     else
       e = f32_lse_stats(static_cast<const float*>(X), static_cast<const float*>(W), targets, N, H, V, Vs, partial,
-                        maxseg, zy, s);
+                        L.maxseg, zy, s);
   }
   if (e == cudaSuccess)
-    e = lse_merge(partial, zy, targets, N, V, Vs, T, tile_v, maxseg, ignore_index, loss, lse, shard_stats, s);
+    e = lse_merge(partial, zy, targets, N, V, Vs, T, L.tile_v, L.maxseg, ignore_index, loss, lse, shard_stats,
+                  status, s);
   if (e == cudaSuccess && (loss_mean || n_bad))
     e = loss_mean_and_bad(loss, targets, N, V, ignore_index, loss_mean, n_bad, s);
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
