@@ -40,7 +40,7 @@ GEMM_STAGES = {"split": ("lse_stats_gemm", "dz_recompute_gemm", "dw_gemm", "dx_g
                "fused": ("lse_p_gemm", "dw_gemm", "dx_gemm")}
 # library stages of the LM head's forward and backward (the gather is timed apart)
 FWD_STAGES = ("lse_stats_gemm", "lse_p_gemm", "lse_merge", "loss_mean", "upstream_scale")
-BWD_STAGES = ("dz_recompute_gemm", "dz_from_p", "dw_gemm", "dx_gemm")
+BWD_STAGES = ("dz_recompute_gemm", "dz_from_p", "x_transpose", "dw_gemm", "dx_gemm")
 
 
 def fwd_bwd_ms(stages, steps):
@@ -331,7 +331,10 @@ def embed_microbench(vp, dev, iters=20):
             alone = [loop(False) for _ in range(3)]
             ms = (statistics.median(both) - statistics.median(alone)) / iters
             nbytes = 2.0 * wl.N * wl.H * 2 + 8.0 * wl.N
-            out[f"{name}_{kind}"] = {"N": wl.N, "H": wl.H, "V": wl.V, "ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9}
+            out[f"{name}_{kind}"] = {"N": wl.N, "H": wl.H, "V": wl.V, "ms": ms, "GB/s": nbytes / (ms / 1e3) / 1e9,
+                                     "rate": ("L2-assisted: repeated Zipf ids hit rows already in L2, so this is "
+                                              "not an HBM rate" if kind == "zipf" else
+                                              "HBM: distinct rows, L2 flushed before each launch")}
         del W, o
     return out
 
@@ -667,7 +670,8 @@ def run_ours(args):
         # read fp16 p, one fp32 tile maximum per 256 columns, and write bf16 dZ for valid rows;
         # write zeros for ignored ones
         dzp_bytes = (4.0 * valid_rows + 2.0 * (N - valid_rows)) * V + 4.0 * valid_rows * -(-V // 256)
-        dzp_gbs = dzp_bytes / (dzp_ms / max(1, dzp_n) / 1e3) / 1e9
+        # those bytes are the whole batch's, moved by the step's launches (one per token chunk)
+        dzp_gbs = dzp_bytes * args.steps / (dzp_ms / 1e3) / 1e9
         extra["roofline_dz_from_p"] = {"kernel": "dz_from_p_kernel", "bound": "hbm", "achieved": dzp_gbs,
                                        "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dzp_gbs / peaks["hbm_gbs"]}
     launches = sum(c for _, c in stages.values())

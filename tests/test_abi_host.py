@@ -82,16 +82,25 @@ def test_ce_rejects_bad_arguments(lib):
     assert bwd(X, W, y, lse, None, None, 6, 64, 16, 4, -100, vp.VP_F32, P(0x70000), P(0x80000), ws, 64, None) == 3
 
 
+SK = 2 * 160 * 256 * 256 * 4   # bf16 backward: stream-K partial tiles of the dX GEMM
+
+
+def XT(rows, H):                # bf16 backward: X^T (rows rounded up to 8) for the dW GEMM
+    return H * ((rows + 7) // 8 * 8) * 2
+
+
 def test_workspace_sizes(lib):
     N, H, V, T = 16384, 4096, 128256, 8
     fwd = vp.workspace_size(N, H, V, T, vp.VP_BF16, 0)
     # records: ceil(V/256) tiles x 2 segment slots x N tokens x (m, R) fp32, plus z_y
     assert fwd >= 501 * 2 * N * 8 + N * 4 and fwd < 501 * 2 * N * 8 + N * 4 + 4096
     one = vp.workspace_size(N, H, V, T, vp.VP_BF16, 1, V)
-    assert one >= N * V * 2 and one < N * V * 2 + N * 4 + 4096       # one chunk: bf16 dZ, no fp32 dX partial
+    one_body = N * V * 2 + SK + XT(N, H)
+    assert one_body <= one < one_body + N * 4 + 4096       # one chunk: bf16 dZ, no fp32 dX partial
     # default: one shard's dZ (V/T = 16032 rounded up to 16128) plus the fp32 dX partial
     d = vp.workspace_size(N, H, V, T, vp.VP_BF16, 1)
-    assert N * 16128 * 2 + N * H * 4 <= d < N * 16128 * 2 + N * H * 4 + N * 4 + 4096
+    d_body = N * 16128 * 2 + N * H * 4 + SK + XT(N, H)
+    assert d_body <= d < d_body + N * 4 + 4096
     assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 1, 16032) == d
     assert vp.workspace_size(N, H, V, 1, vp.VP_BF16, 1) == one          # T = 1: the shard is all of V
     assert vp.workspace_size(N, H, V, 7, vp.VP_BF16, 1) == 0           # V % T != 0
@@ -102,10 +111,10 @@ def test_fused_workspace_sizes(lib):
     N, H, V, T = 16384, 4096, 128256, 8
     full = vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, N)
     # fp16 p / bf16 dZ [N, V] + per tile and token: 2 (m, R) slots, the tile max; + z_y, g
-    body = N * V * 2 + 501 * N * (2 * 8 + 4) + 2 * N * 4
+    body = N * V * 2 + 501 * N * (2 * 8 + 4) + 2 * N * 4 + SK + XT(N, H)
     assert body <= full < body + 8192
     half = vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 8192)
-    assert half < full / 2 + N * 8 and half > full / 2 - N * V
+    assert half - SK < (full - SK) / 2 + N * 8 and half - SK > (full - SK) / 2 - N * V - XT(N, H)
     assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 100) == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 128)
     # default: saved probabilities of at most 1 GiB (4096 token rows of V = 128256)
     assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 2) == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 4096)

@@ -314,21 +314,41 @@ def test_gemm_forms_agree_on_the_path(variant):
         vp.set_gemm_variant(0)
 
 
-@pytest.mark.parametrize("N,H,V,chunk", [(300, 264, 1800, 1024), (1100, 512, 3000, None), (77, 64, 700, 256)])
-def test_dx_tile_forms_bit_identical(N, H, V, chunk):
+@pytest.mark.parametrize("N,H,V,chunk,streamk", [
+    (300, 264, 1800, 1800, False), (1100, 512, 3000, 3000, False), (77, 64, 700, 256, False),
+    (2560, 1024, 2000, 2000, True),      # 40 tiles of 256 x 256 over 148 SMs: every tile split over ~4 CTAs
+    (2600, 1032, 6000, 1536, True),      # ragged rows and columns, four vocab chunks (fp32 store / add / bf16)
+    (2600, 1032, 2000, None, True),      # the default chunks (one shard each)
+])
+def test_dx_tile_forms(N, H, V, chunk, streamk):
     """dX from 256 x 256 tiles (two 128-row accumulators sharing each B stage)
-    equals dX from 128 x 256 tiles bit for bit: every output element runs the
-    same K loop in the same order.  N not a multiple of 256 leaves the second
-    128-row block of the last tile partly or wholly past the end."""
+    against dX from 128 x 256 tiles, and dW through X^T against dW = dZ^T X.  Without stream-K every output element runs
+    the same K loop in the same order: bit-identical.  With stream-K (tiles that
+    do not fill whole waves) a split tile's k-blocks are summed per CTA and the
+    fp32 partial sums added in k order, so the two differ by fp32 summation
+    order only; both are held to the oracle's elementwise bound.  N not a
+    multiple of 256 leaves the second 128-row block of the last tile partly or
+    wholly past the end."""
     inp = synth.small_case(N, H, V, 4, "bf16", seed=N + V, ignore_frac=0.1)
     outs = []
     for variant in (0, 2):
         vp.set_gemm_variant(variant)
+        vp.stage_timing_enable(256)
         try:
             f, dX, dW = _run(inp, 4, vocab_chunk=chunk)
+            stages = vp.stage_timing_read()
         finally:
+            vp.stage_timing_enable(0)
             vp.set_gemm_variant(0)
-        outs.append((f["loss"], dX, dW))
-    for a, b in zip(*outs):
-        assert torch.equal(a, b)
-    _check(inp, 4, f, dX, dW)
+        _check(inp, 4, f, dX, dW)
+        outs.append((f["loss"], dX, dW, stages["dx_gemm"][1], stages["dw_gemm"][1]))
+    (l0, x0, w0, k0, c0), (l2, x2, w2, k2, c2) = outs
+    assert c0 == c2                                 # vocab chunks: one dW launch each
+    assert k2 == c2                                 # 128-row tiles: whole tiles, one dX kernel per chunk
+    assert k0 == (2 * c2 if streamk else c2)        # stream-K: the GEMM and its fix-up pass
+    # dW: through X^T (form 0) or directly (form 2); the same products summed in the same K order
+    assert torch.equal(l0, l2) and rel_fro(np64(w0), np64(w2)) <= 1e-5
+    if streamk:
+        assert rel_fro(np64(x0), np64(x2)) <= 1e-3
+    else:
+        assert torch.equal(x0, x2)

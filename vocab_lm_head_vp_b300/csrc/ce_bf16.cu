@@ -383,6 +383,73 @@ struct EpiStore {
   }
 };
 
+// dW through its transpose: the GEMM computes tiles of dW^T = X^T dZ (rows =
+// hidden index h, columns = vocab index v) from K-major X^T and MN-major dZ,
+// and the epilogue writes each 32 x 32 block transposed into dW [V, H] fp32
+// through shared memory, adding the old values first when accumulating (the
+// sum over token chunks).  A K-major A operand keeps the tensor pipe busier
+// than the MN-major dZ^T that dW = dZ^T X would take as A.
+struct EpiStoreT {
+  static constexpr uint32_t kStagingBytes = kStoreStagingBytes;
+  struct Params {
+    float* out;       // dW rows of this launch's vocab range, [V][ld]
+    int64_t ld;       // row length of out (H)
+    int64_t V, H;     // valid vocab rows / hidden columns
+    int add;          // 1: out += tile, 0: out = tile
+  };
+  __device__ static void run(const Params& p, const CUtensorMap* tm, uint32_t taddr, int64_t h, int nb,
+                             EpiCtx& ctx) {
+    const int64_t h0 = ctx.row0;   // this warp's first hidden index (warp-uniform)
+    if (h0 >= p.H) return;
+    const int64_t vbase = static_cast<int64_t>(nb) * kBN;
+    const bool hok = h < p.H;
+#pragma unroll 1
+    for (int b = 0; b < kBN / 32; ++b) {
+      const int64_t v0 = vbase + b * 32;
+      if (v0 >= p.V) break;   // uniform over the CTA
+      uint32_t r[32];
+      __syncwarp();
+      tmem_ld32(taddr + b * 32, r);
+      tmem_ld_wait();
+      if (p.add) {
+        // old dW[v0 + j][h]: for each j the warp reads 32 consecutive floats
+        float old[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) old[j] = (hok && v0 + j < p.V) ? p.out[(v0 + j) * p.ld + h] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(as_f(r[j]) + old[j]);
+      }
+      // columns >= H and rows >= V are clipped by the tensor map
+      stage_transposed_and_store(ctx, tm, r, static_cast<int32_t>(h0), static_cast<int32_t>(v0));
+    }
+  }
+};
+
+// out[c][r] = in[r][c] for a bf16 [rows][cols] matrix; cols a multiple of 8.
+// 64 x 64 tiles through shared memory, 16-byte loads along the input rows.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __restrict__ in, int64_t rows,
+                                                             int64_t cols, int64_t ld_in, uint16_t* __restrict__ out,
+                                                             int64_t ld_out) {
+  __shared__ uint16_t t[64][64 + 2];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, c0 = static_cast<int64_t>(blockIdx.x) * 64;
+  for (int e = threadIdx.x; e < 64 * 8; e += blockDim.x) {
+    const int r = e >> 3, cv = (e & 7) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r0 + r < rows && c0 + cv < cols) v = *reinterpret_cast<const uint4*>(in + (r0 + r) * ld_in + c0 + cv);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      t[r][cv + 2 * q] = static_cast<uint16_t>(w[q] & 0xffffu);
+      t[r][cv + 2 * q + 1] = static_cast<uint16_t>(w[q] >> 16);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < 64 * 64; e += blockDim.x) {
+    const int c = e >> 6, r = e & 63;
+    if (c0 + c < cols && r0 + r < rows) out[(c0 + c) * ld_out + r0 + r] = t[r][c];
+  }
+}
+
 // ------------------------------------------------------------------ host side
 namespace {
 
@@ -442,17 +509,32 @@ cudaError_t ensure_smem(Kern kern, size_t smem, std::atomic<int>* done) {
   return e;
 }
 
+// Stream-K launches use at most this many CTAs (the partial workspace holds
+// two 256 x 256 fp32 slots per CTA: sk_workspace_bytes()).
+constexpr int kSkMaxCtas = 160;
+
 // Diagnostic of the bounded waits (vp_test_set_wait_fault): a role of every
 // later one-SM GEMM launch that issues nothing, and the waits' time limit.
 int g_hold = kHoldNone;
 uint64_t g_wait_ns = kWaitTimeoutNs;
 
+// Stream-K plan of one launch: the partial workspace and its tensor map.
+struct StreamK {
+  float* ws = nullptr;    // 2 * kSkMaxCtas * 256 rows x 256 fp32 (partial slots)
+  CUtensorMap tp;         // over ws, 32-row x 32-column fp32 boxes
+  int64_t iters = 0;      // 0: whole tiles
+  int grid = 0;
+};
+
 // kMB 128-row blocks per CTA tile (1: 128 x 256 tiles, 2: 256 x 256 tiles);
-// group_m_rows: output rows per tile group.
+// group_m_rows: output rows per tile group.  With sk_ws, a launch whose tiles
+// do not fill whole waves of the persistent grid runs stream-K (the CTAs
+// split the (tile, k-block) iterations evenly) and `sk` returns the plan the
+// fix-up pass needs.
 template <bool A_MN, bool B_MN, class Epi, int kMB = 1>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, int64_t M,
                         int64_t Ncols, int64_t K, const typename Epi::Params& ep, uint32_t* status,
-                        cudaStream_t stream, int group_m_rows) {
+                        cudaStream_t stream, int group_m_rows, float* sk_ws = nullptr, StreamK* sk = nullptr) {
   auto kern = umma_gemm_kernel<A_MN, B_MN, Epi, kMB>;
   constexpr size_t smem = GemmShape<kMB>::kSmem + Epi::kStagingBytes;
   static std::atomic<int> attr_done[kMaxDevices];
@@ -467,9 +549,28 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   a.status = status;
   a.wait_ns = g_wait_ns;
   a.hold = g_hold;
+  a.sk_iters = 0;
   const int total = a.sched.num_m * a.sched.num_n;
-  const int grid = total < sm_count() ? total : sm_count();
-  kern<<<grid, kGemmThreads, smem, stream>>>(ta, tb, tc, a, ep);
+  int grid = total < sm_count() ? total : sm_count();
+  const CUtensorMap* tp = &tc;
+  if (sk) sk->iters = 0;
+  if (sk && sk_ws && Epi::kStagingBytes > 0) {
+    const int G = sm_count() < kSkMaxCtas ? sm_count() : kSkMaxCtas;
+    const int64_t iters = static_cast<int64_t>(total) * a.num_k;
+    // at least G/4 tiles, so a tile's k-blocks spread over at most 8 CTAs (the fix-up's piece limit)
+    if (total % G != 0 && 4 * total >= G && a.num_k >= 2 && iters >= G) {
+      sk->ws = sk_ws;
+      const int64_t rows = static_cast<int64_t>(2 * G) * kMB * kBM;
+      if (!make_tmap(&sk->tp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sk_ws, rows, kBN, kBN, 32, 32))
+        return cudaErrorInvalidValue;
+      sk->iters = iters;
+      sk->grid = G;
+      a.sk_iters = iters;
+      grid = G;
+      tp = &sk->tp;
+    }
+  }
+  kern<<<grid, kGemmThreads, smem, stream>>>(ta, tb, tc, *tp, a, ep);
   return cudaGetLastError();
 }
 
@@ -514,6 +615,7 @@ cudaError_t launch_gemm_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const 
   a.status = status;
   a.wait_ns = g_wait_ns;
   a.hold = kHoldNone;   // the hold diagnostic covers the one-SM form only
+  a.sk_iters = 0;
   const int total = a.sched.num_m * a.sched.num_n;
   const int pairs = total < max_pairs ? total : max_pairs;
   cfg.gridDim = dim3(2 * pairs);
@@ -532,19 +634,75 @@ int kmajor_b_box_rows() { return pair_kernels() ? 128 : kBN; }
 template <bool A_MN, bool B_MN, class Epi, int kMB = 1>
 cudaError_t launch_any(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, int64_t M,
                        int64_t Ncols, int64_t K, const typename Epi::Params& ep, uint32_t* status,
-                       cudaStream_t stream, int group_m_rows) {
+                       cudaStream_t stream, int group_m_rows, float* sk_ws = nullptr, StreamK* sk = nullptr) {
+  if (sk) sk->iters = 0;
   if (pair_kernels())
     return launch_gemm_2sm<A_MN, B_MN, Epi>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows / kPairBM);
   if (kMB == 2 && g_variant == 2)
     return launch_gemm<A_MN, B_MN, Epi, 1>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows);
-  return launch_gemm<A_MN, B_MN, Epi, kMB>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows);
+  return launch_gemm<A_MN, B_MN, Epi, kMB>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows, sk_ws, sk);
+}
+
+// Stream-K fix-up: one block per CTA boundary of the launch that falls inside a
+// tile (the first such boundary of each tile does the tile).  The tile's
+// pieces, in CTA order (k order), are added in fp32 and the sum finished as
+// the store epilogue would: fp32 store, fp32 add onto the output, or bf16
+// (after adding `partial`).  Columns come in fours (H is a multiple of 8).
+__global__ void __launch_bounds__(256) sk_fixup_kernel(const float* __restrict__ ws, int64_t iters, int G, int num_k,
+                                                       TileSched sched, int tile_rows, void* __restrict__ out,
+                                                       const float* __restrict__ partial, int64_t ld, int64_t M,
+                                                       int64_t Ncols, int mode) {
+  const int c = static_cast<int>(blockIdx.x) + 1;
+  const int64_t b = sk_begin(c, G, iters);
+  if (b % num_k == 0) return;                                        // a tile edge: nothing split here
+  const int64_t t = b / num_k;
+  if (sk_begin(c - 1, G, iters) > t * num_k) return;                 // an earlier boundary inside t does it
+  int c_last = c;
+  while (c_last + 1 < G && sk_begin(c_last + 1, G, iters) < (t + 1) * num_k) ++c_last;
+  int slots[8];
+  int np = 0;
+  for (int q = c - 1; q <= c_last && np < 8; ++q)
+    slots[np++] = (sk_begin(q, G, iters) / num_k == t) ? 2 * q : 2 * q + 1;
+  int mb, nb;
+  sched.tile(static_cast<int>(t), mb, nb);
+  const int64_t row0 = static_cast<int64_t>(mb) * tile_rows, col0 = static_cast<int64_t>(nb) * kBN;
+  for (int e = threadIdx.x; e < tile_rows * (kBN / 4); e += blockDim.x) {
+    const int r = e / (kBN / 4), cq = (e % (kBN / 4)) * 4;
+    const int64_t row = row0 + r, col = col0 + cq;
+    if (row >= M || col >= Ncols) continue;
+    float4 acc = *reinterpret_cast<const float4*>(ws + (static_cast<int64_t>(slots[0]) * tile_rows + r) * kBN + cq);
+    for (int q = 1; q < np; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(ws + (static_cast<int64_t>(slots[q]) * tile_rows + r) * kBN + cq);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int64_t o = row * ld + col;
+    if (mode == kStoreF32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + o) = acc;
+    } else if (mode == kAddF32) {
+      float4* d = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
+      const float4 x = *d;
+      *d = make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
+    } else {
+      if (mode == kStoreBf16AddPartial) {
+        const float4 x = *reinterpret_cast<const float4*>(partial + o);
+        acc = make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
+      }
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + o) =
+          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    }
+  }
 }
 
 }  // namespace
 
 void set_gemm_variant(int variant) { g_variant = (variant == 1 || variant == 2) ? variant : 0; }
 
-int gemm_sm_count() { return sm_count(); }
+bool dw_through_xt() { return g_variant != 2; }
+
+size_t sk_workspace_bytes() { return size_t(2) * kSkMaxCtas * 2 * kBM * kBN * sizeof(float); }
 
 void set_wait_fault(int hold, uint64_t wait_ns) {
   g_hold = (hold == kHoldProducer || hold == kHoldMma) ? hold : kHoldNone;
@@ -597,7 +755,7 @@ cudaError_t bf16_dz_chunk(const void* X, const void* W, const int64_t* targets, 
 
 cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N, int64_t H, int64_t c0,
                           int64_t Vc, void* out, const float* partial, int mode, uint32_t* status,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, float* sk_ws, int* kernels) {
   // dX[N,H] (+)= dZ_c[N,Vc] * W_c[Vc,H]: A = dZ_c (K-major), B = W_c viewed as
   // [K=Vc rows][N=H cols] (MN-major).
   CUtensorMap ta, tb, tc;
@@ -607,8 +765,23 @@ cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N,
   if (!make_store_tmap(&tc, mode >= kStoreBf16AddPartial, out, N, H, H)) return cudaErrorInvalidValue;
   EpiStore::Params p{mode == kAddF32 ? static_cast<const float*>(out) : partial, H, N, H, mode};
   // 256-row tiles: the K loop runs over the whole vocabulary chunk, so the
-  // accumulator overlap of 128-row tiles matters little and W is streamed half as often
-  return launch_any<false, true, EpiStore, 2>(ta, tb, tc, N, H, Vc, p, status, stream, VP_GROUP_ROWS_DX);
+  // accumulator overlap of 128-row tiles matters little and W is streamed half as often.
+  // Stream-K (with sk_ws) when the tiles leave the last wave of the grid part empty.
+  StreamK sk;
+  if (kernels) *kernels = 1;
+  cudaError_t e = launch_any<false, true, EpiStore, 2>(ta, tb, tc, N, H, Vc, p, status, stream, VP_GROUP_ROWS_DX,
+                                                       sk_ws, &sk);
+  if (e != cudaSuccess || sk.iters == 0) return e;
+  if (kernels) *kernels = 2;
+  TileSched sched;
+  sched.num_m = static_cast<int>((N + 2 * kBM - 1) / (2 * kBM));
+  sched.num_n = static_cast<int>((H + kBN - 1) / kBN);
+  const int group_m = VP_GROUP_ROWS_DX / (2 * kBM);
+  sched.group_m = group_m < 1 ? 1 : group_m;
+  sk_fixup_kernel<<<static_cast<unsigned>(sk.grid - 1), 256, 0, stream>>>(
+      sk.ws, sk.iters, sk.grid, static_cast<int>((Vc + kBK - 1) / kBK), sched, 2 * kBM, out,
+      mode == kAddF32 ? static_cast<const float*>(out) : partial, H, N, H, mode);
+  return cudaGetLastError();
 }
 
 cudaError_t bf16_dw_chunk(const void* dz, int64_t ldz, const void* X, int64_t N, int64_t H, int64_t c0,
@@ -623,6 +796,30 @@ cudaError_t bf16_dw_chunk(const void* dz, int64_t ldz, const void* X, int64_t N,
   if (!make_store_tmap(&tc, false, out, Vc, H, H)) return cudaErrorInvalidValue;
   EpiStore::Params p{accumulate ? out : nullptr, H, Vc, H, accumulate ? kAddF32 : kStoreF32};
   return launch_any<true, true, EpiStore>(ta, tb, tc, Vc, H, N, p, status, stream, VP_GROUP_ROWS_DW);
+}
+
+cudaError_t transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out, int64_t ld_out,
+                           cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
+  transpose_bf16_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(in), rows, cols, ld_in,
+                                                  static_cast<uint16_t*>(out), ld_out);
+  return cudaGetLastError();
+}
+
+cudaError_t bf16_dwt_chunk(const void* Xt, int64_t ldxt, const void* dz, int64_t ldz, int64_t N, int64_t H,
+                           int64_t c0, int64_t Vc, float* dW, bool accumulate, uint32_t* status, cudaStream_t stream) {
+  if (g_variant == 2)   // the direct form, dW = dZ^T X with both operands MN-major (for comparison)
+    return cudaErrorNotSupported;
+  // dW_c^T[H, Vc] = X^T[H, N] dZ_c[N, Vc]: A = X^T (K-major, K = tokens), B = dZ_c viewed as
+  // [K = N rows][N = Vc cols] (MN-major); the epilogue stores each block transposed into dW.
+  CUtensorMap ta, tb, tc;
+  if (!make_tmap_bf16(&ta, Xt, H, N, ldxt, kBK, kBM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, dz, N, Vc, ldz, 64, kBK)) return cudaErrorInvalidValue;
+  float* out = dW + c0 * H;
+  if (!make_store_tmap(&tc, false, out, Vc, H, H)) return cudaErrorInvalidValue;
+  EpiStoreT::Params p{out, H, Vc, H, accumulate ? 1 : 0};
+  // all of H's row blocks per group: consecutive tiles share one dZ column block in L2
+  return launch_any<false, true, EpiStoreT>(ta, tb, tc, H, Vc, N, p, status, stream, static_cast<int>(H));
 }
 
 // Plain GEMM entry used by the unit tests of the core: D[M,N] = A * B^T with

@@ -92,6 +92,28 @@ __device__ __forceinline__ void stage_and_store(EpiCtx& ctx, const CUtensorMap* 
   ctx.buf ^= 1;
 }
 
+// Thread `lane` holds column `lane` of a 32 x 32 fp32 block (w[j] = row j):
+// write the block row-major into the warp's staging box in the 128-byte
+// swizzled order TMA expects (for each row, 32 lanes hit 32 banks), then one
+// lane stores the 32-row box at (c0, c1).  All 32 lanes call it.
+__device__ __forceinline__ void stage_transposed_and_store(EpiCtx& ctx, const CUtensorMap* tm, const uint32_t (&w)[32],
+                                                           int32_t c0, int32_t c1) {
+  uint8_t* box = ctx.stg + ctx.buf * kStoreBoxBytes;
+  if (ctx.lane == 0) bulk_wait_group_read<1>();   // the store that last used this box has read it
+  __syncwarp();
+  const int chunk = ctx.lane >> 2, within = (ctx.lane & 3) * 4;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    *reinterpret_cast<uint32_t*>(box + j * 128 + ((chunk ^ (j & 7)) << 4) + within) = w[j];
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (ctx.lane == 0) {
+    tma_store_2d(tm, box, c0, c1);
+    bulk_commit_group();
+  }
+  ctx.buf ^= 1;
+}
+
 struct TileSched {
   int num_m, num_n, group_m;
   // Tile id -> (m block, n block): ids run down groups of `group_m` m-blocks
@@ -117,17 +139,86 @@ struct GemmArgs {
   uint32_t* status;    // device status word (VP_DEV_* bits)
   uint64_t wait_ns;    // limit of every mbarrier wait
   int hold;            // GemmHold (kHoldNone outside diagnostics)
+  int64_t sk_iters;    // > 0: stream-K over tiles x num_k (tile, k-block) iterations; 0: whole tiles
 };
+
+// First stream-K iteration of CTA c out of G: floor(c * I / G), without
+// forming the product c * I.
+__host__ __device__ __forceinline__ int64_t sk_begin(int64_t c, int64_t G, int64_t I) {
+  return c * (I / G) + (c * (I % G)) / G;
+}
+
+// A CTA's share of a launch, one piece at a time: the k-blocks [kb0, kb1) of
+// one tile.  Whole tiles (blockIdx.x, + gridDim.x, ...) by default; with
+// stream-K the contiguous iteration range [sk_begin(c), sk_begin(c + 1)) cut
+// at tile edges, so every CTA gets the same number of k-blocks whatever the
+// tile count.  A piece that is not a whole tile goes to partial slot 2c (the
+// CTA's first piece) or 2c + 1 (its last); a fix-up pass adds the slots of a
+// tile in CTA order, which is k order.
+struct Piece {
+  int tile, kb0, kb1, slot;   // slot -1: a whole tile
+};
+struct WorkIter {
+  int64_t i, hi, first_tile;
+  int tile, step, total, num_k, cta;
+  bool sk;
+  __device__ WorkIter(const GemmArgs& a, int total_tiles, bool none) {
+    total = none ? 0 : total_tiles;
+    num_k = a.num_k;
+    cta = static_cast<int>(blockIdx.x);
+    step = static_cast<int>(gridDim.x);
+    tile = cta;
+    sk = a.sk_iters > 0;
+    i = sk ? sk_begin(cta, step, a.sk_iters) : 0;
+    hi = (sk && !none) ? sk_begin(cta + 1, step, a.sk_iters) : 0;
+    first_tile = i / num_k;
+  }
+  __device__ __forceinline__ bool next(Piece& p) {
+    if (!sk) {
+      if (tile >= total) return false;
+      p.tile = tile;
+      p.kb0 = 0;
+      p.kb1 = num_k;
+      p.slot = -1;
+      tile += step;
+      return true;
+    }
+    if (i >= hi) return false;
+    const int64_t t = i / num_k;
+    p.tile = static_cast<int>(t);
+    p.kb0 = static_cast<int>(i - t * num_k);
+    p.kb1 = static_cast<int>(min(static_cast<int64_t>(num_k), p.kb0 + (hi - i)));
+    p.slot = (p.kb0 == 0 && p.kb1 == num_k) ? -1 : (t == first_tile ? 2 * cta : 2 * cta + 1);
+    i += p.kb1 - p.kb0;
+    return true;
+  }
+};
+
+// A stream-K partial piece: this thread's accumulator row (256 fp32 columns)
+// into the partial workspace row `row` through TMA (32-column boxes).
+__device__ __forceinline__ void store_partial_f32(EpiCtx& ctx, const CUtensorMap* tm, uint32_t taddr) {
+#pragma unroll 1
+  for (int b = 0; b < kBN / 32; ++b) {
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld32(taddr + b * 32, r);
+    tmem_ld_wait();
+    stage_and_store(ctx, tm, r, b * 32);
+  }
+}
 
 __device__ __forceinline__ void record_failure(uint32_t* status, volatile int* abort, uint32_t bit) {
   *abort = 1;
   if (status) atomicOr(status, bit);
 }
 
+// tmP: the fp32 partial workspace of stream-K launches, rows of 256 columns,
+// slot s at row s * kMB * 128 (unused when args.sk_iters == 0).
 template <bool A_MN, bool B_MN, class Epi, int kMB = 1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const GemmArgs args, const typename Epi::Params ep) {
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
+                     const GemmArgs args, const typename Epi::Params ep) {
   using S = GemmShape<kMB>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
@@ -164,6 +255,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (Epi::kStagingBytes) tma_prefetch_desc(&tmC);
+    if (Epi::kStagingBytes && args.sk_iters > 0) tma_prefetch_desc(&tmP);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -181,12 +273,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;   // bit s: stage s has a load in flight / its parity
-      const int first_tile = args.hold == kHoldProducer ? total : static_cast<int>(blockIdx.x);
-      for (int tile = first_tile; tile < total; tile += gridDim.x) {
+      WorkIter it(args, total, args.hold == kHoldProducer);
+      Piece pc;
+      while (it.next(pc)) {
         int mb, nb;
-        args.sched.tile(tile, mb, nb);
+        args.sched.tile(pc.tile, mb, nb);
         bool ok = true;
-        for (int kb = 0; kb < args.num_k; ++kb) {
+        for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort, args.wait_ns)) {
             record_failure(args.status, abort, 0x1u);
             ok = false;
@@ -234,8 +327,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      const int first_tile = args.hold == kHoldMma ? total : static_cast<int>(blockIdx.x);
-      for (int tile = first_tile; tile < total; tile += gridDim.x) {
+      WorkIter it(args, total, args.hold == kHoldMma);
+      Piece pc;
+      while (it.next(pc)) {
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort, args.wait_ns)) {
           record_failure(args.status, abort, 0x2u);
           break;
@@ -244,7 +338,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // accumulator set acc: kMB x 256 columns (acc is always 0 when kMB = 2)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kMB * kBN);
         bool ok = true;
-        for (int kb = 0; kb < args.num_k; ++kb) {
+        for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort, args.wait_ns)) {
             record_failure(args.status, abort, 0x2u);
             ok = false;
@@ -262,7 +356,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const uint32_t ah = a0 + h * kABytes;
               const uint64_t ad = A_MN ? sdesc_sw128(ah + kk * 2048, kMnBoxBytes, 1024)
                                        : sdesc_sw128(ah + kk * 32, 16, 1024);
-              umma_bf16(d_tmem + h * kBN, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma_bf16(d_tmem + h * kBN, ad, bd, idesc, (kb != pc.kb0 || kk != 0) ? 1u : 0u);
             }
           }
           umma_commit(&empty[stage]);
@@ -288,9 +382,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     EpiCtx ctx{sC + (warp - 2) * 2 * kStoreBoxBytes, 0, lane, 0};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    WorkIter it(args, total, false);
+    Piece pc;
+    while (it.next(pc)) {
       int mb, nb;
-      args.sched.tile(tile, mb, nb);
+      args.sched.tile(pc.tile, mb, nb);
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, args.wait_ns));
       if (!ok) {
         if (lane == 0) record_failure(args.status, abort, 0x4u);
@@ -301,8 +397,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int h = 0; h < kMB; ++h) {
         const uint32_t taddr = tmem_base + static_cast<uint32_t>((acc * kMB + h) * kBN) +
                                (static_cast<uint32_t>(quad * 32) << 16);
-        ctx.row0 = static_cast<int64_t>(mb * kMB + h) * kBM + quad * 32;
-        Epi::run(ep, &tmC, taddr, ctx.row0 + lane, nb, ctx);
+        if (pc.slot < 0) {
+          ctx.row0 = static_cast<int64_t>(mb * kMB + h) * kBM + quad * 32;
+          Epi::run(ep, &tmC, taddr, ctx.row0 + lane, nb, ctx);
+        } else if constexpr (Epi::kStagingBytes > 0) {
+          ctx.row0 = static_cast<int64_t>(pc.slot * kMB + h) * kBM + quad * 32;
+          store_partial_f32(ctx, &tmP, taddr);
+        }
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);

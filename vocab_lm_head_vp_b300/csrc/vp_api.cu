@@ -32,8 +32,8 @@ namespace {
 
 // ---------------- backward workspace: header | g | dZ chunk | dX fp32 partial (bf16, >1 chunk)
 struct BwdLayout {
-  int64_t Vc, ldz;
-  size_t off_g, off_dz, off_acc, total;
+  int64_t Vc, ldz, ldxt;
+  size_t off_g, off_dz, off_acc, off_sk, off_xt, total;
 };
 int bwd_tile(vp_dtype dt) { return dt == VP_BF16 ? kBf16TileV : kF32TileV; }
 BwdLayout bwd_layout_for_chunk(int64_t N, int64_t H, int64_t V, vp_dtype dt, int64_t Vc) {
@@ -44,7 +44,10 @@ BwdLayout bwd_layout_for_chunk(int64_t N, int64_t H, int64_t V, vp_dtype dt, int
   L.off_dz = align_up(L.off_g + size_t(N) * sizeof(float), kAlign);
   L.off_acc = align_up(L.off_dz + size_t(N) * L.ldz * esize_of(dt), kAlign);
   const bool need_acc = dt == VP_BF16 && Vc < V;
-  L.total = align_up(L.off_acc + (need_acc ? size_t(N) * H * sizeof(float) : 0), kAlign);
+  L.off_sk = align_up(L.off_acc + (need_acc ? size_t(N) * H * sizeof(float) : 0), kAlign);
+  L.off_xt = align_up(L.off_sk + (dt == VP_BF16 ? sk_workspace_bytes() : 0), kAlign);
+  L.ldxt = (N + 7) / 8 * 8;   // X^T [H][ldxt] bf16, for the dW GEMMs
+  L.total = align_up(L.off_xt + (dt == VP_BF16 ? size_t(H) * L.ldxt * 2 : 0), kAlign);
   return L;
 }
 // Largest chunk that fits in ws bytes (0 if none does).
@@ -62,11 +65,11 @@ int64_t bwd_chunk_from_ws(int64_t N, int64_t H, int64_t V, vp_dtype dt, size_t w
 // ---------------- fused workspace (bf16), token chunk Nc:
 // header | g [N] | records [ntiles*maxseg][Nc] | z_y [Nc] | tmax [ntiles][Nc] | P, then dZ, [Nc][ldp] 2-byte
 struct FusedLayout {
-  int64_t Nc, ldp, ntiles;
+  int64_t Nc, ldp, ntiles, ldxt;
   int maxseg;
-  size_t off_g, off_partial, off_zy, off_tmax, off_p, total;
+  size_t off_g, off_partial, off_zy, off_tmax, off_p, off_sk, off_xt, total;
 };
-FusedLayout fused_layout(int64_t N, int64_t V, int T, int64_t Nc) {
+FusedLayout fused_layout(int64_t N, int64_t H, int64_t V, int T, int64_t Nc) {
   FusedLayout L;
   L.Nc = Nc;
   L.ldp = (V + 7) / 8 * 8;
@@ -77,7 +80,10 @@ FusedLayout fused_layout(int64_t N, int64_t V, int T, int64_t Nc) {
   L.off_zy = align_up(L.off_partial + size_t(L.ntiles) * L.maxseg * Nc * sizeof(float2), kAlign);
   L.off_tmax = align_up(L.off_zy + size_t(Nc) * sizeof(float), kAlign);
   L.off_p = align_up(L.off_tmax + size_t(L.ntiles) * Nc * sizeof(float), kAlign);
-  L.total = align_up(L.off_p + size_t(Nc) * L.ldp * 2, kAlign);
+  L.off_sk = align_up(L.off_p + size_t(Nc) * L.ldp * 2, kAlign);
+  L.off_xt = align_up(L.off_sk + sk_workspace_bytes(), kAlign);
+  L.ldxt = (Nc + 7) / 8 * 8;   // X_c^T [H][ldxt] bf16, for the dW GEMMs
+  L.total = align_up(L.off_xt + size_t(H) * L.ldxt * 2, kAlign);
   return L;
 }
 constexpr int64_t kFusedRowAlign = 128;   // token chunks are whole 128-row GEMM blocks
@@ -94,29 +100,16 @@ int64_t fused_default_chunk(int64_t N, int64_t V) {
   return nc >= N ? N : nc;
 }
 
-// Token chunk of the fused call for at most nc_max rows per chunk.  Each
-// chunk's dX GEMM runs ceil(rows/128) * ceil(H/256) tiles on the persistent
-// grid, so equal chunks can leave a mostly idle last wave in every chunk:
-// among chunk sizes from nc_max down to half of it, take the one with the
-// fewest dX waves over all chunks, then the fewest chunks (each chunk after
-// the first adds an fp32 read-modify-write of dW).
-int64_t balanced_token_chunk(int64_t N, int64_t H, int64_t nc_max) {
+// Token chunk of the fused call for at most nc_max rows per chunk: the fewest
+// chunks (each chunk after the first adds an fp32 read-modify-write of dW),
+// as equal as the 128-row blocks allow, so that no chunk is a sliver.  The
+// dX GEMM's stream-K schedule keeps every chunk's tiles spread evenly over
+// the SMs whatever their count.
+int64_t balanced_token_chunk(int64_t N, int64_t nc_max) {
   if (nc_max >= N) return N;
-  const int64_t cols = (H + 255) / 256;
-  const int64_t sms = gemm_sm_count();
-  const auto waves = [&](int64_t rows) { return ((rows + 127) / 128 * cols + sms - 1) / sms; };
-  const int64_t mmax = nc_max / kFusedRowAlign;
-  int64_t best = mmax, best_w = -1, best_k = -1;
-  for (int64_t m = mmax; m >= 1 && 2 * m >= mmax; --m) {
-    const int64_t nc = m * kFusedRowAlign, k = (N + nc - 1) / nc;
-    const int64_t w = (k - 1) * waves(nc) + waves(N - (k - 1) * nc);
-    if (best_w < 0 || w < best_w || (w == best_w && k < best_k)) {
-      best = m;
-      best_w = w;
-      best_k = k;
-    }
-  }
-  return best * kFusedRowAlign;
+  const int64_t k = (N + nc_max - 1) / nc_max;
+  const int64_t nc = ((N + k - 1) / k + kFusedRowAlign - 1) / kFusedRowAlign * kFusedRowAlign;
+  return nc < nc_max ? nc : nc_max;
 }
 
 // Vocab chunk of the split backward for at most vc_max ids per chunk: the
@@ -136,14 +129,14 @@ int64_t bwd_default_chunk(int64_t V, int T, vp_dtype dt) {
   return vc >= V ? V : vc;
 }
 // Largest token chunk that fits in ws bytes: all N, else a multiple of 128 (0 if none fits).
-int64_t fused_chunk_from_ws(int64_t N, int64_t V, int T, size_t ws) {
-  if (fused_layout(N, V, T, N).total <= ws) return N;
-  const size_t per_row = fused_layout(N, V, T, 2).total - fused_layout(N, V, T, 1).total;
-  const size_t fixed = fused_layout(N, V, T, 0).total;
+int64_t fused_chunk_from_ws(int64_t N, int64_t H, int64_t V, int T, size_t ws) {
+  if (fused_layout(N, H, V, T, N).total <= ws) return N;
+  const size_t per_row = fused_layout(N, H, V, T, 2).total - fused_layout(N, H, V, T, 1).total;
+  const size_t fixed = fused_layout(N, H, V, T, 0).total;
   if (ws < fixed || per_row == 0) return 0;
   int64_t nc = int64_t((ws - fixed) / per_row) / kFusedRowAlign * kFusedRowAlign;
   if (nc >= N) nc = (N - 1) / kFusedRowAlign * kFusedRowAlign;
-  while (nc >= kFusedRowAlign && fused_layout(N, V, T, nc).total > ws) nc -= kFusedRowAlign;
+  while (nc >= kFusedRowAlign && fused_layout(N, H, V, T, nc).total > ws) nc -= kFusedRowAlign;
   return nc >= kFusedRowAlign ? nc : 0;
 }
 
@@ -153,12 +146,12 @@ constexpr int kMergeKernels = 2;   // lse_merge: the per-shard pass, then the pe
 
 // ---------------- optional per-launch event timing (vp_stage_timing_enable)
 enum Stage {
-  kEmbed, kLseGemm, kMerge, kMean, kScale, kDzGemm, kDwGemm, kDxGemm, kLsePGemm, kDzFromP, kEmbedBwd,
+  kEmbed, kLseGemm, kMerge, kMean, kScale, kDzGemm, kDwGemm, kDxGemm, kLsePGemm, kDzFromP, kEmbedBwd, kXT,
   kNumStages
 };
 const char* const kStageNames[kNumStages] = {"embed_gather",   "lse_stats_gemm",    "lse_merge", "loss_mean",
                                              "upstream_scale", "dz_recompute_gemm", "dw_gemm",   "dx_gemm",
-                                             "lse_p_gemm",     "dz_from_p",         "embed_bwd"};
+                                             "lse_p_gemm",     "dz_from_p",         "embed_bwd", "x_transpose"};
 struct StageTimer {
   int cap = 0, used = 0;
   int dropped = 0;            // timed regions past `cap`, not recorded
@@ -167,8 +160,10 @@ struct StageTimer {
   int* kernels = nullptr;   // kernels launched inside each timed region
 } g_timer;
 
+// kernels_after: where the launch leaves the number of kernels it launched
+// (read after it returns), for launches whose count depends on the shapes.
 template <class F>
-cudaError_t timed(Stage st, cudaStream_t s, F&& launch, int kernels = 1) {
+cudaError_t timed(Stage st, cudaStream_t s, F&& launch, int kernels = 1, const int* kernels_after = nullptr) {
   int slot = -1;
   if (g_timer.cap > 0 && g_timer.used >= g_timer.cap) ++g_timer.dropped;
   if (g_timer.cap > 0 && g_timer.used < g_timer.cap) {
@@ -178,8 +173,19 @@ cudaError_t timed(Stage st, cudaStream_t s, F&& launch, int kernels = 1) {
     cudaEventRecord(g_timer.ev[2 * slot], s);
   }
   cudaError_t e = launch();
-  if (slot >= 0) cudaEventRecord(g_timer.ev[2 * slot + 1], s);
+  if (slot >= 0) {
+    if (kernels_after) g_timer.kernels[slot] = *kernels_after;
+    cudaEventRecord(g_timer.ev[2 * slot + 1], s);
+  }
   return e;
+}
+
+// dW_c (+)= dZ_c^T X: through X^T (transposed once into `xt` by the caller)
+// when the GEMM form allows, else directly.
+cudaError_t dw_gemm(const void* dz, int64_t ldz, const void* X, const void* xt, int64_t ldxt, int64_t N, int64_t H,
+                    int64_t c0, int64_t Vc, float* dW, bool accumulate, uint32_t* status, cudaStream_t s) {
+  if (dw_through_xt()) return bf16_dwt_chunk(xt, ldxt, dz, ldz, N, H, c0, Vc, dW, accumulate, status, s);
+  return bf16_dw_chunk(dz, ldz, X, N, H, c0, Vc, dW, accumulate, status, s);
 }
 
 }  // namespace
@@ -257,9 +263,9 @@ VP_EXPORT size_t vp_lmhead_ce_workspace_size(int64_t N, int64_t H, int64_t V, in
       if (nc < kFusedRowAlign) nc = kFusedRowAlign;
     }
     if (nc > N) nc = N;
-    return fused_layout(N, V, T, nc).total;
+    return fused_layout(N, H, V, T, nc).total;
   }
-  if (pass == 3 && dtype == VP_BF16) return fused_layout(N, V, T, N).total;   // kept forward state, all N
+  if (pass == 3 && dtype == VP_BF16) return fused_layout(N, H, V, T, N).total;   // kept forward state, all N
   if (pass == 2 || pass == 3) {   // fp32: the forward, then the recompute backward in the same bytes
     const size_t f = fwd_layout(N, V, T, dtype).total;
     const size_t b = vp_lmhead_ce_workspace_size(N, H, V, T, dtype, 1, chunk);
@@ -335,9 +341,13 @@ VP_EXPORT vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t
   float* g = reinterpret_cast<float*>(ws + L.off_g);
   void* dz = ws + L.off_dz;
   float* acc = reinterpret_cast<float*>(ws + L.off_acc);
+  float* skw = reinterpret_cast<float*>(ws + L.off_sk);
+  void* xt = ws + L.off_xt;
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess)
     e = timed(kScale, s, [&] { return upstream_scale(targets, dloss, dmean, N, V, ignore_index, g, s); });
+  if (e == cudaSuccess && dtype == VP_BF16 && dw_through_xt())
+    e = timed(kXT, s, [&] { return transpose_bf16(X, N, H, H, xt, L.ldxt, s); });
   const bool single = Vc >= V;
   for (int64_t c0 = 0; c0 < V && e == cudaSuccess; c0 += Vc) {
     const int64_t vc = (V - c0) < Vc ? (V - c0) : Vc;
@@ -345,14 +355,16 @@ VP_EXPORT vp_status vp_lmhead_ce_bwd(const void* X, const void* W, const int64_t
     if (dtype == VP_BF16) {
       e = timed(kDzGemm, s, [&] { return bf16_dz_chunk(X, W, targets, lse, g, N, H, c0, vc, dz, L.ldz, status, s); });
       if (e == cudaSuccess)
-        e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(dz, L.ldz, X, N, H, c0, vc, dW, false, status, s); });
+        e = timed(kDwGemm, s,
+                  [&] { return dw_gemm(dz, L.ldz, X, xt, L.ldxt, N, H, c0, vc, dW, false, status, s); });
       if (e == cudaSuccess) {
         // dX over chunks: bf16 store (one chunk), else fp32 store / fp32 add / bf16 = fp32 partial + last
         void* out = (single || last) ? dX : static_cast<void*>(acc);
         const int mode = single ? 3 : first ? 0 : !last ? 1 : 2;
+        int nk = 1;
         e = timed(kDxGemm, s, [&] {
-          return bf16_dx_chunk(dz, L.ldz, W, N, H, c0, vc, out, mode == 2 ? acc : nullptr, mode, status, s);
-        });
+          return bf16_dx_chunk(dz, L.ldz, W, N, H, c0, vc, out, mode == 2 ? acc : nullptr, mode, status, s, skw, &nk);
+        }, 1, &nk);
       }
     } else {
       const float* Xf = static_cast<const float*>(X);
@@ -391,11 +403,11 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int
     return vp_lmhead_ce_bwd(X, W, targets, lse, dloss, dmean, N, H, V, T, ignore_index, dtype, dX, dW, workspace,
                             ws_bytes, stream);
   }
-  const int64_t Nc_max = fused_chunk_from_ws(N, V, T, ws_bytes);
+  const int64_t Nc_max = fused_chunk_from_ws(N, H, V, T, ws_bytes);
   if (Nc_max <= 0) return VP_ERR_WORKSPACE;
-  const int64_t Nc = balanced_token_chunk(N, H, Nc_max);
+  const int64_t Nc = balanced_token_chunk(N, Nc_max);
   if (!tensor_map_encoder()) return VP_ERR_CUDA;
-  const FusedLayout L = fused_layout(N, V, T, Nc);
+  const FusedLayout L = fused_layout(N, H, V, T, Nc);
   cudaStream_t s = as_stream(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
@@ -404,6 +416,8 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int
   float* zy = reinterpret_cast<float*>(ws + L.off_zy);
   float* tmax = reinterpret_cast<float*>(ws + L.off_tmax);
   void* P = ws + L.off_p;
+  float* skw = reinterpret_cast<float*>(ws + L.off_sk);
+  void* xt = ws + L.off_xt;
   const int64_t Vs = V / T;
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess)
@@ -425,9 +439,16 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int
     if (e == cudaSuccess)
       e = timed(kDzFromP, s, [&] { return dz_from_p(P, L.ldp, tmax, lse + n0, g + n0, yc, nc, V, s); });
     if (e == cudaSuccess)
-      e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(P, L.ldp, Xc, nc, H, 0, V, dW, n0 > 0, status, s); });
+      e = timed(kXT, s, [&] { return dw_through_xt() ? transpose_bf16(Xc, nc, H, H, xt, L.ldxt, s) : cudaSuccess; },
+                dw_through_xt() ? 1 : 0);
     if (e == cudaSuccess)
-      e = timed(kDxGemm, s, [&] { return bf16_dx_chunk(P, L.ldp, W, nc, H, 0, V, dXc, nullptr, 3, status, s); });
+      e = timed(kDwGemm, s,
+                [&] { return dw_gemm(P, L.ldp, Xc, xt, L.ldxt, nc, H, 0, V, dW, n0 > 0, status, s); });
+    int nk = 1;
+    if (e == cudaSuccess)
+      e = timed(kDxGemm, s, [&] {
+        return bf16_dx_chunk(P, L.ldp, W, nc, H, 0, V, dXc, nullptr, 3, status, s, skw, &nk);
+      }, 1, &nk);
   }
   if (e == cudaSuccess && (loss_mean || n_bad))
     e = timed(kMean, s, [&] { return loss_mean_and_bad(loss, targets, N, V, ignore_index, loss_mean, n_bad, s); });
@@ -444,7 +465,7 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_keep(const void* X, const void* W, const in
   if (dtype == VP_F32)   // fp32: nothing is kept; the backward recomputes in the same bytes
     return vp_lmhead_ce_fwd(X, W, targets, N, H, V, T, ignore_index, dtype, loss, lse, loss_mean, shard_stats, n_bad,
                             saved, saved_bytes, stream);
-  const FusedLayout L = fused_layout(N, V, T, N);
+  const FusedLayout L = fused_layout(N, H, V, T, N);
   if (saved_bytes < L.total) return VP_ERR_WORKSPACE;
   if (!tensor_map_encoder()) return VP_ERR_CUDA;
   cudaStream_t s = as_stream(stream);
@@ -481,7 +502,7 @@ VP_EXPORT vp_status vp_lmhead_ce_bwd_saved(const void* X, const void* W, const i
   if (dtype == VP_F32)
     return vp_lmhead_ce_bwd(X, W, targets, lse, dloss, dmean, N, H, V, T, ignore_index, dtype, dX, dW, saved,
                             saved_bytes, stream);
-  const FusedLayout L = fused_layout(N, V, T, N);
+  const FusedLayout L = fused_layout(N, H, V, T, N);
   if (saved_bytes < L.total) return VP_ERR_WORKSPACE;
   if (!tensor_map_encoder()) return VP_ERR_CUDA;
   cudaStream_t s = as_stream(stream);
@@ -490,15 +511,21 @@ VP_EXPORT vp_status vp_lmhead_ce_bwd_saved(const void* X, const void* W, const i
   float* g = reinterpret_cast<float*>(ws + L.off_g);
   float* tmax = reinterpret_cast<float*>(ws + L.off_tmax);
   void* P = ws + L.off_p;
+  float* skw = reinterpret_cast<float*>(ws + L.off_sk);
+  void* xt = ws + L.off_xt;
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess)
     e = timed(kScale, s, [&] { return upstream_scale(targets, dloss, dmean, N, V, ignore_index, g, s); });
   // p becomes dZ in place, scaled per row and tile by c = g exp(tmax - lse) from the kept tile maxima
   if (e == cudaSuccess) e = timed(kDzFromP, s, [&] { return dz_from_p(P, L.ldp, tmax, lse, g, targets, N, V, s); });
+  if (e == cudaSuccess && dw_through_xt())
+    e = timed(kXT, s, [&] { return transpose_bf16(X, N, H, H, xt, L.ldxt, s); });
   if (e == cudaSuccess)
-    e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(P, L.ldp, X, N, H, 0, V, dW, false, status, s); });
+    e = timed(kDwGemm, s, [&] { return dw_gemm(P, L.ldp, X, xt, L.ldxt, N, H, 0, V, dW, false, status, s); });
+  int nk = 1;
   if (e == cudaSuccess)
-    e = timed(kDxGemm, s, [&] { return bf16_dx_chunk(P, L.ldp, W, N, H, 0, V, dX, nullptr, 3, status, s); });
+    e = timed(kDxGemm, s, [&] { return bf16_dx_chunk(P, L.ldp, W, N, H, 0, V, dX, nullptr, 3, status, s, skw, &nk); },
+              1, &nk);
   return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
 }
 
@@ -573,10 +600,14 @@ VP_EXPORT vp_status vp_lmhead_ce_shard_bwd(const void* X, const void* W_t, const
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   float* g = reinterpret_cast<float*>(ws + L.off_g);
   void* dz = ws + L.off_dz;
+  float* skw = reinterpret_cast<float*>(ws + L.off_sk);
+  void* xt = ws + L.off_xt;
   const int64_t start = static_cast<int64_t>(t) * Vs;
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess)   // validity against the whole vocabulary: every rank sees the same N_valid
     e = timed(kScale, s, [&] { return upstream_scale(targets, dloss, dmean, N, V, ignore_index, g, s); });
+  if (e == cudaSuccess && dtype == VP_BF16 && dw_through_xt())
+    e = timed(kXT, s, [&] { return transpose_bf16(X, N, H, H, xt, L.ldxt, s); });
   for (int64_t c0 = 0; c0 < Vs && e == cudaSuccess; c0 += Vc) {
     const int64_t vc = (Vs - c0) < Vc ? (Vs - c0) : Vc;
     const bool first = c0 == 0;
@@ -584,12 +615,15 @@ VP_EXPORT vp_status vp_lmhead_ce_shard_bwd(const void* X, const void* W_t, const
       e = timed(kDzGemm, s,
                 [&] { return bf16_dz_chunk(X, W_t, targets, lse, g, N, H, c0, vc, dz, L.ldz, status, s, start); });
       if (e == cudaSuccess)
-        e = timed(kDwGemm, s, [&] { return bf16_dw_chunk(dz, L.ldz, X, N, H, c0, vc, dW_t, false, status, s); });
+        e = timed(kDwGemm, s,
+                  [&] { return dw_gemm(dz, L.ldz, X, xt, L.ldxt, N, H, c0, vc, dW_t, false, status, s); });
       // this shard's part of dX in fp32: stored by the first chunk, added by the others
-      if (e == cudaSuccess)
+      if (e == cudaSuccess) {
+        int nk = 1;
         e = timed(kDxGemm, s, [&] {
-          return bf16_dx_chunk(dz, L.ldz, W_t, N, H, c0, vc, dX_t, nullptr, first ? 0 : 1, status, s);
-        });
+          return bf16_dx_chunk(dz, L.ldz, W_t, N, H, c0, vc, dX_t, nullptr, first ? 0 : 1, status, s, skw, &nk);
+        }, 1, &nk);
+      }
     } else {
       const float* Xf = static_cast<const float*>(X);
       const float* Wf = static_cast<const float*>(W_t);

@@ -26,8 +26,22 @@ cudaError_t bf16_lse_stats(const void* X, const void* W, const int64_t* targets,
 cudaError_t bf16_dz_chunk(const void* X, const void* W, const int64_t* targets, const float* lse, const float* g,
                           int64_t N, int64_t H, int64_t c0, int64_t Vc, void* dz, int64_t ldz, uint32_t* status,
                           cudaStream_t stream, int64_t y_off = 0);
+// sk_ws: sk_workspace_bytes() of fp32 scratch for stream-K partial tiles (the
+// launch splits the (tile, k-block) iterations evenly over the SMs when its
+// tiles do not fill whole waves); nullptr: whole tiles only.
 cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N, int64_t H, int64_t c0, int64_t Vc,
-                          void* out, const float* partial, int mode, uint32_t* status, cudaStream_t stream);
+                          void* out, const float* partial, int mode, uint32_t* status, cudaStream_t stream,
+                          float* sk_ws = nullptr, int* kernels = nullptr);
+size_t sk_workspace_bytes();
+// dW through X^T (A K-major): Xt = X^T [H][ldxt] bf16 (transpose_bf16 of X).
+// cudaErrorNotSupported under GEMM form 2 (callers then use bf16_dw_chunk).
+cudaError_t bf16_dwt_chunk(const void* Xt, int64_t ldxt, const void* dz, int64_t ldz, int64_t N, int64_t H,
+                           int64_t c0, int64_t Vc, float* dW, bool accumulate, uint32_t* status, cudaStream_t stream);
+// out[c][r] = in[r][c], bf16, cols a multiple of 8.
+cudaError_t transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out, int64_t ld_out,
+                           cudaStream_t stream);
+// Whether the dW GEMMs take the X^T form (GEMM forms 0 and 1).
+bool dw_through_xt();
 cudaError_t bf16_dw_chunk(const void* dz, int64_t ldz, const void* X, int64_t N, int64_t H, int64_t c0, int64_t Vc,
                           float* dW, bool accumulate, uint32_t* status, cudaStream_t stream);
 // Forward statistics plus p = exp(z - tile row max) in fp16 into P [N][ldp]
@@ -40,8 +54,6 @@ cudaError_t bf16_gemm_test(const void* A, const void* B, float* D, int64_t M, in
 // 0 (default): one SM per tile, dX in 256 x 256 tiles, the other GEMMs in
 // 128 x 256; 1: 2-SM CTA pairs (256 x 256 tiles); 2: one SM per 128 x 256 tile.
 void set_gemm_variant(int variant);
-// SMs of the current device (the persistent GEMMs' grid); 148 if the query fails.
-int gemm_sm_count();
 // Later one-SM GEMM launches: hold = 1 (the TMA producer issues no load) or
 // 2 (the MMA issuer issues no MMA), 0 = none; every mbarrier wait gives up
 // after wait_ns (0 = the default limit).
