@@ -87,29 +87,32 @@ def parse_args():
     return args
 
 
-# DRAM bytes (read + write) per launch of the tcgen05 GEMM kernel in the fused
-# v128k step, from one ncu capture (profiles/launches_fused_step_v128k.md: mean of
-# the three GEMM launches over four steps).  They describe the kernel built from the
-# sources hashed here; once those change, `traffic` is reported as null until a
-# new capture replaces the number.
-GEMM_TRAFFIC = {"workload": "v128k", "path": "fused", "gemm_variant": "single", "bytes_per_launch": 21.62e9,
-                "by_launch": {"lse_p_gemm": 8.76e9, "dw_gemm": 22.28e9, "dx_gemm": 33.82e9},
+# DRAM bytes (read + write) per GEMM stage (one 2NHV contraction, summed over
+# its token-chunk launches) of the tcgen05 GEMM kernel in the fused v128k step
+# with the default bounded workspace, from one ncu capture
+# (profiles/launches_fused_step_v128k.md: mean of the three stages over four
+# steps).  They describe the kernel built from the sources hashed here; once
+# those change, `traffic` is reported as null until a new capture replaces the
+# number.
+GEMM_TRAFFIC = {"workload": "v128k", "path": "fused", "gemm_variant": "single", "token_chunk": 0,
+                "bytes_per_stage": 20.57e9,
+                "by_stage": {"lse_p_gemm": 11.83e9, "dw_gemm": 23.94e9, "dx_gemm": 25.95e9},
                 "sources": ("vocab_lm_head_vp_b300/csrc/ce_bf16.cu", "vocab_lm_head_vp_b300/csrc/ptx.cuh",
                             "vocab_lm_head_vp_b300/csrc/umma_gemm.cuh"),
-                "sha256": "5c604a4df2e8c74a1eea2b195e22b14e876326a161e1d6df435713c485961e68"}
+                "sha256": "d44ff05879df578b05910ecd5946deeb200a795f1d084fed7c448b253fd020e9"}
 
 
-def gemm_traffic(workload, path, variant):
-    """ncu DRAM bytes per GEMM launch if they were taken on this kernel and step, else None."""
+def gemm_traffic(workload, path, variant, token_chunk):
+    """ncu DRAM bytes per GEMM stage if they were taken on this kernel and step, else None."""
     import hashlib
     t = GEMM_TRAFFIC
-    if (workload, path, variant) != (t["workload"], t["path"], t["gemm_variant"]):
+    if (workload, path, variant, token_chunk) != (t["workload"], t["path"], t["gemm_variant"], t["token_chunk"]):
         return None
     h = hashlib.sha256()
     for f in t["sources"]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
-    return t["bytes_per_launch"] if h.hexdigest() == t["sha256"] else None
+    return t["bytes_per_stage"] if h.hexdigest() == t["sha256"] else None
 
 
 def load_peaks():
@@ -359,25 +362,32 @@ def embed_bwd_microbench(vp, dev, iters=20):
     for kind, ids in (("zipf", synth.zipf_ids(rng, wl.N, wl.V, 1.1)), ("uniform", rng.integers(0, wl.V, wl.N))):
         idt = torch.from_numpy(ids).to(dev)
 
-        def loop(with_bwd):
+        def loop(what):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
             e0.record()
             for _ in range(iters):
                 flush.zero_()
-                if with_bwd:
+                if what == "call":
                     vp.embed_bwd(idt, G, wl.V, wl.T, dW=dW, accumulate=True, workspace=ws)
+                elif what == "planned":
+                    vp.embed_bwd_planned(ws, G, wl.V, wl.T, dW=dW, accumulate=True)
             e1.record()
             torch.cuda.synchronize()
             return e0.elapsed_time(e1)
 
-        loop(True)   # warm-up
-        both = [loop(True) for _ in range(3)]
-        alone = [loop(False) for _ in range(3)]
-        ms = (statistics.median(both) - statistics.median(alone)) / iters
+        loop("call")   # warm-up; leaves the plan of these ids in ws
+        call = [loop("call") for _ in range(3)]
+        planned = [loop("planned") for _ in range(3)]
+        alone = [loop(None) for _ in range(3)]
+        ms = (statistics.median(call) - statistics.median(alone)) / iters
+        ms_sums = (statistics.median(planned) - statistics.median(alone)) / iters
         distinct = len(np.unique(ids))
         nbytes = wl.N * wl.H * 2.0 + 8.0 * wl.N + 2.0 * distinct * wl.H * 4
-        out[kind] = {"ms": ms, "distinct_ids": distinct, "alg_bytes": nbytes, "GB/s": nbytes / (ms / 1e3) / 1e9}
+        out[kind] = {"ms": ms, "distinct_ids": distinct, "alg_bytes": nbytes, "GB/s": nbytes / (ms / 1e3) / 1e9,
+                     "sums_ms": ms_sums, "sums_GB/s": (nbytes - 8.0 * wl.N) / (ms_sums / 1e3) / 1e9,
+                     "note": "ms / GB/s: the whole vp_embed_bwd call (sort of the ids + sums); sums_*: "
+                             "vp_embed_bwd_planned alone, the sort done ahead by vp_embed_bwd_plan"}
     del G, dW, ws
     return out
 
@@ -696,7 +706,7 @@ def run_ours(args):
                      "peak_kind": f"bf16 burst ({peaks['source']})",
                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                      "peak_sustained": peaks["bf16_tflops_sustained"],
-                     "traffic": gemm_traffic(wl.name, args.path, args.gemm_variant),
+                     "traffic": gemm_traffic(wl.name, args.path, args.gemm_variant, args.token_chunk),
                      "launches_per_gemm_stage": gemm_launches_per_stage,
                      "traffic_unit": "bytes per GEMM stage (one 2NHV contraction; ncu dram read + write, "
                                      "summed over the stage's launches)",

@@ -137,6 +137,22 @@ vp_status vp_embed_bwd(const int64_t* ids, const void* dOut, float* dW,
                        int accumulate, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * vp_embed_bwd_plan / vp_embed_bwd_planned -- vp_embed_bwd in two steps.
+ * The grouping of the tokens by id (a sort of the (id, n) keys, latency-bound
+ * index work) needs only the ids, which a training step knows from its start;
+ * the sums need dOut.  vp_embed_bwd_plan sorts into `workspace`, for instance
+ * on a side stream while the LM head runs; vp_embed_bwd_planned, later, adds
+ * the rows into dW from that workspace (same N, H, V, T; the workspace left
+ * untouched in between).  Together they compute what vp_embed_bwd computes,
+ * bit for bit.  Arguments and errors as for vp_embed_bwd.
+ */
+vp_status vp_embed_bwd_plan(const int64_t* ids, int64_t N, int64_t H, int64_t V, int T,
+                            void* workspace, size_t ws_bytes, void* stream);
+vp_status vp_embed_bwd_planned(const void* dOut, float* dW, int64_t N, int64_t H, int64_t V, int T,
+                               vp_dtype dtype, int accumulate, void* workspace, size_t ws_bytes,
+                               void* stream);
+
+/*
  * vp_lmhead_ce_workspace_size -- bytes of device workspace for a call.
  *   pass 0: vp_lmhead_ce_fwd (exact size needed).
  *   pass 1: vp_lmhead_ce_bwd with the vocab processed in chunks of

@@ -116,8 +116,9 @@ def test_fused_workspace_sizes(lib):
     half = vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 8192)
     assert half - SK < (full - SK) / 2 + N * 8 and half - SK > (full - SK) / 2 - N * V - XT(N, H)
     assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 100) == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 128)
-    # default: saved probabilities of at most 1 GiB (4096 token rows of V = 128256)
-    assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 2) == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 4096)
+    # default: saved probabilities of at most 1.25 GiB, in the chunk that fills the dX GEMM's
+    # waves best (4736 token rows of V = 128256: 592 tiles of 128 x 256, four waves of 148)
+    assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 2) == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 4736)
     # small problems fit in one chunk by default
     assert vp.workspace_size(4096, 512, 6400, 2, vp.VP_BF16, 2) == vp.workspace_size(4096, 512, 6400, 2,
                                                                                         vp.VP_BF16, 2, 4096)

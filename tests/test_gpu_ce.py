@@ -316,9 +316,9 @@ def test_gemm_forms_agree_on_the_path(variant):
 
 @pytest.mark.parametrize("N,H,V,chunk,streamk", [
     (300, 264, 1800, 1800, False), (1100, 512, 3000, 3000, False), (77, 64, 700, 256, False),
-    (2560, 1024, 2000, 2000, True),      # 40 tiles of 256 x 256 over 148 SMs: every tile split over ~4 CTAs
     (2600, 1032, 6000, 1536, True),      # ragged rows and columns, four vocab chunks (fp32 store / add / bf16)
-    (2600, 1032, 2000, None, True),      # the default chunks (one shard each)
+    (768, 4096, 2000, 2000, True),       # 48 tiles of 256 x 256 for 148 SMs: each split over ~3 CTAs
+    (700, 4104, 12000, 2048, True),      # ragged, six vocab chunks through stream-K (fp32 store / add / bf16)
 ])
 def test_dx_tile_forms(N, H, V, chunk, streamk):
     """dX from 256 x 256 tiles (two 128-row accumulators sharing each B stage)

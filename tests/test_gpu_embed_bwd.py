@@ -63,12 +63,33 @@ CASES = [  # N, H, V, T, dtype, ids
     (300, 136, 1000, 8, "bf16", "uniform"),
     (300, 64, 50, 5, "bf16", "uniform"),          # ids repeat ~6 times: segments cross runs
     (1000, 256, 5000, 4, "bf16", "zipf"),         # id 0 spans many runs
-    (513, 64, 700, 2, "bf16", "uniform"),         # n_pad 1024: 2 sorted chunks, one rank placement
-    (4097, 64, 2048, 2, "bf16", "zipf"),          # n_pad 8192: 16 sorted chunks, one rank placement
-    (9000, 128, 4000, 8, "f32", "zipf"),          # n_pad 16384: 32 sorted chunks, one rank placement
+    (2049, 64, 700, 2, "bf16", "uniform"),        # n_pad 4096: 8 sorted chunks, one 8-way merge
+    (4097, 64, 2048, 2, "bf16", "zipf"),          # n_pad 8192: 16 sorted chunks, 8-way then 2-way merges
+    (9000, 128, 4000, 8, "f32", "zipf"),          # n_pad 16384: 32 sorted chunks, 8-way then 4-way merges
     (16384, 64, 128256, 8, "bf16", "uniform"),    # the V128k id count, uniform: mostly one token per id
     (20000, 64, 3000, 4, "bf16", "zipf"),         # n_pad 32768: 64 sorted chunks, two 8-way merges
+    (70000, 16, 9000, 3, "bf16", "zipf"),         # n_pad 131072: 256 sorted chunks, 8-, 8- and 4-way merges
 ]
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_plan_then_planned_equals_one_call(accumulate):
+    """vp_embed_bwd_plan on a side stream (the ids' sort, ahead of time), then
+    vp_embed_bwd_planned on the main stream: the same bits as vp_embed_bwd."""
+    rng = np.random.default_rng(8)
+    N, H, V, T = 9000, 256, 5000, 4
+    ids = torch.from_numpy(synth.zipf_ids(rng, N, V, 1.1)).cuda()
+    G = torch.from_numpy(rng.standard_normal((N, H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    D = torch.from_numpy(rng.standard_normal((V, H)).astype(np.float32)).cuda()
+    want = vp.embed_bwd(ids, G, V, T, dW=D.clone() if accumulate else None, accumulate=accumulate)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        plan = vp.embed_bwd_plan(ids, H, V, T)
+    torch.cuda.current_stream().wait_stream(side)
+    got = vp.embed_bwd_planned(plan, G, V, T, dW=D.clone() if accumulate else None, accumulate=accumulate)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
 
 
 @pytest.mark.parametrize("N,H,V,T,dtype,kind", CASES)

@@ -18,7 +18,7 @@ import os
 
 import torch
 
-__all__ = ["embed_fwd", "embed_fwd_sp", "embed_bwd", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce_fwd_bwd", "lmhead_ce",
+__all__ = ["embed_fwd", "embed_fwd_sp", "embed_bwd", "embed_bwd_plan", "embed_bwd_planned", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce_fwd_bwd", "lmhead_ce",
            "lmhead_ce_shard_fwd", "lmhead_ce_merge_stats", "lmhead_ce_shard_bwd", "vocab_parallel_lmhead_ce", "workspace_size", "read_device_status",
            "test_gemm_bf16", "set_gemm_variant", "set_wait_fault", "stage_timing_enable", "stage_timing_read", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
 
@@ -60,6 +60,10 @@ def _load():
     L.vp_embed_bwd_workspace_size.argtypes = [I64, I64, I64, I32, I32]
     L.vp_embed_bwd.restype = I32
     L.vp_embed_bwd.argtypes = [P, P, P, I64, I64, I64, I32, I32, I32, P, SZ, P]
+    L.vp_embed_bwd_plan.restype = I32
+    L.vp_embed_bwd_plan.argtypes = [P, I64, I64, I64, I32, P, SZ, P]
+    L.vp_embed_bwd_planned.restype = I32
+    L.vp_embed_bwd_planned.argtypes = [P, P, I64, I64, I64, I32, I32, I32, P, SZ, P]
     L.vp_lmhead_ce_workspace_size.restype = SZ
     L.vp_lmhead_ce_workspace_size.argtypes = [I64, I64, I64, I32, I32, I32, I64]
     L.vp_lmhead_ce_fwd.restype = I32
@@ -197,6 +201,38 @@ def embed_bwd(ids: torch.Tensor, dOut: torch.Tensor, V: int, T: int, dW: torch.T
     _check("vp_embed_bwd", L.vp_embed_bwd(_ptr(ids), _ptr(dOut), _ptr(dW), N, H, V, T, _dtype_code(dOut),
                                           int(bool(accumulate)), _ptr(ws), ws.numel() * ws.element_size(),
                                           _stream(dev)))
+    return dW
+
+
+def embed_bwd_plan(ids: torch.Tensor, H: int, V: int, T: int, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """The id-only step of embed_bwd (the tokens grouped by id) into a
+    workspace, for embed_bwd_planned later; returns the workspace."""
+    _need(ids, "ids", torch.int64)
+    N = ids.numel()
+    L = _load()
+    nb = int(L.vp_embed_bwd_workspace_size(N, H, V, T, VP_BF16))
+    if nb == 0:
+        raise VpError("vp_embed_bwd_workspace_size", 1)
+    ws = _workspace(nb, ids.device, workspace)
+    _check("vp_embed_bwd_plan", L.vp_embed_bwd_plan(_ptr(ids), N, H, V, T, _ptr(ws), ws.numel() * ws.element_size(),
+                                                    _stream(ids.device)))
+    return ws
+
+
+def embed_bwd_planned(plan: torch.Tensor, dOut: torch.Tensor, V: int, T: int, dW: torch.Tensor | None = None,
+                      accumulate: bool = False) -> torch.Tensor:
+    """The sums of embed_bwd over a workspace that embed_bwd_plan prepared."""
+    _need(dOut, "dOut")
+    N, H = dOut.shape
+    dev = dOut.device
+    if dW is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs dW")
+        dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    _need(dW, "dW", torch.float32, dev)
+    _check("vp_embed_bwd_planned", _load().vp_embed_bwd_planned(
+        _ptr(dOut), _ptr(dW), N, H, V, T, _dtype_code(dOut), int(bool(accumulate)), _ptr(plan),
+        plan.numel() * plan.element_size(), _stream(dev)))
     return dW
 
 

@@ -399,28 +399,56 @@ struct EpiStoreT {
   };
   __device__ static void run(const Params& p, const CUtensorMap* tm, uint32_t taddr, int64_t h, int nb,
                              EpiCtx& ctx) {
+    (void)h;
     const int64_t h0 = ctx.row0;   // this warp's first hidden index (warp-uniform)
     if (h0 >= p.H) return;
     const int64_t vbase = static_cast<int64_t>(nb) * kBN;
-    const bool hok = h < p.H;
+    const int lane = ctx.lane;
 #pragma unroll 1
     for (int b = 0; b < kBN / 32; ++b) {
       const int64_t v0 = vbase + b * 32;
       if (v0 >= p.V) break;   // uniform over the CTA
+      // accumulating: lane l fetches old row v0 + l, columns h0 .. h0+31, as 8
+      // 16-byte vectors (8 rows' lines in flight per load, like a row-major tile)
+      float4 old[8];
+      const int64_t vr = v0 + lane;
+      if (p.add) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          old[q] = (vr < p.V && h0 + 4 * q < p.H)
+                       ? *reinterpret_cast<const float4*>(p.out + vr * p.ld + h0 + 4 * q)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       uint32_t r[32];
       __syncwarp();
       tmem_ld32(taddr + b * 32, r);
       tmem_ld_wait();
+      // the 32 x 32 block transposed into the staging box (row = vocab row), the
+      // old values added row by row, then one TMA store; columns >= H and rows
+      // >= V are clipped by the tensor map
+      uint8_t* box = ctx.stg + ctx.buf * kStoreBoxBytes;
+      if (lane == 0) bulk_wait_group_read<1>();   // the store that last used this box has read it
+      __syncwarp();
+      const int chunk = lane >> 2, within = (lane & 3) * 4;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        *reinterpret_cast<uint32_t*>(box + j * 128 + ((chunk ^ (j & 7)) << 4) + within) = r[j];
       if (p.add) {
-        // old dW[v0 + j][h]: for each j the warp reads 32 consecutive floats
-        float old[32];
+        __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) old[j] = (hok && v0 + j < p.V) ? p.out[(v0 + j) * p.ld + h] : 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(as_f(r[j]) + old[j]);
+        for (int q = 0; q < 8; ++q) {
+          float4* cell = reinterpret_cast<float4*>(box + lane * 128 + ((q ^ (lane & 7)) << 4));
+          const float4 a = *cell;
+          *cell = make_float4(a.x + old[q].x, a.y + old[q].y, a.z + old[q].z, a.w + old[q].w);
+        }
       }
-      // columns >= H and rows >= V are clipped by the tensor map
-      stage_transposed_and_store(ctx, tm, r, static_cast<int32_t>(h0), static_cast<int32_t>(v0));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tm, box, static_cast<int32_t>(h0), static_cast<int32_t>(v0));
+        bulk_commit_group();
+      }
+      ctx.buf ^= 1;
     }
   }
 };
@@ -702,6 +730,30 @@ void set_gemm_variant(int variant) { g_variant = (variant == 1 || variant == 2) 
 
 bool dw_through_xt() { return g_variant != 2; }
 
+// Relative time of a dX launch over `rows` token rows in units of one wave of
+// 128 x 256 tiles: its waves on the persistent grid, a 256-row wave counting
+// twice, a 128-row wave 4% more than half of that (it streams W twice as
+// often per row).  The tile shape with the lower cost is taken.
+DxPlan dx_plan(int64_t rows, int64_t H) {
+  const int64_t G = sm_count(), cols = (H + kBN - 1) / kBN;
+  const auto waves = [&](int64_t tile_rows) { return ((rows + tile_rows - 1) / tile_rows * cols + G - 1) / G; };
+  const double c1 = 1.04 * static_cast<double>(waves(kBM)), c2 = 2.0 * static_cast<double>(waves(2 * kBM));
+  DxPlan p;
+  const bool two = g_variant != 2 && c2 <= c1;
+  p.rows = two ? 2 * kBM : kBM;
+  p.cost = two ? c2 : c1;
+  // fewer 256-row tiles than SMs, and whole waves would take over a third longer
+  // than the work: split the tiles over the SMs
+  const int64_t t2 = (rows + 2 * kBM - 1) / (2 * kBM) * cols;
+  const double ideal = static_cast<double>((rows + kBM - 1) / kBM * cols) / static_cast<double>(G);
+  p.streamk = g_variant != 2 && 4 * t2 >= G && t2 < G && ideal < 0.75 * p.cost;
+  if (p.streamk) {
+    p.rows = 2 * kBM;
+    p.cost = ideal;
+  }
+  return p;
+}
+
 size_t sk_workspace_bytes() { return size_t(2) * kSkMaxCtas * 2 * kBM * kBN * sizeof(float); }
 
 void set_wait_fault(int hold, uint64_t wait_ns) {
@@ -764,13 +816,20 @@ cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N,
   if (!make_tmap_bf16(&tb, Wc, Vc, H, H, 64, kBK)) return cudaErrorInvalidValue;
   if (!make_store_tmap(&tc, mode >= kStoreBf16AddPartial, out, N, H, H)) return cudaErrorInvalidValue;
   EpiStore::Params p{mode == kAddF32 ? static_cast<const float*>(out) : partial, H, N, H, mode};
-  // 256-row tiles: the K loop runs over the whole vocabulary chunk, so the
-  // accumulator overlap of 128-row tiles matters little and W is streamed half as often.
-  // Stream-K (with sk_ws) when the tiles leave the last wave of the grid part empty.
+  // 256-row tiles stream W half as often; 128-row tiles when they fill the
+  // grid's waves better (dx_plan).  Stream-K only for launches with too few
+  // tiles to fill a wave: its CTAs sit at different K offsets, so they share
+  // no W slices in L2, which costs more than a partly empty last wave of a
+  // large launch (measured at V = 151936: 42% slower).
   StreamK sk;
   if (kernels) *kernels = 1;
-  cudaError_t e = launch_any<false, true, EpiStore, 2>(ta, tb, tc, N, H, Vc, p, status, stream, VP_GROUP_ROWS_DX,
-                                                       sk_ws, &sk);
+  const DxPlan plan = dx_plan(N, H);
+  cudaError_t e;
+  if (plan.rows == 2 * kBM)
+    e = launch_any<false, true, EpiStore, 2>(ta, tb, tc, N, H, Vc, p, status, stream, VP_GROUP_ROWS_DX,
+                                             plan.streamk ? sk_ws : nullptr, &sk);
+  else
+    e = launch_any<false, true, EpiStore, 1>(ta, tb, tc, N, H, Vc, p, status, stream, VP_GROUP_ROWS_DX);
   if (e != cudaSuccess || sk.iters == 0) return e;
   if (kernels) *kernels = 2;
   TileSched sched;

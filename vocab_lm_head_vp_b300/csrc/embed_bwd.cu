@@ -13,12 +13,12 @@
 // Deterministic, no atomics:
 //   1. keys (id << 32 | n) for valid ids, all-ones for the rest and the
 //      padding, sorted: blocks build and bitonic-sort 512-key chunks in shared
-//      memory; then every key places itself at its rank, the count of keys
-//      that precede it in every other chunk (binary searches; the keys are
-//      distinct, the all-ones ones tie-broken by chunk).  Up to 16384 keys this
-//      is one pass with all keys in each block's shared memory; beyond, groups
-//      of up to 8 sorted runs merge in one pass each, the searches in global
-//      memory.  The sorted order groups tokens by id, by n within.
+//      memory, then groups of up to 8 sorted runs merge in one pass each, every
+//      key placing itself at its rank (binary searches in the other runs of its
+//      group; the keys are distinct, the all-ones ones tie-broken by run).
+//      The sorted order groups tokens by id, by n within.  This step needs only
+//      the ids, so a caller can run it ahead (vp_embed_bwd_plan), off the
+//      critical path, and the rest later (vp_embed_bwd_planned).
 //   2. runs of kRun sorted positions: one thread per 16-byte column vector of
 //      the row walks the run in order and sums; a segment (one id) that starts
 //      and ends inside the run is added to dW at once, a segment cut by the
@@ -39,9 +39,7 @@ namespace {
 constexpr uint64_t kSentinel = ~0ull;
 constexpr uint32_t kNoId = 0xffffffffu;
 constexpr int kChunk = 512;           // keys sorted per block in shared memory
-constexpr int kMergeWays = 8;         // sorted runs merged per pass (beyond kRankAllKeys)
-constexpr int kRankAllKeys = 16384;   // keys the one-pass rank placement holds in shared memory (128 KB)
-constexpr int kRankAllChunks = kRankAllKeys / kChunk;
+constexpr int kMergeWays = 8;         // sorted runs merged per pass
 constexpr int kSortThreads = 256;
 constexpr int kRun = 32;              // sorted positions per run
 constexpr int kRedThreads = 256;
@@ -82,45 +80,6 @@ __global__ void __launch_bounds__(kSortThreads) keys_chunk_sort(const int64_t* _
   for (int k = 2; k <= len; k <<= 1)
     for (int j = k >> 1; j > 0; j >>= 1) smem_step(s, len, k, j);
   for (int i = threadIdx.x; i < len; i += blockDim.x) keys[gbase + i] = s[i];
-}
-
-// All n_pad <= kRankAllKeys keys at once, sorted in chunks of kChunk: block c
-// holds every key in shared memory and places each key of chunk c at its
-// index in the chunk plus, for every other chunk, the keys there that precede
-// it (an earlier chunk's equal keys first).  The chunks' binary searches
-// advance in lockstep, one independent shared-memory load per chunk and round.
-__global__ void __launch_bounds__(kChunk) rank_all_kernel(const uint64_t* __restrict__ in,
-                                                          uint64_t* __restrict__ out, int n_pad) {
-  extern __shared__ uint64_t sk_all[];
-  for (int i = threadIdx.x; i < n_pad; i += blockDim.x) sk_all[i] = in[i];
-  __syncthreads();
-  const int chunks = n_pad / kChunk;
-  const int own = blockIdx.x;
-  const int i = own * kChunk + static_cast<int>(threadIdx.x);
-  const uint64_t key = sk_all[i];
-  int lo[kRankAllChunks], hi[kRankAllChunks];
-#pragma unroll
-  for (int c = 0; c < kRankAllChunks; ++c) {
-    lo[c] = 0;
-    hi[c] = (c < chunks && c != own) ? kChunk : 0;   // no search in the own chunk or past the last
-  }
-  for (int span = kChunk; span > 0; span >>= 1) {   // log2(kChunk) + 1 rounds finish every search
-#pragma unroll
-    for (int c = 0; c < kRankAllChunks; ++c) {
-      if (lo[c] < hi[c]) {
-        const int mid = (lo[c] + hi[c]) >> 1;
-        const uint64_t x = sk_all[c * kChunk + mid];
-        if (c < own ? x <= key : x < key)
-          lo[c] = mid + 1;
-        else
-          hi[c] = mid;
-      }
-    }
-  }
-  int pos = static_cast<int>(threadIdx.x);
-#pragma unroll
-  for (int c = 0; c < kRankAllChunks; ++c) pos += lo[c];
-  out[pos] = key;
 }
 
 // Merge each group of G consecutive sorted runs of L keys (G, L, n_pad powers
@@ -330,12 +289,10 @@ int64_t pad_pow2(int64_t n) {
 
 }  // namespace
 
-int embed_bwd_kernels(int64_t N) {
+int embed_bwd_sort_kernels(int64_t N) {
   const int64_t n_pad = pad_pow2(N);
-  int k = 3;   // keys + chunk sort, run sums, cross-run sums
-  if (n_pad <= kChunk) return k;
-  if (n_pad <= kRankAllKeys) return k + 1;   // one rank placement
-  for (int64_t L = kChunk; L < n_pad; L *= kMergeWays) ++k;   // merge passes
+  int k = 1;   // keys + chunk sort
+  for (int64_t L = n_pad < kChunk ? n_pad : kChunk; L < n_pad; L *= kMergeWays) ++k;   // merge passes
   return k;
 }
 
@@ -344,36 +301,16 @@ size_t embed_bwd_workspace(int64_t N, int64_t H) {
   return 2 * size_t(pad_pow2(N)) * sizeof(uint64_t) + 2 * size_t(runs) * H * sizeof(float);
 }
 
-cudaError_t embed_bwd(const int64_t* ids, const void* dOut, float* dW, int64_t N, int64_t H, int64_t V, int esize,
-                      bool accumulate, void* workspace, cudaStream_t stream) {
+// Step 1: the sorted keys, left in the workspace's first key buffer when the
+// number of merge passes is even and in the second when it is odd
+// (sorted_keys() finds them).
+cudaError_t embed_bwd_sort(const int64_t* ids, int64_t N, int64_t V, void* workspace, cudaStream_t stream) {
   const int64_t n_pad = pad_pow2(N);
-  const int64_t runs = (N + kRun - 1) / kRun;
   uint64_t* keys = static_cast<uint64_t*>(workspace);   // two n_pad buffers, sorted in turn
   uint64_t* spare = keys + n_pad;
-  float* head = reinterpret_cast<float*>(keys + 2 * n_pad);
-  float* tail = head + runs * H;
-  cudaError_t e = cudaSuccess;
-  if (!accumulate) e = cudaMemsetAsync(dW, 0, size_t(V) * H * sizeof(float), stream);
-  if (e != cudaSuccess) return e;
   const int len = static_cast<int>(n_pad < kChunk ? n_pad : kChunk);
   keys_chunk_sort<<<static_cast<unsigned>(n_pad / len), kSortThreads, 0, stream>>>(ids, N, V, keys, len);
-  if (n_pad > kChunk && n_pad <= kRankAllKeys) {
-    const size_t smem = size_t(n_pad) * sizeof(uint64_t);
-    static bool attr_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    if (!attr_set[dev]) {
-      e = cudaFuncSetAttribute(rank_all_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kRankAllKeys * static_cast<int>(sizeof(uint64_t)));
-      if (e != cudaSuccess) return e;
-      attr_set[dev] = true;
-    }
-    rank_all_kernel<<<static_cast<unsigned>(n_pad / kChunk), kChunk, smem, stream>>>(keys, spare, static_cast<int>(n_pad));
-    uint64_t* t = keys;
-    keys = spare;
-    spare = t;
-  }
-  for (int64_t L = len; n_pad > kRankAllKeys && L < n_pad;) {
+  for (int64_t L = len; L < n_pad;) {
     const int G = static_cast<int>(n_pad / L < kMergeWays ? n_pad / L : kMergeWays);
     rank_merge_kernel<<<static_cast<unsigned>((n_pad + 255) / 256), 256, 0, stream>>>(keys, spare, n_pad, L, G);
     uint64_t* t = keys;
@@ -381,6 +318,28 @@ cudaError_t embed_bwd(const int64_t* ids, const void* dOut, float* dW, int64_t N
     spare = t;
     L *= G;
   }
+  return cudaGetLastError();
+}
+
+namespace {
+const uint64_t* sorted_keys(const void* workspace, int64_t N) {
+  const int64_t n_pad = pad_pow2(N);
+  const int passes = embed_bwd_sort_kernels(N) - 1;
+  return static_cast<const uint64_t*>(workspace) + ((passes & 1) ? n_pad : 0);
+}
+}  // namespace
+
+// Steps 2 and 3 on keys sorted by embed_bwd_sort into the same workspace.
+cudaError_t embed_bwd_sums(const void* dOut, float* dW, int64_t N, int64_t H, int64_t V, int esize, bool accumulate,
+                           void* workspace, cudaStream_t stream) {
+  const int64_t n_pad = pad_pow2(N);
+  const int64_t runs = (N + kRun - 1) / kRun;
+  const uint64_t* keys = sorted_keys(workspace, N);
+  float* head = reinterpret_cast<float*>(static_cast<uint64_t*>(workspace) + 2 * n_pad);
+  float* tail = head + runs * H;
+  cudaError_t e = cudaSuccess;
+  if (!accumulate) e = cudaMemsetAsync(dW, 0, size_t(V) * H * sizeof(float), stream);
+  if (e != cudaSuccess) return e;
   const int64_t rowvec = H * esize / 16;
   const dim3 grid(static_cast<unsigned>(runs), static_cast<unsigned>((rowvec + kRedThreads - 1) / kRedThreads));
   const uint4* src = static_cast<const uint4*>(dOut);

@@ -92,28 +92,6 @@ __device__ __forceinline__ void stage_and_store(EpiCtx& ctx, const CUtensorMap* 
   ctx.buf ^= 1;
 }
 
-// Thread `lane` holds column `lane` of a 32 x 32 fp32 block (w[j] = row j):
-// write the block row-major into the warp's staging box in the 128-byte
-// swizzled order TMA expects (for each row, 32 lanes hit 32 banks), then one
-// lane stores the 32-row box at (c0, c1).  All 32 lanes call it.
-__device__ __forceinline__ void stage_transposed_and_store(EpiCtx& ctx, const CUtensorMap* tm, const uint32_t (&w)[32],
-                                                           int32_t c0, int32_t c1) {
-  uint8_t* box = ctx.stg + ctx.buf * kStoreBoxBytes;
-  if (ctx.lane == 0) bulk_wait_group_read<1>();   // the store that last used this box has read it
-  __syncwarp();
-  const int chunk = ctx.lane >> 2, within = (ctx.lane & 3) * 4;
-#pragma unroll
-  for (int j = 0; j < 32; ++j)
-    *reinterpret_cast<uint32_t*>(box + j * 128 + ((chunk ^ (j & 7)) << 4) + within) = w[j];
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (ctx.lane == 0) {
-    tma_store_2d(tm, box, c0, c1);
-    bulk_commit_group();
-  }
-  ctx.buf ^= 1;
-}
-
 struct TileSched {
   int num_m, num_n, group_m;
   // Tile id -> (m block, n block): ids run down groups of `group_m` m-blocks

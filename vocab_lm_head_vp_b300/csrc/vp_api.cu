@@ -90,8 +90,9 @@ constexpr int64_t kFusedRowAlign = 128;   // token chunks are whole 128-row GEMM
 
 // Budget of the fused call's saved probabilities when the caller names no
 // token chunk: N_c x round8(V) 2-byte values stay below it (the logits are
-// never held for all N tokens at once).
-constexpr size_t kFusedDefaultSavedBytes = size_t(1) << 30;
+// never held for all N tokens at once).  1.25 GiB: at V = 128256 the chunk
+// that fills the dX GEMM's waves best within it holds 4736 tokens (1.2 GB).
+constexpr size_t kFusedDefaultSavedBytes = size_t(5) << 28;
 
 int64_t fused_default_chunk(int64_t N, int64_t V) {
   const size_t per_row = size_t((V + 7) / 8 * 8) * 2;
@@ -100,16 +101,27 @@ int64_t fused_default_chunk(int64_t N, int64_t V) {
   return nc >= N ? N : nc;
 }
 
-// Token chunk of the fused call for at most nc_max rows per chunk: the fewest
-// chunks (each chunk after the first adds an fp32 read-modify-write of dW),
-// as equal as the 128-row blocks allow, so that no chunk is a sliver.  The
-// dX GEMM's stream-K schedule keeps every chunk's tiles spread evenly over
-// the SMs whatever their count.
-int64_t balanced_token_chunk(int64_t N, int64_t nc_max) {
+// Token chunk of the fused call for at most nc_max rows per chunk.  Each
+// chunk's dX GEMM runs in whole waves of the persistent grid (dx_plan), so
+// equal chunks can leave a mostly idle last wave in every chunk: among chunk
+// sizes from nc_max down to half of it (128-row blocks), take the one with the
+// lowest total dX cost plus a quarter wave per chunk after the first (its fp32
+// read-modify-write of dW), fewer chunks on a tie.
+int64_t balanced_token_chunk(int64_t N, int64_t H, int64_t nc_max) {
   if (nc_max >= N) return N;
-  const int64_t k = (N + nc_max - 1) / nc_max;
-  const int64_t nc = ((N + k - 1) / k + kFusedRowAlign - 1) / kFusedRowAlign * kFusedRowAlign;
-  return nc < nc_max ? nc : nc_max;
+  const int64_t mmax = nc_max / kFusedRowAlign;
+  int64_t best = mmax, best_k = -1;
+  double best_cost = 0.0;
+  for (int64_t m = mmax; m >= 1 && 2 * m >= mmax; --m) {
+    const int64_t nc = m * kFusedRowAlign, k = (N + nc - 1) / nc;
+    const double cost = static_cast<double>(k - 1) * (dx_plan(nc, H).cost + 0.25) + dx_plan(N - (k - 1) * nc, H).cost;
+    if (best_k < 0 || cost < best_cost - 1e-9 || (cost < best_cost + 1e-9 && k < best_k)) {
+      best = m;
+      best_k = k;
+      best_cost = cost;
+    }
+  }
+  return best * kFusedRowAlign;
 }
 
 // Vocab chunk of the split backward for at most vc_max ids per chunk: the
@@ -147,11 +159,12 @@ constexpr int kMergeKernels = 2;   // lse_merge: the per-shard pass, then the pe
 // ---------------- optional per-launch event timing (vp_stage_timing_enable)
 enum Stage {
   kEmbed, kLseGemm, kMerge, kMean, kScale, kDzGemm, kDwGemm, kDxGemm, kLsePGemm, kDzFromP, kEmbedBwd, kXT,
-  kNumStages
+  kEmbedSort, kNumStages
 };
 const char* const kStageNames[kNumStages] = {"embed_gather",   "lse_stats_gemm",    "lse_merge", "loss_mean",
                                              "upstream_scale", "dz_recompute_gemm", "dw_gemm",   "dx_gemm",
-                                             "lse_p_gemm",     "dz_from_p",         "embed_bwd", "x_transpose"};
+                                             "lse_p_gemm",     "dz_from_p",         "embed_bwd", "x_transpose",
+                                             "embed_bwd_sort"};
 struct StageTimer {
   int cap = 0, used = 0;
   int dropped = 0;            // timed regions past `cap`, not recorded
@@ -237,19 +250,48 @@ VP_EXPORT size_t vp_embed_bwd_workspace_size(int64_t N, int64_t H, int64_t V, in
   return align_up(embed_bwd_workspace(N, H), kAlign);
 }
 
+static vp_status check_embed_bwd(const void* dOut, const float* dW, int64_t N, int64_t H, int64_t V, int T,
+                                 vp_dtype dtype, const void* workspace, size_t ws_bytes) {
+  if (!dOut || !dW || !workspace || !dtype_ok(dtype) || !shape_ok(N, H, V, T)) return VP_ERR_INVALID_ARG;
+  const int es = esize_of(dtype);
+  if (!aligned16(dOut) || !aligned16(dW) || !aligned16(workspace) || (H * es) % 16 != 0) return VP_ERR_UNSUPPORTED;
+  if (ws_bytes < embed_bwd_workspace(N, H)) return VP_ERR_WORKSPACE;
+  return VP_OK;
+}
+
+VP_EXPORT vp_status vp_embed_bwd_plan(const int64_t* ids, int64_t N, int64_t H, int64_t V, int T, void* workspace,
+                                      size_t ws_bytes, void* stream) {
+  if (!ids || !workspace || !shape_ok(N, H, V, T)) return VP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ids) & 7u) != 0 || !aligned16(workspace)) return VP_ERR_UNSUPPORTED;
+  if (ws_bytes < embed_bwd_workspace(N, H)) return VP_ERR_WORKSPACE;
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e = timed(kEmbedSort, s, [&] { return embed_bwd_sort(ids, N, V, workspace, s); },
+                        embed_bwd_sort_kernels(N));
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
+VP_EXPORT vp_status vp_embed_bwd_planned(const void* dOut, float* dW, int64_t N, int64_t H, int64_t V, int T,
+                                         vp_dtype dtype, int accumulate, void* workspace, size_t ws_bytes,
+                                         void* stream) {
+  const vp_status st = check_embed_bwd(dOut, dW, N, H, V, T, dtype, workspace, ws_bytes);
+  if (st != VP_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e = timed(kEmbedBwd, s, [&] {
+    return embed_bwd_sums(dOut, dW, N, H, V, esize_of(dtype), accumulate != 0, workspace, s);
+  }, 2);
+  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+}
+
 VP_EXPORT vp_status vp_embed_bwd(const int64_t* ids, const void* dOut, float* dW, int64_t N, int64_t H, int64_t V,
                                  int T, vp_dtype dtype, int accumulate, void* workspace, size_t ws_bytes,
                                  void* stream) {
-  if (!ids || !dOut || !dW || !workspace || !dtype_ok(dtype) || !shape_ok(N, H, V, T)) return VP_ERR_INVALID_ARG;
-  const int es = esize_of(dtype);
-  if (!aligned16(dOut) || !aligned16(dW) || !aligned16(workspace) || (H * es) % 16 != 0) return VP_ERR_UNSUPPORTED;
+  if (!ids) return VP_ERR_INVALID_ARG;
+  vp_status st = check_embed_bwd(dOut, dW, N, H, V, T, dtype, workspace, ws_bytes);
+  if (st != VP_OK) return st;
   if ((reinterpret_cast<uintptr_t>(ids) & 7u) != 0) return VP_ERR_UNSUPPORTED;
-  if (ws_bytes < embed_bwd_workspace(N, H)) return VP_ERR_WORKSPACE;
-  cudaStream_t s = as_stream(stream);
-  cudaError_t e =
-      timed(kEmbedBwd, s, [&] { return embed_bwd(ids, dOut, dW, N, H, V, es, accumulate != 0, workspace, s); },
-            embed_bwd_kernels(N));
-  return e == cudaSuccess ? VP_OK : VP_ERR_CUDA;
+  st = vp_embed_bwd_plan(ids, N, H, V, T, workspace, ws_bytes, stream);
+  if (st != VP_OK) return st;
+  return vp_embed_bwd_planned(dOut, dW, N, H, V, T, dtype, accumulate, workspace, ws_bytes, stream);
 }
 
 VP_EXPORT size_t vp_lmhead_ce_workspace_size(int64_t N, int64_t H, int64_t V, int T, vp_dtype dtype, int pass,
@@ -257,7 +299,7 @@ VP_EXPORT size_t vp_lmhead_ce_workspace_size(int64_t N, int64_t H, int64_t V, in
   if (!dtype_ok(dtype) || !shape_ok(N, H, V, T)) return 0;
   if (pass == 0) return fwd_layout(N, V, T, dtype).total;
   if (pass == 2 && dtype == VP_BF16) {
-    int64_t nc = chunk <= 0 ? fused_default_chunk(N, V) : chunk;
+    int64_t nc = chunk <= 0 ? balanced_token_chunk(N, H, fused_default_chunk(N, V)) : chunk;
     if (nc < N) {
       nc = nc / kFusedRowAlign * kFusedRowAlign;
       if (nc < kFusedRowAlign) nc = kFusedRowAlign;
@@ -405,7 +447,7 @@ VP_EXPORT vp_status vp_lmhead_ce_fwd_bwd(const void* X, const void* W, const int
   }
   const int64_t Nc_max = fused_chunk_from_ws(N, H, V, T, ws_bytes);
   if (Nc_max <= 0) return VP_ERR_WORKSPACE;
-  const int64_t Nc = balanced_token_chunk(N, Nc_max);
+  const int64_t Nc = balanced_token_chunk(N, H, Nc_max);
   if (!tensor_map_encoder()) return VP_ERR_CUDA;
   const FusedLayout L = fused_layout(N, H, V, T, Nc);
   cudaStream_t s = as_stream(stream);

@@ -33,6 +33,14 @@ cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N,
                           void* out, const float* partial, int mode, uint32_t* status, cudaStream_t stream,
                           float* sk_ws = nullptr, int* kernels = nullptr);
 size_t sk_workspace_bytes();
+// How bf16_dx_chunk runs a dX GEMM over `rows` token rows: tile rows (128 or
+// 256), whether stream-K, and the relative time (waves of 128 x 256 tiles).
+struct DxPlan {
+  int rows;
+  bool streamk;
+  double cost;
+};
+DxPlan dx_plan(int64_t rows, int64_t H);
 // dW through X^T (A K-major): Xt = X^T [H][ldxt] bf16 (transpose_bf16 of X).
 // cudaErrorNotSupported under GEMM form 2 (callers then use bf16_dw_chunk).
 cudaError_t bf16_dwt_chunk(const void* Xt, int64_t ldxt, const void* dz, int64_t ldz, int64_t N, int64_t H,
@@ -112,9 +120,13 @@ cudaError_t embed_gather(const int64_t* ids, const void* W, void* out, int64_t N
 
 // ---- embedding backward (embed_bwd.cu)
 size_t embed_bwd_workspace(int64_t N, int64_t H);
-int embed_bwd_kernels(int64_t N);   // kernels one call launches (the dW memset not counted)
-cudaError_t embed_bwd(const int64_t* ids, const void* dOut, float* dW, int64_t N, int64_t H, int64_t V, int esize,
-                      bool accumulate, void* workspace, cudaStream_t stream);
+int embed_bwd_sort_kernels(int64_t N);   // kernels embed_bwd_sort launches
+// Step 1, ids only: the tokens' (id, n) keys sorted into the workspace.
+cudaError_t embed_bwd_sort(const int64_t* ids, int64_t N, int64_t V, void* workspace, cudaStream_t stream);
+// Steps 2-3 (two kernels, after a dW memset when not accumulating): the sums
+// over the keys embed_bwd_sort left in the same workspace.
+cudaError_t embed_bwd_sums(const void* dOut, float* dW, int64_t N, int64_t H, int64_t V, int esize, bool accumulate,
+                           void* workspace, cudaStream_t stream);
 
 // ---- argument checks and the forward workspace layout (vp_api.cu, vp_noalloc.cu)
 constexpr size_t kAlign = 256;
