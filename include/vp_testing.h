@@ -30,15 +30,16 @@ vp_status vp_test_gemm_bf16(const void* A, const void* B, float* D, int64_t M, i
                             int a_mn_major, int b_mn_major, void* workspace, void* stream);
 
 /*
- * vp_test_set_gemm_variant -- select the tcgen05 GEMM form used by every
+ * vp_test_set_gemm_variant -- select the tcgen05 GEMM forms used by every
  * later bf16 call in this process:
- *   0 (default): one SM per tile; the dX contraction in 256 x 256 tiles (two
- *      128-row blocks sharing each B stage, B streamed half as often), the
- *      other GEMMs in 128 x 256 tiles with the epilogue overlapping the MMAs;
- *   1: each 256 x 256 tile on a pair of SMs (cta_group::2, a cluster of 2 CTAs);
- *   2: one SM per 128 x 256 tile for every GEMM, dX included.
- * All compute the same results; this exists to compare them.  Other values:
- * VP_ERR_INVALID_ARG.
+ *   0 (default): the logits GEMMs on one SM per 128 x 256 tile (the epilogue
+ *      overlapping the next tile's MMAs); dX on one SM per 256 x 256 or
+ *      128 x 256 tile, whichever fills the waves better; dW as dW^T = X^T dZ
+ *      with each 256 x 256 tile on a pair of SMs (cta_group::2);
+ *   1: each 256 x 256 tile of every GEMM on a pair of SMs;
+ *   2: one SM per 128 x 256 tile for every GEMM, and dW = dZ^T X directly.
+ * All compute the same results within rounding; this exists to compare them.
+ * Other values: VP_ERR_INVALID_ARG.
  */
 vp_status vp_test_set_gemm_variant(int variant);
 
