@@ -628,8 +628,8 @@ def run_ours(args):
     d2h = loss_h.numel() * 4 + 4
     assert all(vp.read_device_status(w) == 0 for w in workspaces)
 
-    emb_micro = embed_microbench(vp, dev) if args.embed_iters > 0 else None
-    emb_bwd_micro = embed_bwd_microbench(vp, dev) if args.embed_iters > 0 else None
+    emb_micro = embed_microbench(vp, dev, args.embed_iters) if args.embed_iters > 0 else None
+    emb_bwd_micro = embed_bwd_microbench(vp, dev, args.embed_iters) if args.embed_iters > 0 else None
 
     # ---------------- the other path, briefly (reported beside, not in `value`)
     other = None

@@ -34,6 +34,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 #ifndef VP_GROUP_ROWS_LOGITS
 #define VP_GROUP_ROWS_LOGITS 4096   // forward / recompute: token rows (W re-read once per group)
 #endif
+#ifndef VP_GROUP_ROWS_LOGITS_MAX
+#define VP_GROUP_ROWS_LOGITS_MAX 6144   // up to this many token rows form a single group
+#endif
 #ifndef VP_GROUP_ROWS_DX
 #define VP_GROUP_ROWS_DX 1024       // dX: token rows
 #endif
@@ -481,6 +484,15 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __r
 // ------------------------------------------------------------------ host side
 namespace {
 
+// Token rows per tile group of a logits GEMM over N rows: all of them when
+// they are few enough that X stays in L2 beside the W tiles in use (W then
+// streams from DRAM once), else VP_GROUP_ROWS_LOGITS.  A token chunk of the
+// fused call (e.g. 4736 rows) would otherwise end in a small group that
+// streams all of W again for a few rows.
+int logits_group_rows(int64_t N) {
+  return N <= VP_GROUP_ROWS_LOGITS_MAX ? static_cast<int>(N) : VP_GROUP_ROWS_LOGITS;
+}
+
 // 2-D bf16 tensor map over a row-major [rows][cols] matrix with leading
 // dimension `ld` elements; box = {box_cols (inner), box_rows}, 128B swizzle,
 // out-of-bounds elements read as zero.
@@ -779,7 +791,7 @@ cudaError_t bf16_lse_stats(const void* X, const void* W, const int64_t* targets,
   if (!make_tmap_bf16(&ta, X, N, H, H, kBK, kBM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, W, V, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
   EpiLseStats::Params p{partial, zy, targets, N, V, Vs, maxseg, nullptr, y_off};
-  return launch_any<false, false, EpiLseStats>(ta, tb, ta, N, V, H, p, status, stream, VP_GROUP_ROWS_LOGITS);
+  return launch_any<false, false, EpiLseStats>(ta, tb, ta, N, V, H, p, status, stream, logits_group_rows(N));
 }
 
 cudaError_t bf16_lse_stats_p(const void* X, const void* W, const int64_t* targets, int64_t N, int64_t H, int64_t V,
@@ -791,7 +803,7 @@ cudaError_t bf16_lse_stats_p(const void* X, const void* W, const int64_t* target
   // fp16 boxes of 32 rows x 64 columns (128 bytes), clipped at V columns and N rows
   if (!make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, P, N, V, ldp, 64, 32)) return cudaErrorInvalidValue;
   EpiLseStatsP::Params p{partial, zy, targets, N, V, Vs, maxseg, tmax, 0};
-  return launch_any<false, false, EpiLseStatsP>(ta, tb, tc, N, V, H, p, status, stream, VP_GROUP_ROWS_LOGITS);
+  return launch_any<false, false, EpiLseStatsP>(ta, tb, tc, N, V, H, p, status, stream, logits_group_rows(N));
 }
 
 cudaError_t bf16_dz_chunk(const void* X, const void* W, const int64_t* targets, const float* lse, const float* g,
@@ -803,7 +815,7 @@ cudaError_t bf16_dz_chunk(const void* X, const void* W, const int64_t* targets, 
   if (!make_tmap_bf16(&tb, Wc, Vc, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
   if (!make_store_tmap(&tc, true, dz, N, Vc, ldz)) return cudaErrorInvalidValue;
   EpiDZ::Params p{lse, g, targets, N, y_off + c0, Vc};
-  return launch_any<false, false, EpiDZ>(ta, tb, tc, N, Vc, H, p, status, stream, VP_GROUP_ROWS_LOGITS);
+  return launch_any<false, false, EpiDZ>(ta, tb, tc, N, Vc, H, p, status, stream, logits_group_rows(N));
 }
 
 cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N, int64_t H, int64_t c0,
