@@ -98,7 +98,7 @@ GEMM_TRAFFIC = {"workload": "v128k", "path": "fused", "gemm_variant": "single", 
                 "bytes_per_stage": 20.57e9,
                 "by_stage": {"lse_p_gemm": 11.83e9, "dw_gemm": 23.94e9, "dx_gemm": 25.95e9},
                 "sources": ("vocab_lm_head_vp_b300/csrc/ce_bf16.cu", "vocab_lm_head_vp_b300/csrc/ptx.cuh",
-                            "vocab_lm_head_vp_b300/csrc/umma_gemm.cuh"),
+                            "vocab_lm_head_vp_b300/csrc/umma_gemm.cuh", "vocab_lm_head_vp_b300/csrc/umma_gemm_2sm.cuh"),
                 "sha256": "d44ff05879df578b05910ecd5946deeb200a795f1d084fed7c448b253fd020e9"}
 
 
@@ -554,7 +554,8 @@ def run_ours(args):
         r = {"path": path, "steps": steps, "ms_per_step": oms, "value": job_tokens_per_s(N, world, 1, oms / 1e3),
              "unit": UNIT, "fwd_ms": ofwd, "bwd_ms": obwd, "chunks": ost.get("dw_gemm", (0, 0))[1] / steps,
              "workspace_bytes": int(sum(w.numel() for w in ows)),
-             "pct_bf16_burst_algorithmic": 100.0 * 6.0 * N * H * V / (oms / 1e3) / 1e12 / load_peaks()["bf16_tflops"]}
+             "pct_bf16_burst_algorithmic": 100.0 * 6.0 * N * H * V / (oms / 1e3) / 1e12 / load_peaks()["bf16_tflops"],
+             "stages_ms_per_step": {k: round(v[0] / steps, 4) for k, v in ost.items() if v[1]}}
         del ostep, ows
         torch.cuda.empty_cache()
         return r

@@ -302,9 +302,10 @@ def test_results_repeatable():
 
 @pytest.mark.parametrize("variant", [0, 1, 2])
 def test_gemm_forms_agree_on_the_path(variant):
-    """The split fwd/bwd with each GEMM form (one SM with 256-row dX tiles, SM
-    pairs, one SM with 128-row tiles everywhere) matches the oracle (ragged N
-    and V, a shard edge inside tiles, two vocab chunks)."""
+    """The split fwd/bwd with each GEMM form (the default: dX tiles chosen per
+    launch, dW^T on SM pairs; SM pairs everywhere; one SM with 128-row tiles
+    everywhere) matches the oracle (ragged N and V, a shard edge inside tiles,
+    two vocab chunks)."""
     vp.set_gemm_variant(variant)
     try:
         inp = synth.small_case(333, 264, 1800, 6, "bf16", seed=77, ignore_frac=0.1)

@@ -552,6 +552,25 @@ cudaError_t ensure_smem(Kern kern, size_t smem, std::atomic<int>* done) {
 // Stream-K launches use at most this many CTAs (the partial workspace holds
 // two 256 x 256 fp32 slots per CTA: sk_workspace_bytes()).
 constexpr int kSkMaxCtas = 160;
+// The fix-up pass adds at most this many pieces (CTAs) per tile, in this many
+// row slabs per tile (blocks).
+constexpr int kSkMaxPieces = 8;
+constexpr int kSkSlabs = 16;
+
+// The largest number of CTAs whose stream-K iteration ranges meet one tile's
+// k-blocks, for `tiles` tiles of num_k k-blocks split over G CTAs.
+int sk_max_pieces(int64_t tiles, int64_t num_k, int64_t G) {
+  const int64_t I = tiles * num_k;
+  int64_t most = 0, c = 0;
+  for (int64_t t = 0; t < tiles; ++t) {
+    const int64_t lo = t * num_k, hi = lo + num_k;
+    while (sk_begin(c + 1, G, I) <= lo) ++c;   // c holds iteration lo
+    int64_t d = c;
+    while (d + 1 < G && sk_begin(d + 1, G, I) < hi) ++d;
+    if (d - c + 1 > most) most = d - c + 1;
+  }
+  return static_cast<int>(most);
+}
 
 // Diagnostic of the bounded waits (vp_test_set_wait_fault): a role of every
 // later one-SM GEMM launch that issues nothing, and the waits' time limit.
@@ -583,7 +602,7 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   GemmArgs a;
   a.sched.num_m = static_cast<int>((M + kMB * kBM - 1) / (kMB * kBM));
   a.sched.num_n = static_cast<int>((Ncols + kBN - 1) / kBN);
-  const int group_m = group_m_rows / (kMB * kBM);
+  const int group_m = (group_m_rows + kMB * kBM - 1) / (kMB * kBM);
   a.sched.group_m = group_m < 1 ? 1 : group_m;
   a.num_k = static_cast<int>((K + kBK - 1) / kBK);
   a.status = status;
@@ -597,8 +616,8 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   if (sk && sk_ws && Epi::kStagingBytes > 0) {
     const int G = sm_count() < kSkMaxCtas ? sm_count() : kSkMaxCtas;
     const int64_t iters = static_cast<int64_t>(total) * a.num_k;
-    // at least G/4 tiles, so a tile's k-blocks spread over at most 8 CTAs (the fix-up's piece limit)
-    if (total % G != 0 && 4 * total >= G && a.num_k >= 2 && iters >= G) {
+    // only while no tile's k-blocks spread over more CTAs than the fix-up adds
+    if (total % G != 0 && a.num_k >= 2 && iters >= G && sk_max_pieces(total, a.num_k, G) <= kSkMaxPieces) {
       sk->ws = sk_ws;
       const int64_t rows = static_cast<int64_t>(2 * G) * kMB * kBM;
       if (!make_tmap(&sk->tp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, sk_ws, rows, kBN, kBN, 32, 32))
@@ -678,37 +697,42 @@ cudaError_t launch_any(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
                        cudaStream_t stream, int group_m_rows, float* sk_ws = nullptr, StreamK* sk = nullptr) {
   if (sk) sk->iters = 0;
   if (pair_kernels())
-    return launch_gemm_2sm<A_MN, B_MN, Epi>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows / kPairBM);
+    return launch_gemm_2sm<A_MN, B_MN, Epi>(ta, tb, tc, M, Ncols, K, ep, status, stream,
+                                            (group_m_rows + kPairBM - 1) / kPairBM);
   if (kMB == 2 && g_variant == 2)
     return launch_gemm<A_MN, B_MN, Epi, 1>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows);
   return launch_gemm<A_MN, B_MN, Epi, kMB>(ta, tb, tc, M, Ncols, K, ep, status, stream, group_m_rows, sk_ws, sk);
 }
 
-// Stream-K fix-up: one block per CTA boundary of the launch that falls inside a
-// tile (the first such boundary of each tile does the tile).  The tile's
-// pieces, in CTA order (k order), are added in fp32 and the sum finished as
-// the store epilogue would: fp32 store, fp32 add onto the output, or bf16
-// (after adding `partial`).  Columns come in fours (H is a multiple of 8).
+// Stream-K fix-up: blockIdx.x runs over the CTA boundaries of the launch; a
+// boundary that falls inside a tile, and is that tile's first, finishes the
+// tile, one slab of tile_rows / gridDim.y rows per blockIdx.y (so that the
+// few split tiles still spread over the SMs).  The tile's pieces, in CTA order
+// (k order), are added in fp32 and the sum finished as the store epilogue
+// would: fp32 store, fp32 add onto the output, or bf16 (after adding
+// `partial`).  Columns come in fours (H is a multiple of 8).
 __global__ void __launch_bounds__(256) sk_fixup_kernel(const float* __restrict__ ws, int64_t iters, int G, int num_k,
                                                        TileSched sched, int tile_rows, void* __restrict__ out,
                                                        const float* __restrict__ partial, int64_t ld, int64_t M,
                                                        int64_t Ncols, int mode) {
   const int c = static_cast<int>(blockIdx.x) + 1;
+  const int slab_rows = tile_rows / static_cast<int>(gridDim.y);
+  const int r_begin = static_cast<int>(blockIdx.y) * slab_rows;
   const int64_t b = sk_begin(c, G, iters);
   if (b % num_k == 0) return;                                        // a tile edge: nothing split here
   const int64_t t = b / num_k;
   if (sk_begin(c - 1, G, iters) > t * num_k) return;                 // an earlier boundary inside t does it
   int c_last = c;
   while (c_last + 1 < G && sk_begin(c_last + 1, G, iters) < (t + 1) * num_k) ++c_last;
-  int slots[8];
+  int slots[kSkMaxPieces];
   int np = 0;
-  for (int q = c - 1; q <= c_last && np < 8; ++q)
+  for (int q = c - 1; q <= c_last && np < kSkMaxPieces; ++q)
     slots[np++] = (sk_begin(q, G, iters) / num_k == t) ? 2 * q : 2 * q + 1;
   int mb, nb;
   sched.tile(static_cast<int>(t), mb, nb);
   const int64_t row0 = static_cast<int64_t>(mb) * tile_rows, col0 = static_cast<int64_t>(nb) * kBN;
-  for (int e = threadIdx.x; e < tile_rows * (kBN / 4); e += blockDim.x) {
-    const int r = e / (kBN / 4), cq = (e % (kBN / 4)) * 4;
+  for (int e = threadIdx.x; e < slab_rows * (kBN / 4); e += blockDim.x) {
+    const int r = r_begin + e / (kBN / 4), cq = (e % (kBN / 4)) * 4;
     const int64_t row = row0 + r, col = col0 + cq;
     if (row >= M || col >= Ncols) continue;
     float4 acc = *reinterpret_cast<const float4*>(ws + (static_cast<int64_t>(slots[0]) * tile_rows + r) * kBN + cq);
@@ -746,7 +770,9 @@ bool dw_through_xt() { return g_variant != 2; }
 // Relative time of a dX launch over `rows` token rows in units of one wave of
 // 128 x 256 tiles: its waves on the persistent grid, a 256-row wave counting
 // twice, a 128-row wave 4% more than half of that (it streams W twice as
-// often per row).  The tile shape with the lower cost is taken.
+// often per row).  The tile shape with the lower cost is taken.  (256 x 256
+// tiles on SM pairs, which fill waves of 74 pairs, were measured slower for
+// this contraction than either one-SM form at equal wave counts.)
 DxPlan dx_plan(int64_t rows, int64_t H) {
   const int64_t G = sm_count(), cols = (H + kBN - 1) / kBN;
   const auto waves = [&](int64_t tile_rows) { return ((rows + tile_rows - 1) / tile_rows * cols + G - 1) / G; };
@@ -755,8 +781,10 @@ DxPlan dx_plan(int64_t rows, int64_t H) {
   const bool two = g_variant != 2 && c2 <= c1;
   p.rows = two ? 2 * kBM : kBM;
   p.cost = two ? c2 : c1;
-  // fewer 256-row tiles than SMs, and whole waves would take over a third longer
-  // than the work: split the tiles over the SMs
+  // fewer 256-row tiles than SMs (but at least a quarter as many: with fewer,
+  // the fp32 partials of tiles split over many CTAs cost more than the idle
+  // SMs, measured on the MiniMind dX shape), and whole waves would take over a
+  // third longer than the work: split the tiles over the SMs
   const int64_t t2 = (rows + 2 * kBM - 1) / (2 * kBM) * cols;
   const double ideal = static_cast<double>((rows + kBM - 1) / kBM * cols) / static_cast<double>(G);
   p.streamk = g_variant != 2 && 4 * t2 >= G && t2 < G && ideal < 0.75 * p.cost;
@@ -850,7 +878,7 @@ cudaError_t bf16_dx_chunk(const void* dz, int64_t ldz, const void* W, int64_t N,
   sched.num_n = static_cast<int>((H + kBN - 1) / kBN);
   const int group_m = VP_GROUP_ROWS_DX / (2 * kBM);
   sched.group_m = group_m < 1 ? 1 : group_m;
-  sk_fixup_kernel<<<static_cast<unsigned>(sk.grid - 1), 256, 0, stream>>>(
+  sk_fixup_kernel<<<dim3(static_cast<unsigned>(sk.grid - 1), kSkSlabs), 256, 0, stream>>>(
       sk.ws, sk.iters, sk.grid, static_cast<int>((Vc + kBK - 1) / kBK), sched, 2 * kBM, out,
       mode == kAddF32 ? static_cast<const float*>(out) : partial, H, N, H, mode);
   return cudaGetLastError();
