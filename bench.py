@@ -73,7 +73,7 @@ def parse_args():
                         "SM pairs, or 128x256 tiles on one SM for every GEMM")
     p.add_argument("--token-chunk", type=int, default=0,
                    help="fused path: token rows per chunk the workspace is sized for (0: the library's bounded "
-                        "default, saved probabilities <= 1 GiB; N: all tokens at once)")
+                        "default, saved probabilities <= 1.25 GiB; N: all tokens at once)")
     p.add_argument("--vocab-chunk", type=int, default=0,
                    help="split path: vocab ids per backward chunk (0: the library's default, one shard V/T; "
                         "V: the whole vocabulary at once)")
@@ -88,18 +88,18 @@ def parse_args():
 
 
 # DRAM bytes (read + write) per GEMM stage (one 2NHV contraction, summed over
-# its token-chunk launches) of the tcgen05 GEMM kernel in the fused v128k step
+# its token-chunk launches) of the tcgen05 GEMM kernels in the fused v128k step
 # with the default bounded workspace, from one ncu capture
 # (profiles/launches_fused_step_v128k.md: mean of the three stages over four
-# steps).  They describe the kernel built from the sources hashed here; once
+# steps).  They describe the kernels built from the sources hashed here; once
 # those change, `traffic` is reported as null until a new capture replaces the
 # number.
 GEMM_TRAFFIC = {"workload": "v128k", "path": "fused", "gemm_variant": "single", "token_chunk": 0,
-                "bytes_per_stage": 20.57e9,
-                "by_stage": {"lse_p_gemm": 11.83e9, "dw_gemm": 23.94e9, "dx_gemm": 25.95e9},
+                "bytes_per_stage": 19.65e9,
+                "by_stage": {"lse_p_gemm": 9.37e9, "dw_gemm": 25.99e9, "dx_gemm": 23.58e9},
                 "sources": ("vocab_lm_head_vp_b300/csrc/ce_bf16.cu", "vocab_lm_head_vp_b300/csrc/ptx.cuh",
                             "vocab_lm_head_vp_b300/csrc/umma_gemm.cuh", "vocab_lm_head_vp_b300/csrc/umma_gemm_2sm.cuh"),
-                "sha256": "d44ff05879df578b05910ecd5946deeb200a795f1d084fed7c448b253fd020e9"}
+                "sha256": "55891af739f93889dfb31d33b6f927279c4e030c1d6538c8d37e9560f03e5038"}
 
 
 def gemm_traffic(workload, path, variant, token_chunk):
@@ -449,6 +449,27 @@ def config_table(vp, dev, names, rank, world, barrier):
             torch.cuda.synchronize()
             ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
             assert all(vp.read_device_status(w) == 0 for w in ws)
+            # the same step captured once in a CUDA graph and replayed: the launches
+            # cost no host time, so a small workload shows its device time
+            graph = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                run()
+            torch.cuda.current_stream(dev).wait_stream(side)
+            with torch.cuda.graph(graph):
+                run()
+            graph.replay()
+            torch.cuda.synchronize()
+            barrier()
+            e0.record()
+            for _ in range(steps):
+                graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ms_graph = max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
+            assert all(vp.read_device_status(w) == 0 for w in ws)
+            del graph
             alg = 6.0 * N * H * V / (ms / 1e3) / 1e12
             exe = (6.0 if path == "fused" else 8.0) * N * H * V / (ms / 1e3) / 1e12
             rows.append({"workload": name, "path": path, "N": N, "H": H, "V": V, "T": T, "steps": steps,
@@ -456,13 +477,18 @@ def config_table(vp, dev, names, rank, world, barrier):
                          "tflops_algorithmic": alg, "tflops_executed": exe,
                          "pct_bf16_burst_algorithmic": 100.0 * alg / peaks["bf16_tflops"],
                          "pct_bf16_burst_executed": 100.0 * exe / peaks["bf16_tflops"],
+                         "ms_per_step_graph": ms_graph,
+                         "pct_bf16_burst_algorithmic_graph": 100.0 * 6.0 * N * H * V / (ms_graph / 1e3) / 1e12
+                         / peaks["bf16_tflops"],
                          "workspace_bytes": int(sum(w.numel() for w in ws)),
                          "l2": "inputs fit in L2" if (N + V) * H * 2 < 100e6 else "inputs larger than L2"})
             del ws, run
         del X, W, y, o
         torch.cuda.empty_cache()
-    return {"note": "library default workspaces (fused: saved probabilities <= 1 GiB; split: one shard's dZ); "
-                    "X, W drawn on the device; no L2 flush (MiniMind's inputs stay in L2)", "rows": rows}
+    return {"note": "library default workspaces (fused: saved probabilities <= 1.25 GiB; split: one shard's dZ); "
+                    "X, W drawn on the device; no L2 flush (MiniMind's inputs stay in L2); ms_per_step: the "
+                    "calls issued from Python every step; ms_per_step_graph: the same calls captured once in a "
+                    "CUDA graph and replayed", "rows": rows}
 
 
 # ------------------------------------------------------------------ our arm

@@ -53,6 +53,7 @@ __device__ __forceinline__ int64_t shard_slot(int t, int64_t Vs, int tile_v, int
 // Step 1, one thread per (token, shard): the shard's tile records, in tile
 // order, into (m_t, R_t), written over the record of the shard's first tile
 // (a record slot belongs to exactly one shard, so only this thread touches it).
+constexpr int kMergeBatch = 8;
 __global__ void shard_merge_kernel(float2* __restrict__ partial, int64_t N, int64_t Vs, int T, int tile_v,
                                    int maxseg) {
   const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -64,8 +65,22 @@ __global__ void shard_merge_kernel(float2* __restrict__ partial, int64_t N, int6
     // every record holds at least one logit: start from the shard's first one
     const float2 r0 = partial[(nb0 * maxseg + (t - static_cast<int>((nb0 * tile_v) / Vs))) * N + n];
     float mt = r0.x, rt = r0.y;
-    for (int64_t nb = nb0 + 1; nb <= (b - 1) / tile_v; ++nb) {
-      const int k = t - static_cast<int>((nb * tile_v) / Vs);   // slot of shard t inside tile nb
+    const int64_t nb_last = (b - 1) / tile_v;
+    int64_t nb = nb0 + 1;
+    // the records of kMergeBatch tiles are loaded before any is merged, so that
+    // their loads are in flight together; the merge order stays tile order
+    for (; nb + kMergeBatch - 1 <= nb_last; nb += kMergeBatch) {
+      float2 r[kMergeBatch];
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int k = t - static_cast<int>(((nb + u) * tile_v) / Vs);   // slot of shard t inside tile nb + u
+        r[u] = partial[((nb + u) * maxseg + k) * N + n];
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) merge_mr(mt, rt, r[u].x, r[u].y);
+    }
+    for (; nb <= nb_last; ++nb) {
+      const int k = t - static_cast<int>((nb * tile_v) / Vs);
       const float2 r = partial[(nb * maxseg + k) * N + n];
       merge_mr(mt, rt, r.x, r.y);
     }
@@ -132,7 +147,15 @@ __global__ void shard_stats_kernel(const float2* __restrict__ partial, const flo
   }
   const float2 r0 = partial[n];
   float m = r0.x, r = r0.y;
-  for (int64_t nb = 1; nb < ntiles; ++nb) {
+  int64_t nb = 1;
+  for (; nb + kMergeBatch - 1 < ntiles; nb += kMergeBatch) {   // loads in flight together, merged in order
+    float2 rec[kMergeBatch];
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) rec[u] = partial[(nb + u) * N + n];
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) merge_mr(m, r, rec[u].x, rec[u].y);
+  }
+  for (; nb < ntiles; ++nb) {
     const float2 rec = partial[nb * N + n];
     merge_mr(m, r, rec.x, rec.y);
   }
