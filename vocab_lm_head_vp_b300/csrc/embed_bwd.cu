@@ -15,7 +15,8 @@
 //      padding, sorted: blocks build and bitonic-sort 512-key chunks in shared
 //      memory, then groups of up to 8 sorted runs merge in one pass each, every
 //      key placing itself at its rank (binary searches in the other runs of its
-//      group; the keys are distinct, the all-ones ones tie-broken by run).
+//      group, held in shared memory for groups of up to 16384 keys; the keys
+//      are distinct, the all-ones ones tie-broken by run).
 //      The sorted order groups tokens by id, by n within.  This step needs only
 //      the ids, so a caller can run it ahead (vp_embed_bwd_plan), off the
 //      critical path, and the rest later (vp_embed_bwd_planned).
@@ -31,6 +32,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "vp_internal.h"
 
 namespace vp {
@@ -40,7 +43,7 @@ constexpr uint64_t kSentinel = ~0ull;
 constexpr uint32_t kNoId = 0xffffffffu;
 constexpr int kChunk = 512;           // keys sorted per block in shared memory
 constexpr int kMergeWays = 8;         // sorted runs merged per pass
-constexpr int kSortThreads = 256;
+constexpr int kSortThreads = kChunk;   // one key per thread
 constexpr int kRun = 32;              // sorted positions per run
 constexpr int kRedThreads = 256;
 
@@ -52,34 +55,35 @@ __device__ __forceinline__ uint64_t make_key(const int64_t* __restrict__ ids, in
   return (id >= 0 && id < V) ? (static_cast<uint64_t>(id) << 32) | static_cast<uint64_t>(i) : kSentinel;
 }
 
-// Compare-exchange step j of merge size k on `len` keys in shared memory.
-// Pair p -> (i, i + j); the direction follows the key's index inside the
-// chunk, so the last merge (k = len) leaves the chunk ascending.
-__device__ __forceinline__ void smem_step(uint64_t* s, int len, int k, int j) {
-  for (int p = threadIdx.x; p < len / 2; p += blockDim.x) {
-    const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
-    const int l = i + j;
-    const bool asc = (i & k) == 0;
-    const uint64_t a = s[i], b = s[l];
-    if ((a > b) == asc) {
-      s[i] = b;
-      s[l] = a;
-    }
-  }
-  __syncthreads();
-}
-
 // The keys of each chunk of len = min(kChunk, n_pad) positions, bitonic-sorted
 // into ascending order (merge sizes 2..len), ready for the rank placement.
+// One key per thread: compare-exchange partners less than a warp apart trade
+// keys by shuffles, farther ones through shared memory.  A key's direction
+// follows its index inside the chunk, so the last merge (k = len) leaves the
+// chunk ascending.
 __global__ void __launch_bounds__(kSortThreads) keys_chunk_sort(const int64_t* __restrict__ ids, int64_t N,
                                                                 int64_t V, uint64_t* __restrict__ keys, int len) {
   __shared__ uint64_t s[kChunk];
+  const int t = threadIdx.x;
   const int64_t gbase = static_cast<int64_t>(blockIdx.x) * len;
-  for (int i = threadIdx.x; i < len; i += blockDim.x) s[i] = make_key(ids, N, V, gbase + i);
-  __syncthreads();
-  for (int k = 2; k <= len; k <<= 1)
-    for (int j = k >> 1; j > 0; j >>= 1) smem_step(s, len, k, j);
-  for (int i = threadIdx.x; i < len; i += blockDim.x) keys[gbase + i] = s[i];
+  uint64_t x = t < len ? make_key(ids, N, V, gbase + t) : kSentinel;
+  for (int k = 2; k <= len; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      uint64_t y;
+      if (j >= 32) {
+        s[t] = x;
+        __syncthreads();
+        y = s[t ^ j];
+        __syncthreads();
+      } else {
+        y = __shfl_xor_sync(0xffffffffu, x, j);
+      }
+      const bool asc = (t & k) == 0;
+      const bool keep_min = ((t & j) == 0) == asc;
+      x = keep_min ? (x < y ? x : y) : (x < y ? y : x);
+    }
+  }
+  if (t < len) keys[gbase + t] = x;
 }
 
 // Merge each group of G consecutive sorted runs of L keys (G, L, n_pad powers
@@ -117,6 +121,61 @@ __global__ void rank_merge_kernel(const uint64_t* __restrict__ in, uint64_t* __r
 #pragma unroll
   for (int r = 0; r < kMergeWays; ++r) pos += lo[r];
   out[first * L + pos] = key;
+}
+
+// The same placement with the group's runs first copied into shared memory
+// (groups of up to kSmemMergeKeys keys): block b places keys [part * per,
+// (part + 1) * per) of group b / parts, each by binary searches in the other
+// runs held in shared memory.  Every block of a group copies the whole group.
+constexpr int kSmemMergeKeys = 16384;   // 128 KB of keys
+constexpr int kSmemMergeThreads = 512;
+__global__ void __launch_bounds__(kSmemMergeThreads)
+    rank_merge_smem_kernel(const uint64_t* __restrict__ in, uint64_t* __restrict__ out, int64_t L, int G, int parts) {
+  extern __shared__ uint4 smem_keys[];
+  const uint64_t* sg = reinterpret_cast<const uint64_t*>(smem_keys);
+  const int64_t group = blockIdx.x / parts;
+  const int part = static_cast<int>(blockIdx.x % parts);
+  const int gsize = G * static_cast<int>(L);
+  const uint4* src = reinterpret_cast<const uint4*>(in + group * gsize);
+  const int nvec = gsize / 2;
+  for (int base = threadIdx.x; base < nvec; base += 8 * blockDim.x) {   // 8 loads in flight per thread
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (base + u * static_cast<int>(blockDim.x) < nvec) v[u] = src[base + u * blockDim.x];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (base + u * static_cast<int>(blockDim.x) < nvec) smem_keys[base + u * blockDim.x] = v[u];
+  }
+  __syncthreads();
+  const int per = gsize / parts, Li = static_cast<int>(L);
+  for (int j = part * per + threadIdx.x; j < (part + 1) * per; j += blockDim.x) {
+    const int run = j / Li;
+    const uint64_t key = sg[j];
+    int lo[kMergeWays], hi[kMergeWays];
+#pragma unroll
+    for (int r = 0; r < kMergeWays; ++r) {
+      lo[r] = 0;
+      hi[r] = (r < G && r != run) ? Li : 0;   // no search in the own run or past the group
+    }
+    for (int span = Li; span > 0; span >>= 1) {   // the searches advance in lockstep
+#pragma unroll
+      for (int r = 0; r < kMergeWays; ++r) {
+        if (lo[r] < hi[r]) {
+          const int mid = (lo[r] + hi[r]) >> 1;
+          const uint64_t x = sg[r * Li + mid];
+          if (r < run ? x <= key : x < key)
+            lo[r] = mid + 1;
+          else
+            hi[r] = mid;
+        }
+      }
+    }
+    int pos = j - run * Li;
+#pragma unroll
+    for (int r = 0; r < kMergeWays; ++r) pos += lo[r];
+    out[group * gsize + pos] = key;
+  }
 }
 
 // 16 bytes of an upstream row as fp32 values: 8 bf16 or 4 f32.
@@ -281,6 +340,19 @@ __global__ void __launch_bounds__(kRedThreads)
   add_to<ESIZE>(dW + static_cast<int64_t>(id) * H + col, a);
 }
 
+// The shared-memory merge's opt-in to kSmemMergeKeys keys of dynamic shared
+// memory, made once per device.
+cudaError_t allow_smem_merge() {
+  static std::atomic<int> done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(rank_merge_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemMergeKeys * sizeof(uint64_t)));
+  if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+  return e;
+}
+
 int64_t pad_pow2(int64_t n) {
   int64_t p = 2;
   while (p < n) p <<= 1;
@@ -312,7 +384,19 @@ cudaError_t embed_bwd_sort(const int64_t* ids, int64_t N, int64_t V, void* works
   keys_chunk_sort<<<static_cast<unsigned>(n_pad / len), kSortThreads, 0, stream>>>(ids, N, V, keys, len);
   for (int64_t L = len; L < n_pad;) {
     const int G = static_cast<int>(n_pad / L < kMergeWays ? n_pad / L : kMergeWays);
-    rank_merge_kernel<<<static_cast<unsigned>((n_pad + 255) / 256), 256, 0, stream>>>(keys, spare, n_pad, L, G);
+    const int64_t gsize = G * L;
+    if (gsize <= kSmemMergeKeys) {
+      const size_t smem = size_t(gsize) * sizeof(uint64_t);
+      if (smem > 48 * 1024) {
+        const cudaError_t e = allow_smem_merge();
+        if (e != cudaSuccess) return e;
+      }
+      const int parts = static_cast<int>(gsize / kChunk);   // kChunk keys placed per block
+      rank_merge_smem_kernel<<<static_cast<unsigned>(n_pad / gsize * parts), kSmemMergeThreads, smem, stream>>>(
+          keys, spare, L, G, parts);
+    } else {
+      rank_merge_kernel<<<static_cast<unsigned>((n_pad + 255) / 256), 256, 0, stream>>>(keys, spare, n_pad, L, G);
+    }
     uint64_t* t = keys;
     keys = spare;
     spare = t;
