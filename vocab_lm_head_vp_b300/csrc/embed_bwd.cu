@@ -301,42 +301,60 @@ __global__ void __launch_bounds__(kRedThreads)
   const uint32_t id = key_id(key_at(keys, n_pad, last));
   if (id >= V || key_id(key_at(keys, n_pad, last + 1)) != id) return;   // nothing continues past run r
   if (key_id(key_at(keys, n_pad, r * kRun - 1)) == id) return;              // the segment started earlier
+  // The run where the segment ends (its head slot is the last part): the one
+  // before the first later run whose first key has another id.  Warp 0 reads
+  // the first keys of 32 runs at a time.
+  __shared__ int64_t end_shared;
+  if (threadIdx.x < 32) {
+    int64_t e = -1;
+    for (int64_t base = r + 1; e < 0 && base < runs; base += 32) {
+      const int64_t q = base + threadIdx.x;
+      const bool other = q >= runs || key_id(keys[q * kRun]) != id;
+      const unsigned m = __ballot_sync(0xffffffffu, other);
+      if (m) e = base + __ffs(m) - 2;
+    }
+    if (threadIdx.x == 0) end_shared = e < 0 ? runs - 1 : e;
+  }
+  __syncthreads();
+  const int64_t end_run = end_shared;
   const int64_t v = static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x;
   if (v >= rowvec) return;
-  // the segment's last position: just before the first key with a larger id
-  const uint64_t bound = (static_cast<uint64_t>(id) + 1) << 32;
-  int64_t lo = last + 1, hi = n_pad;
-  while (lo < hi) {
-    const int64_t mid = (lo + hi) >> 1;
-    if (keys[mid] < bound)
-      lo = mid + 1;
-    else
-      hi = mid;
-  }
-  int64_t end_run = (lo - 1) / kRun;   // the run where the segment ends (its head slot is the last part)
-  if (end_run >= runs) end_run = runs - 1;
   constexpr int kN = Vec<ESIZE>::kN;
   const int64_t col = v * kN;
-  float s[kN];
+  // the tail of run r, then the head slots of runs r+1 .. end_run (8 runs'
+  // 16-byte vectors in flight at a time), added in run order
+  constexpr int kV4 = kN / 4;
+  float4 s[kV4];
 #pragma unroll
-  for (int q = 0; q < kN; ++q) s[q] = tail[r * H + col + q];
-  // head slots of runs r+1 .. end_run, loaded 8 runs at a time, added in run order
+  for (int q = 0; q < kV4; ++q) s[q] = reinterpret_cast<const float4*>(tail + r * H + col)[q];
   for (int64_t r0 = r + 1; r0 <= end_run; r0 += 8) {
-    float h[8][kN];
+    float4 h[8][kV4];
 #pragma unroll
     for (int u = 0; u < 8; ++u)
 #pragma unroll
-      for (int q = 0; q < kN; ++q) h[u][q] = r0 + u <= end_run ? head[(r0 + u) * H + col + q] : 0.f;
+      for (int q = 0; q < kV4; ++q)
+        h[u][q] = r0 + u <= end_run ? reinterpret_cast<const float4*>(head + (r0 + u) * H + col)[q]
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int u = 0; u < 8; ++u)
       if (r0 + u <= end_run) {
 #pragma unroll
-        for (int q = 0; q < kN; ++q) s[q] += h[u][q];
+        for (int q = 0; q < kV4; ++q) {
+          s[q].x += h[u][q].x;
+          s[q].y += h[u][q].y;
+          s[q].z += h[u][q].z;
+          s[q].w += h[u][q].w;
+        }
       }
   }
   Vec<ESIZE> a;
 #pragma unroll
-  for (int q = 0; q < kN; ++q) a.v[q] = s[q];
+  for (int q = 0; q < kV4; ++q) {
+    a.v[4 * q] = s[q].x;
+    a.v[4 * q + 1] = s[q].y;
+    a.v[4 * q + 2] = s[q].z;
+    a.v[4 * q + 3] = s[q].w;
+  }
   add_to<ESIZE>(dW + static_cast<int64_t>(id) * H + col, a);
 }
 
