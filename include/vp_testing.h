@@ -45,7 +45,8 @@ vp_status vp_test_set_gemm_variant(int variant);
 
 /*
  * vp_test_set_wait_fault -- exercise the bounded waits of the tcgen05 GEMMs.
- * Applies to every later bf16 GEMM launch of this process (one-SM form):
+ * Applies to every later bf16 GEMM launch of this process (one-SM and SM-pair
+ * forms; in a pair, both CTAs' producers, or the leader's MMA issuer):
  *   mode 0: normal operation (the default);
  *   mode 1: the TMA producer issues no load, so the MMA issuer's wait for
  *           data runs out (VP_DEV_TIMEOUT_MMA) and the epilogue's wait for an
@@ -58,8 +59,8 @@ vp_status vp_test_set_gemm_variant(int variant);
  *           the default (1 s).
  * A CTA that gives up drains what it issued, frees its tensor memory and
  * exits; the call's forward outputs (loss, lse, shard statistics) come out NaN
- * and the workspace's status word holds the bits.  The SM-pair GEMM form
- * honours wait_ns but not mode.  Process-global, not thread-safe.
+ * and the workspace's status word holds the bits.  Process-global, not
+ * thread-safe.
  */
 vp_status vp_test_set_wait_fault(int mode, uint64_t wait_ns);
 

@@ -26,8 +26,9 @@ PRODUCER, MMA, EPILOGUE = 0x1, 0x2, 0x4
 
 @pytest.fixture
 def inp():
-    # H = 512: 8 K blocks per tile, more than the 4 pipeline stages, so a
-    # producer whose stages are never released blocks with loads in flight
+    # H = 512: 8 K blocks per tile, more than the pipeline's 4 stages (6 on SM
+    # pairs), so a producer whose stages are never released blocks with loads
+    # in flight
     return synth.small_case(256, 512, 1024, 2, "bf16", seed=31)
 
 
@@ -35,6 +36,7 @@ def inp():
 def _restore():
     yield
     vp.set_wait_fault(0, 0)
+    vp.set_gemm_variant(0)
 
 
 def _normal_call_matches_oracle(inp):
@@ -49,9 +51,11 @@ def _normal_call_matches_oracle(inp):
     assert rel_fro(np64(dX), b["dX"]) <= 2e-2 and rel_fro(np64(dW), b["dW"]) <= 2e-2
 
 
+@pytest.mark.parametrize("variant", [0, 1])   # the forward GEMM on one SM per tile, or on SM pairs
 @pytest.mark.parametrize("mode,bits", [(1, MMA | EPILOGUE), (2, PRODUCER | EPILOGUE)])
-def test_forward_wait_runs_out_then_recovers(inp, mode, bits):
+def test_forward_wait_runs_out_then_recovers(inp, mode, bits, variant):
     X, W, y = dev_inputs(inp)
+    vp.set_gemm_variant(variant)
     vp.set_wait_fault(mode, WAIT_NS)
     f = vp.lmhead_ce_fwd(X, W, y, 2, shard_stats=True)
     torch.cuda.synchronize()
@@ -67,7 +71,8 @@ def test_fused_call_reports_and_recovers(inp):
     vp.set_wait_fault(2, WAIT_NS)
     o = vp.lmhead_ce_fwd_bwd(X, W, y, 2)
     torch.cuda.synchronize()
-    # every GEMM of the call gave up (forward, dW, dX); the forward's outputs are NaN
+    # every GEMM of the call gave up (forward and dX on one SM per tile, dW^T on SM pairs);
+    # the forward's outputs are NaN
     assert vp.read_device_status(o["workspace"]) == PRODUCER | EPILOGUE
     assert torch.isnan(o["loss"]).all() and torch.isnan(o["lse"]).all()
     vp.set_wait_fault(0, 0)

@@ -573,7 +573,7 @@ int sk_max_pieces(int64_t tiles, int64_t num_k, int64_t G) {
 }
 
 // Diagnostic of the bounded waits (vp_test_set_wait_fault): a role of every
-// later one-SM GEMM launch that issues nothing, and the waits' time limit.
+// later GEMM launch that issues nothing, and the waits' time limit.
 int g_hold = kHoldNone;
 uint64_t g_wait_ns = kWaitTimeoutNs;
 
@@ -673,7 +673,7 @@ cudaError_t launch_gemm_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const 
   a.num_k = static_cast<int>((K + kBK - 1) / kBK);
   a.status = status;
   a.wait_ns = g_wait_ns;
-  a.hold = kHoldNone;   // the hold diagnostic covers the one-SM form only
+  a.hold = g_hold;
   a.sk_iters = 0;
   const int total = a.sched.num_m * a.sched.num_n;
   const int pairs = total < max_pairs ? total : max_pairs;

@@ -88,7 +88,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;
-      for (int tile = pair; tile < total; tile += npairs) {
+      const int first = args.hold == kHoldProducer ? total : pair;   // the diagnostic hold: issue nothing
+      for (int tile = first; tile < total; tile += npairs) {
         int mb, nb;
         args.sched.tile(tile, mb, nb);
         const int m0 = mb * kPairBM + static_cast<int>(half) * 128;
@@ -147,7 +148,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int tile = pair; tile < total; tile += npairs) {
+      const int first = args.hold == kHoldMma ? total : pair;   // the diagnostic hold: issue nothing
+      for (int tile = first; tile < total; tile += npairs) {
         if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort, args.wait_ns)) {
           record_failure(args.status, abort, 0x2u);
           break;
