@@ -68,9 +68,10 @@ def parse_args():
                    help="fused: one fwd+bwd call with saved probabilities; split: fwd, then bwd with recompute")
     p.add_argument("--other-path-steps", type=int, default=5, help="timed steps of the other path (0: skip)")
     p.add_argument("--embed-iters", type=int, default=20, help="launches per case of the gather microbench (0: skip)")
-    p.add_argument("--gemm-variant", choices=["single", "pair", "single128"], default="single",
-                   help="tcgen05 GEMM form: one SM per tile with dX in 256x256 tiles (default), 256x256 tiles on "
-                        "SM pairs, or 128x256 tiles on one SM for every GEMM")
+    p.add_argument("--gemm-variant", choices=["single", "pair", "single128", "mcast"], default="single",
+                   help="tcgen05 GEMM form: the default (one SM per logits and dX tile, dW^T on SM pairs), SM "
+                        "pairs for every GEMM, 128x256 tiles on one SM for every GEMM, or the default with the "
+                        "logits GEMMs in TMA-multicast clusters")
     p.add_argument("--token-chunk", type=int, default=0,
                    help="fused path: token rows per chunk the workspace is sized for (0: the library's bounded "
                         "default, saved probabilities <= 1.25 GiB; N: all tokens at once)")
@@ -512,7 +513,7 @@ def run_ours(args):
             time.sleep(1.0)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    vp.set_gemm_variant({"single": 0, "pair": 1, "single128": 2}[args.gemm_variant])
+    vp.set_gemm_variant({"single": 0, "pair": 1, "single128": 2, "mcast": 3}[args.gemm_variant])
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 

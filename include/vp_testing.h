@@ -37,7 +37,11 @@ vp_status vp_test_gemm_bf16(const void* A, const void* B, float* D, int64_t M, i
  *      128 x 256 tile, whichever fills the waves better; dW as dW^T = X^T dZ
  *      with each 256 x 256 tile on a pair of SMs (cta_group::2);
  *   1: each 256 x 256 tile of every GEMM on a pair of SMs;
- *   2: one SM per 128 x 256 tile for every GEMM, and dW = dZ^T X directly.
+ *   2: one SM per 128 x 256 tile for every GEMM, and dW = dZ^T X directly;
+ *   3: as 0, but the logits GEMMs run in clusters of two CTAs on vertically
+ *      adjacent 128 x 256 tiles, each CTA loading half of the shared W tile and
+ *      multicasting it into both (TMA multicast), each MMA on its own SM's
+ *      shared memory; bit-identical to form 0.
  * All compute the same results within rounding; this exists to compare them.
  * Other values: VP_ERR_INVALID_ARG.
  */

@@ -300,7 +300,7 @@ def test_results_repeatable():
     assert torch.equal(a[0]["loss"], b[0]["loss"]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
 def test_gemm_forms_agree_on_the_path(variant):
     """The split fwd/bwd with each GEMM form (the default: dX tiles chosen per
     launch, dW^T on SM pairs; SM pairs everywhere; one SM with 128-row tiles

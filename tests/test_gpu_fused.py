@@ -122,7 +122,7 @@ def test_fused_tiny_config_and_repeatable():
     assert torch.equal(a[0]["loss"], b[0]["loss"]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
 def test_fused_gemm_forms(variant):
     vp.set_gemm_variant(variant)
     try:
@@ -175,3 +175,22 @@ def test_autograd_with_saved_probabilities():
     b = ref.lmhead_ce_backward(inp.X, inp.W, inp.targets, inp.wl.V)
     assert rel_fro(np64(X.grad), 2.0 * b["dX"]) <= 2e-2
     assert rel_fro(np64(W.grad), 2.0 * b["dW"]) <= 2e-2
+
+
+def test_multicast_logits_bit_identical():
+    """GEMM form 3 runs the logits GEMMs in clusters of two CTAs that share the
+    W tile by TMA multicast, each CTA's MMAs on its own shared memory: the same
+    products in the same order as one SM per tile, so every output is
+    bit-identical (ragged N: the last cluster's second CTA has no rows)."""
+    inp = synth.small_case(333, 264, 1800, 6, "bf16", seed=78, ignore_frac=0.1)
+    outs = []
+    for variant in (0, 3):
+        vp.set_gemm_variant(variant)
+        try:
+            outs.append(_fused(inp, 6, token_chunk=256))
+        finally:
+            vp.set_gemm_variant(0)
+    (o0, x0, w0), (o3, x3, w3) = outs
+    for k in ("loss", "lse", "mean"):
+        assert torch.equal(o0[k], o3[k]), k
+    assert torch.equal(x0, x3) and torch.equal(w0, w3)

@@ -51,7 +51,7 @@ def _normal_call_matches_oracle(inp):
     assert rel_fro(np64(dX), b["dX"]) <= 2e-2 and rel_fro(np64(dW), b["dW"]) <= 2e-2
 
 
-@pytest.mark.parametrize("variant", [0, 1])   # the forward GEMM on one SM per tile, or on SM pairs
+@pytest.mark.parametrize("variant", [0, 1, 3])   # the forward GEMM on one SM per tile, on SM pairs, in multicast clusters
 @pytest.mark.parametrize("mode,bits", [(1, MMA | EPILOGUE), (2, PRODUCER | EPILOGUE)])
 def test_forward_wait_runs_out_then_recovers(inp, mode, bits, variant):
     X, W, y = dev_inputs(inp)

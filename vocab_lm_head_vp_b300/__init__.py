@@ -470,8 +470,10 @@ def test_gemm_bf16(A, B, a_mn_major=False, b_mn_major=False):
 
 
 def set_gemm_variant(variant) -> None:
-    """tcgen05 GEMM form: 0 / False (default) one SM per tile, dX in 256 x 256
-    tiles; 1 / True SM pairs; 2 one SM per 128 x 256 tile everywhere."""
+    """tcgen05 GEMM form: 0 / False (default) one SM per logits and dX tile
+    (dX tiles chosen per launch), dW^T on SM pairs; 1 / True SM pairs
+    everywhere; 2 one SM per 128 x 256 tile everywhere, dW in the direct form;
+    3 as 0 with the logits GEMMs in clusters that share W by TMA multicast."""
     _check("vp_test_set_gemm_variant", _load().vp_test_set_gemm_variant(int(variant)))
 
 

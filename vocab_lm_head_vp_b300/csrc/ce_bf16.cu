@@ -22,6 +22,7 @@
 
 #include "umma_gemm.cuh"
 #include "umma_gemm_2sm.cuh"
+#include "umma_gemm_mc.cuh"
 #include "vp_internal.h"
 
 namespace vp {
@@ -681,12 +682,62 @@ cudaError_t launch_gemm_2sm(const CUtensorMap& ta, const CUtensorMap& tb, const 
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, a, ep);
 }
 
+// One 128 x 256 tile per SM, the two CTAs of a cluster on vertically adjacent
+// tiles that share B by multicast (umma_gemm_mc_kernel).  K-major operands.
+template <class Epi>
+cudaError_t launch_gemm_mc(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, int64_t M,
+                           int64_t Ncols, int64_t K, const typename Epi::Params& ep, uint32_t* status,
+                           cudaStream_t stream, int group_m) {
+  auto kern = umma_gemm_mc_kernel<Epi>;
+  constexpr size_t smem = GemmShape<1>::kSmem + Epi::kStagingBytes;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static std::atomic<int> attr_done[kMaxDevices];
+  static std::atomic<int> pairs_cache[kMaxDevices];
+  const cudaError_t e = ensure_smem(kern, smem, attr_done);
+  if (e != cudaSuccess) return e;
+  const int dev = current_device();
+  int max_pairs = pairs_cache[dev].load(std::memory_order_relaxed);
+  if (max_pairs == 0) {
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
+    if (cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg) != cudaSuccess || max_pairs <= 0) {
+      cudaGetLastError();
+      max_pairs = sm_count() / 2;
+    }
+    pairs_cache[dev].store(max_pairs, std::memory_order_relaxed);
+  }
+  GemmArgs a;
+  a.sched.num_m = static_cast<int>((M + kPairBM - 1) / kPairBM);
+  a.sched.num_n = static_cast<int>((Ncols + kBN - 1) / kBN);
+  a.sched.group_m = group_m < 1 ? 1 : group_m;
+  a.num_k = static_cast<int>((K + kBK - 1) / kBK);
+  a.status = status;
+  a.wait_ns = g_wait_ns;
+  a.hold = g_hold;
+  a.sk_iters = 0;
+  const int total = a.sched.num_m * a.sched.num_n;
+  const int pairs = total < max_pairs ? total : max_pairs;
+  cfg.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, a, ep);
+}
+
 // GEMM form (vp_test_set_gemm_variant): 0 (default) one SM per tile for the
 // logits and dX (dX tiles by dx_plan), dW^T on SM pairs; 1 SM pairs
 // (cta_group::2, 256 x 256 tiles) everywhere; 2 one SM per 128 x 256 tile
 // everywhere, dW in the direct form.
 int g_variant = 0;
 bool pair_kernels() { return g_variant == 1; }
+// Form 3: as form 0, the logits GEMMs in multicast clusters (launch_gemm_mc).
+bool logits_multicast() { return g_variant == 3; }
 
 // B operand K-major box rows: 256 for one SM, 128 (its half) for a CTA pair.
 int kmajor_b_box_rows() { return pair_kernels() ? 128 : kBN; }
@@ -763,7 +814,7 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const float* __restrict__
 
 }  // namespace
 
-void set_gemm_variant(int variant) { g_variant = (variant == 1 || variant == 2) ? variant : 0; }
+void set_gemm_variant(int variant) { g_variant = (variant >= 1 && variant <= 3) ? variant : 0; }
 
 bool dw_through_xt() { return g_variant != 2; }
 
@@ -817,8 +868,12 @@ cudaError_t bf16_lse_stats(const void* X, const void* W, const int64_t* targets,
                            cudaStream_t stream, int64_t y_off) {
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, X, N, H, H, kBK, kBM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tb, W, V, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, W, V, H, H, kBK, logits_multicast() ? 128 : kmajor_b_box_rows()))
+    return cudaErrorInvalidValue;
   EpiLseStats::Params p{partial, zy, targets, N, V, Vs, maxseg, nullptr, y_off};
+  if (logits_multicast())
+    return launch_gemm_mc<EpiLseStats>(ta, tb, ta, N, V, H, p, status, stream,
+                                       (logits_group_rows(N) + kPairBM - 1) / kPairBM);
   return launch_any<false, false, EpiLseStats>(ta, tb, ta, N, V, H, p, status, stream, logits_group_rows(N));
 }
 
@@ -827,10 +882,14 @@ cudaError_t bf16_lse_stats_p(const void* X, const void* W, const int64_t* target
                              uint32_t* status, cudaStream_t stream) {
   CUtensorMap ta, tb, tc;
   if (!make_tmap_bf16(&ta, X, N, H, H, kBK, kBM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tb, W, V, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, W, V, H, H, kBK, logits_multicast() ? 128 : kmajor_b_box_rows()))
+    return cudaErrorInvalidValue;
   // fp16 boxes of 32 rows x 64 columns (128 bytes), clipped at V columns and N rows
   if (!make_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, P, N, V, ldp, 64, 32)) return cudaErrorInvalidValue;
   EpiLseStatsP::Params p{partial, zy, targets, N, V, Vs, maxseg, tmax, 0};
+  if (logits_multicast())
+    return launch_gemm_mc<EpiLseStatsP>(ta, tb, tc, N, V, H, p, status, stream,
+                                        (logits_group_rows(N) + kPairBM - 1) / kPairBM);
   return launch_any<false, false, EpiLseStatsP>(ta, tb, tc, N, V, H, p, status, stream, logits_group_rows(N));
 }
 
@@ -840,9 +899,13 @@ cudaError_t bf16_dz_chunk(const void* X, const void* W, const int64_t* targets, 
   CUtensorMap ta, tb, tc;
   const uint8_t* Wc = static_cast<const uint8_t*>(W) + c0 * H * 2;
   if (!make_tmap_bf16(&ta, X, N, H, H, kBK, kBM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tb, Wc, Vc, H, H, kBK, kmajor_b_box_rows())) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, Wc, Vc, H, H, kBK, logits_multicast() ? 128 : kmajor_b_box_rows()))
+    return cudaErrorInvalidValue;
   if (!make_store_tmap(&tc, true, dz, N, Vc, ldz)) return cudaErrorInvalidValue;
   EpiDZ::Params p{lse, g, targets, N, y_off + c0, Vc};
+  if (logits_multicast())
+    return launch_gemm_mc<EpiDZ>(ta, tb, tc, N, Vc, H, p, status, stream,
+                                 (logits_group_rows(N) + kPairBM - 1) / kPairBM);
   return launch_any<false, false, EpiDZ>(ta, tb, tc, N, Vc, H, p, status, stream, logits_group_rows(N));
 }
 

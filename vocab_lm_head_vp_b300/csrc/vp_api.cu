@@ -761,7 +761,7 @@ VP_EXPORT const char* vp_stage_name(int stage) {
 }
 
 VP_EXPORT vp_status vp_test_set_gemm_variant(int variant) {
-  if (variant < 0 || variant > 2) return VP_ERR_INVALID_ARG;
+  if (variant < 0 || variant > 3) return VP_ERR_INVALID_ARG;
   set_gemm_variant(variant);
   return VP_OK;
 }
