@@ -457,31 +457,6 @@ struct EpiStoreT {
   }
 };
 
-// out[c][r] = in[r][c] for a bf16 [rows][cols] matrix; cols a multiple of 8.
-// 64 x 64 tiles through shared memory, 16-byte loads along the input rows.
-__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __restrict__ in, int64_t rows,
-                                                             int64_t cols, int64_t ld_in, uint16_t* __restrict__ out,
-                                                             int64_t ld_out) {
-  __shared__ uint16_t t[64][64 + 2];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, c0 = static_cast<int64_t>(blockIdx.x) * 64;
-  for (int e = threadIdx.x; e < 64 * 8; e += blockDim.x) {
-    const int r = e >> 3, cv = (e & 7) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r0 + r < rows && c0 + cv < cols) v = *reinterpret_cast<const uint4*>(in + (r0 + r) * ld_in + c0 + cv);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      t[r][cv + 2 * q] = static_cast<uint16_t>(w[q] & 0xffffu);
-      t[r][cv + 2 * q + 1] = static_cast<uint16_t>(w[q] >> 16);
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < 64 * 64; e += blockDim.x) {
-    const int c = e >> 6, r = e & 63;
-    if (c0 + c < cols && r0 + r < rows) out[(c0 + c) * ld_out + r0 + r] = t[r][c];
-  }
-}
-
 // ------------------------------------------------------------------ host side
 namespace {
 
@@ -959,14 +934,6 @@ cudaError_t bf16_dw_chunk(const void* dz, int64_t ldz, const void* X, int64_t N,
   if (!make_store_tmap(&tc, false, out, Vc, H, H)) return cudaErrorInvalidValue;
   EpiStore::Params p{accumulate ? out : nullptr, H, Vc, H, accumulate ? kAddF32 : kStoreF32};
   return launch_any<true, true, EpiStore>(ta, tb, tc, Vc, H, N, p, status, stream, VP_GROUP_ROWS_DW);
-}
-
-cudaError_t transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out, int64_t ld_out,
-                           cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
-  transpose_bf16_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(in), rows, cols, ld_in,
-                                                  static_cast<uint16_t*>(out), ld_out);
-  return cudaGetLastError();
 }
 
 cudaError_t bf16_dwt_chunk(const void* Xt, int64_t ldxt, const void* dz, int64_t ldz, int64_t N, int64_t H,
