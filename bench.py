@@ -96,11 +96,11 @@ def parse_args():
 # those change, `traffic` is reported as null until a new capture replaces the
 # number.
 GEMM_TRAFFIC = {"workload": "v128k", "path": "fused", "gemm_variant": "single", "token_chunk": 0,
-                "bytes_per_stage": 19.66e9,
-                "by_stage": {"lse_p_gemm": 9.18e9, "dw_gemm": 25.02e9, "dx_gemm": 24.79e9},
+                "bytes_per_stage": 20.20e9,
+                "by_stage": {"lse_p_gemm": 9.19e9, "dw_gemm": 25.58e9, "dx_gemm": 25.84e9},
                 "sources": ("vocab_lm_head_vp_b300/csrc/ce_bf16.cu", "vocab_lm_head_vp_b300/csrc/ptx.cuh",
                             "vocab_lm_head_vp_b300/csrc/umma_gemm.cuh", "vocab_lm_head_vp_b300/csrc/umma_gemm_2sm.cuh"),
-                "sha256": "53c89426bc05a8562929d3d27d21349a089fc2fdf5a2738b98d86b868d0f15e4"}
+                "sha256": "3ed910d96c3df390ab69bcdff452744b3b862f810c002d2373770e1481f851c2"}
 
 
 def gemm_traffic(workload, path, variant, token_chunk):

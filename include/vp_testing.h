@@ -81,8 +81,8 @@ vp_status vp_test_set_wait_fault(int mode, uint64_t wait_ns);
  *   (vp_stage_timing_dropped), so a harness can reject partial totals.
  * vp_stage_timing_read(ms, counts, n): waits for the recorded events and
  *   writes, for stage s < n, the summed milliseconds and the number of
- *   kernels launched in the stage's timed regions (lse_merge is two kernels
- *   per region, embed_bwd several); returns the number of stages, or -1 on a
+ *   kernels launched in the stage's timed regions (embed_bwd several per
+ *   region); returns the number of stages, or -1 on a
  *   CUDA error.
  * vp_stage_timing_dropped(): timed regions not recorded since the last
  *   vp_stage_timing_enable because all max_launches slots were in use.

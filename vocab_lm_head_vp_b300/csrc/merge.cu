@@ -50,52 +50,53 @@ __device__ __forceinline__ int64_t shard_slot(int t, int64_t Vs, int tile_v, int
   return nb * maxseg + k;
 }
 
-// Step 1, one thread per (token, shard): the shard's tile records, in tile
-// order, into (m_t, R_t), written over the record of the shard's first tile
-// (a record slot belongs to exactly one shard, so only this thread touches it).
+// One block per 32 tokens, 8 warps.  Step 1, warp w for shards w, w + 8, ...
+// (lane = token): the shard's tile records, in tile order, into (m_t, R_t),
+// written over the record of the shard's first tile (a record slot belongs to
+// exactly one shard).  Step 2, warp 0 (one thread per token): the shards in
+// order t = 0..T-1.
 constexpr int kMergeBatch = 8;
-__global__ void shard_merge_kernel(float2* __restrict__ partial, int64_t N, int64_t Vs, int T, int tile_v,
-                                   int maxseg) {
-  const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (n >= N) return;
-  for (int t = blockIdx.y; t < T; t += gridDim.y) {
-    const int64_t a = static_cast<int64_t>(t) * Vs;
-    const int64_t b = a + Vs;
-    const int64_t nb0 = a / tile_v;
-    // every record holds at least one logit: start from the shard's first one
-    const float2 r0 = partial[(nb0 * maxseg + (t - static_cast<int>((nb0 * tile_v) / Vs))) * N + n];
-    float mt = r0.x, rt = r0.y;
-    const int64_t nb_last = (b - 1) / tile_v;
-    int64_t nb = nb0 + 1;
-    // the records of kMergeBatch tiles are loaded before any is merged, so that
-    // their loads are in flight together; the merge order stays tile order
-    for (; nb + kMergeBatch - 1 <= nb_last; nb += kMergeBatch) {
-      float2 r[kMergeBatch];
+constexpr int kMergeTokens = 32;
+constexpr int kMergeWarps = 8;
+__global__ void __launch_bounds__(kMergeTokens * kMergeWarps)
+    lse_merge_kernel(float2* __restrict__ partial, const float* __restrict__ zy, const int64_t* __restrict__ targets,
+                     int64_t N, int64_t V, int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index,
+                     float* __restrict__ loss, float* __restrict__ lse, float* __restrict__ shard_stats,
+                     int64_t ss_ld, const uint32_t* __restrict__ status) {
+  const int lane = threadIdx.x % kMergeTokens, w = threadIdx.x / kMergeTokens;
+  const int64_t n = static_cast<int64_t>(blockIdx.x) * kMergeTokens + lane;
+  if (n < N) {
+    for (int t = w; t < T; t += kMergeWarps) {
+      const int64_t a = static_cast<int64_t>(t) * Vs;
+      const int64_t b = a + Vs;
+      const int64_t nb0 = a / tile_v;
+      // every record holds at least one logit: start from the shard's first one
+      const float2 r0 = partial[(nb0 * maxseg + (t - static_cast<int>((nb0 * tile_v) / Vs))) * N + n];
+      float mt = r0.x, rt = r0.y;
+      const int64_t nb_last = (b - 1) / tile_v;
+      int64_t nb = nb0 + 1;
+      // the records of kMergeBatch tiles are loaded before any is merged, so that
+      // their loads are in flight together; the merge order stays tile order
+      for (; nb + kMergeBatch - 1 <= nb_last; nb += kMergeBatch) {
+        float2 r[kMergeBatch];
 #pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        const int k = t - static_cast<int>(((nb + u) * tile_v) / Vs);   // slot of shard t inside tile nb + u
-        r[u] = partial[((nb + u) * maxseg + k) * N + n];
+        for (int u = 0; u < kMergeBatch; ++u) {
+          const int k = t - static_cast<int>(((nb + u) * tile_v) / Vs);   // slot of shard t inside tile nb + u
+          r[u] = partial[((nb + u) * maxseg + k) * N + n];
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) merge_mr(mt, rt, r[u].x, r[u].y);
       }
-#pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) merge_mr(mt, rt, r[u].x, r[u].y);
+      for (; nb <= nb_last; ++nb) {
+        const int k = t - static_cast<int>((nb * tile_v) / Vs);
+        const float2 r = partial[(nb * maxseg + k) * N + n];
+        merge_mr(mt, rt, r.x, r.y);
+      }
+      partial[shard_slot(t, Vs, tile_v, maxseg) * N + n] = make_float2(mt, rt);
     }
-    for (; nb <= nb_last; ++nb) {
-      const int k = t - static_cast<int>((nb * tile_v) / Vs);
-      const float2 r = partial[(nb * maxseg + k) * N + n];
-      merge_mr(mt, rt, r.x, r.y);
-    }
-    partial[shard_slot(t, Vs, tile_v, maxseg) * N + n] = make_float2(mt, rt);
   }
-}
-
-// Step 2, one thread per token: the shards in order t = 0..T-1.
-__global__ void lse_merge_kernel(const float2* __restrict__ partial, const float* __restrict__ zy,
-                                 const int64_t* __restrict__ targets, int64_t N, int64_t V, int64_t Vs, int T,
-                                 int tile_v, int maxseg, int64_t ignore_index, float* __restrict__ loss,
-                                 float* __restrict__ lse, float* __restrict__ shard_stats, int64_t ss_ld,
-                                 const uint32_t* __restrict__ status) {
-  const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (n >= N) return;
+  __syncthreads();   // every shard's (m_t, R_t) of the block's tokens is written
+  if (w != 0 || n >= N) return;
   if (status && *status != 0u) {
     const float nan = __int_as_float(0x7fc00000);
     lse[n] = nan;
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(kRedThreads) loss_mean_kernel(const float* __r
   __shared__ int s_bad[kRedThreads];
   double sum = 0.0;
   int nv = 0, nbad = 0;
+#pragma unroll 4
   for (int64_t n = threadIdx.x; n < N; n += kRedThreads) {
     const int64_t y = targets[n];
     const bool valid = y >= 0 && y < V && y != ignore_index;
@@ -233,6 +235,7 @@ __global__ void __launch_bounds__(kRedThreads) upstream_scale_kernel(const int64
                                                                      float* __restrict__ g) {
   __shared__ int s_valid[kRedThreads];
   int nv = 0;
+#pragma unroll 4
   for (int64_t n = threadIdx.x; n < N; n += kRedThreads) {
     const int64_t y = targets[n];
     nv += (y >= 0 && y < V && y != ignore_index);
@@ -244,6 +247,7 @@ __global__ void __launch_bounds__(kRedThreads) upstream_scale_kernel(const int64
     __syncthreads();
   }
   const float inv = (dmean ? *dmean : 1.0f) / static_cast<float>(s_valid[0] > 1 ? s_valid[0] : 1);
+#pragma unroll 4
   for (int64_t n = threadIdx.x; n < N; n += kRedThreads) {
     const int64_t y = targets[n];
     const bool valid = y >= 0 && y < V && y != ignore_index;
@@ -256,12 +260,9 @@ __global__ void __launch_bounds__(kRedThreads) upstream_scale_kernel(const int64
 cudaError_t lse_merge_ld(float2* partial, const float* zy, const int64_t* targets, int64_t N, int64_t V,
                          int64_t Vs, int T, int tile_v, int maxseg, int64_t ignore_index, float* loss, float* lse,
                          float* shard_stats, int64_t ss_ld, const uint32_t* status, cudaStream_t stream) {
-  const int threads = 256;
-  const int64_t blocks = (N + threads - 1) / threads;
-  const dim3 grid1(static_cast<unsigned>(blocks), static_cast<unsigned>(T < 65535 ? T : 65535));
-  // the records are scratch of this call: step 1 leaves each shard's merge in one of them
-  shard_merge_kernel<<<grid1, threads, 0, stream>>>(partial, N, Vs, T, tile_v, maxseg);
-  lse_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+  // the records are scratch of this call: the shard step leaves each shard's merge in one of them
+  const int64_t blocks = (N + kMergeTokens - 1) / kMergeTokens;
+  lse_merge_kernel<<<static_cast<unsigned>(blocks), kMergeTokens * kMergeWarps, 0, stream>>>(
       partial, zy, targets, N, V, Vs, T, tile_v, maxseg, ignore_index, loss, lse, shard_stats, ss_ld, status);
   return cudaGetLastError();
 }

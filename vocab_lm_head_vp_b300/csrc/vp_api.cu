@@ -154,7 +154,7 @@ int64_t fused_chunk_from_ws(int64_t N, int64_t H, int64_t V, int T, size_t ws) {
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
-constexpr int kMergeKernels = 2;   // lse_merge: the per-shard pass, then the per-token pass
+constexpr int kMergeKernels = 1;   // lse_merge: the per-shard and the per-token steps in one kernel
 
 // ---------------- optional per-launch event timing (vp_stage_timing_enable)
 enum Stage {
