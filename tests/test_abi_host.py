@@ -203,3 +203,29 @@ def test_stage_timing_off_records_nothing(lib):
     k = lib.vp_stage_timing_read(ms, None, 16)
     assert k > 0 and lib.vp_stage_name(k - 1) and not lib.vp_stage_name(k)
     assert all(x == 0.0 for x in ms)
+
+
+def test_suggested_workspaces_are_accepted(lib):
+    """For seeded random shapes and chunks, the bytes vp_lmhead_ce_workspace_size
+    suggests pass the call's workspace check: without a GPU the call then stops
+    at the driver (VP_ERR_CUDA), never at VP_ERR_WORKSPACE.  Small workspaces,
+    where the sections' 256-byte alignment weighs against the rows, included
+    (N=376, H=56, V=1512, T=7 with 128-token chunks was once refused)."""
+    import numpy as np
+    X, W, y, ws = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
+    loss, lse, dX, dW = P(0x50000), P(0x60000), P(0x70000), P(0x80000)
+    rng = np.random.default_rng(11)
+    shapes = [(376, 56, 1512, 7, 128)]
+    for _ in range(300):
+        T = int(rng.choice([1, 2, 3, 4, 7, 8, 16]))
+        shapes.append((int(rng.integers(1, 5000)), 8 * int(rng.integers(1, 80)), T * int(rng.integers(1, 600)), T,
+                       int(rng.choice([0, 128, 256, 384, 1000]))))
+    for N, H, V, T, chunk in shapes:
+        nb = vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, chunk)
+        code = lib.vp_lmhead_ce_fwd_bwd(X, W, y, None, None, N, H, V, T, -100, vp.VP_BF16, loss, lse, None, None,
+                                        None, dX, dW, ws, nb, None)
+        assert code == 4, (N, H, V, T, chunk, code)
+        vc = int(rng.choice([0, 256, 512, 1000]))
+        nb = vp.workspace_size(N, H, V, T, vp.VP_BF16, 1, vc)
+        code = lib.vp_lmhead_ce_bwd(X, W, y, lse, None, None, N, H, V, T, -100, vp.VP_BF16, dX, dW, ws, nb, None)
+        assert code == 4, (N, H, V, T, vc, code)

@@ -12,7 +12,7 @@ from test_gpu_fused import _fused
 
 pytestmark = pytest.mark.gpu
 IGN = -100
-NCASES = 24
+NCASES = 48
 
 
 def _draw(k):

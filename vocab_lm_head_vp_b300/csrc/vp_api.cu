@@ -50,16 +50,21 @@ BwdLayout bwd_layout_for_chunk(int64_t N, int64_t H, int64_t V, vp_dtype dt, int
   L.total = align_up(L.off_xt + (dt == VP_BF16 ? size_t(H) * L.ldxt * 2 : 0), kAlign);
   return L;
 }
-// Largest chunk that fits in ws bytes (0 if none does).
+// Largest chunk that fits in ws bytes (0 if none does): all V, else the most
+// whole tiles (the layout grows with the chunk, so a binary search over the
+// tile count is exact whatever the sections' alignment).
 int64_t bwd_chunk_from_ws(int64_t N, int64_t H, int64_t V, vp_dtype dt, size_t ws) {
   if (bwd_layout_for_chunk(N, H, V, dt, V).total <= ws) return V;
   const int64_t tile = bwd_tile(dt);
-  const size_t fixed = bwd_layout_for_chunk(N, H, V, dt, tile).total - size_t(N) * tile * esize_of(dt);
-  if (ws < fixed) return 0;
-  int64_t vc = int64_t((ws - fixed) / (size_t(N) * esize_of(dt))) / tile * tile;
-  while (vc >= tile && bwd_layout_for_chunk(N, H, V, dt, vc).total > ws) vc -= tile;
-  if (vc >= V) vc = V;
-  return vc >= tile || vc == V ? vc : 0;
+  int64_t lo = 0, hi = (V - 1) / tile;   // tiles per chunk, below V
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) / 2;
+    if (bwd_layout_for_chunk(N, H, V, dt, mid * tile).total <= ws)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo * tile;
 }
 
 // ---------------- fused workspace (bf16), token chunk Nc:
@@ -140,16 +145,21 @@ int64_t bwd_default_chunk(int64_t V, int T, vp_dtype dt) {
   const int64_t vc = (V / T + tile - 1) / tile * tile;
   return vc >= V ? V : vc;
 }
-// Largest token chunk that fits in ws bytes: all N, else a multiple of 128 (0 if none fits).
+// Largest token chunk that fits in ws bytes: all N, else a multiple of 128 (0
+// if none fits).  The layout grows with the chunk, so a binary search over the
+// 128-row block count is exact; an estimate from the size of one row misjudges
+// small workspaces, where the sections' 256-byte alignment weighs.
 int64_t fused_chunk_from_ws(int64_t N, int64_t H, int64_t V, int T, size_t ws) {
   if (fused_layout(N, H, V, T, N).total <= ws) return N;
-  const size_t per_row = fused_layout(N, H, V, T, 2).total - fused_layout(N, H, V, T, 1).total;
-  const size_t fixed = fused_layout(N, H, V, T, 0).total;
-  if (ws < fixed || per_row == 0) return 0;
-  int64_t nc = int64_t((ws - fixed) / per_row) / kFusedRowAlign * kFusedRowAlign;
-  if (nc >= N) nc = (N - 1) / kFusedRowAlign * kFusedRowAlign;
-  while (nc >= kFusedRowAlign && fused_layout(N, H, V, T, nc).total > ws) nc -= kFusedRowAlign;
-  return nc >= kFusedRowAlign ? nc : 0;
+  int64_t lo = 0, hi = (N - 1) / kFusedRowAlign;   // 128-row blocks per chunk, below N
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) / 2;
+    if (fused_layout(N, H, V, T, mid * kFusedRowAlign).total <= ws)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo * kFusedRowAlign;
 }
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
