@@ -33,6 +33,22 @@ def assert_loss_close(got, ref, dtype, what="loss"):
                            f"(ref {ref.flat[int(np.nanargmax(err))]:.6g})")
 
 
+def assert_lse_close(got, ref, inp, what="lse"):
+    """lse per token.  bf16: the loss tolerance.  fp32: lse = m + log1p(R) is
+    a smooth function of the logits with weights (the softmax) summing to 1, so
+    it moves by at most the largest logit error, an H-term fp32 dot product
+    held to gamma_H sum_i |x_i w_i| (Higham), plus the rounding of the sum of
+    exps, gamma_(V+8); and by rel 1e-5 of itself.  A relative bound alone would
+    be meaningless for an lse near zero (it changes sign with the logits)."""
+    wl = inp.wl
+    if wl.dtype == "bf16":
+        assert_loss_close(got, ref, "bf16", what=what)
+        return
+    A = np.abs(np.asarray(inp.X, np.float64)) @ np.abs(np.asarray(inp.W, np.float64)).T   # [N, V]
+    bound = 1e-5 * np.abs(np.asarray(ref, np.float64)) + gamma(wl.H) * A.max(axis=1) + gamma(wl.V + 8)
+    assert_within(what, got, ref, bound)
+
+
 def gamma(n, u=2.0 ** -24):
     """Higham's gamma_n = n u / (1 - n u): the relative bound of an n-term fp32 sum."""
     return n * u / (1.0 - n * u)
@@ -101,6 +117,23 @@ def term_magnitudes(dZ, g, y, cols=None):
     return M
 
 
+# The saved probabilities are fp16 relative to their tile's maximum: below
+# 2^-14 they are subnormal, with an absolute error up to 2^-25 (r15), scaled
+# by g and by exp(m_tile - lse) <= 1.  In units of u this adds 2^-25 / u to
+# every term of a bf16 row with g != 0.
+P16_FLOOR = 2.0 ** -25
+
+
+def with_p16_floor(M, g, dtype):
+    """M plus, for bf16, the fp16 quantum of the saved probabilities on every
+    entry of a row (the elementwise bound then holds for tiny probabilities too,
+    e.g. a batch of one token, where no larger term of a sum dilutes them)."""
+    if dtype != "bf16":
+        return M
+    M += (P16_FLOOR / elementwise_u(dtype)) * np.abs(np.asarray(g, np.float64))[:, None]
+    return M
+
+
 def elementwise_u(dtype):
     """The bound's factor: for bf16, 2^-7 covers the bf16 rounding of dZ
     (2^-9), the bf16 rounding of dX itself (2^-9), the fp16 rounding of saved
@@ -131,11 +164,12 @@ def assert_grads_elementwise(inp, dX, dW, b):
 
         |dX_gpu - dX| <= u (M |W|),      |dW_gpu - dW| <= u (M^T |X|)
 
-    with M from term_magnitudes and u from elementwise_u.  b is the oracle's
+    with M from term_magnitudes (plus the fp16 quantum of the saved
+    probabilities, with_p16_floor) and u from elementwise_u.  b is the oracle's
     backward (dZ, g, dX, dW).  A mistake confined to a few small entries (a
     ragged tail tile, a rarely targeted vocab row) fails this although the
     tensor's relative Frobenius error stays small."""
-    M = term_magnitudes(b["dZ"], b["g"], inp.targets)
+    M = with_p16_floor(term_magnitudes(b["dZ"], b["g"], inp.targets), b["g"], inp.wl.dtype)
     u = elementwise_u(inp.wl.dtype)
     assert_within("dX", np64(dX), b["dX"], u * abs_matmul(M, inp.W))
     assert_within("dW", np64(dW), b["dW"], u * abs_matmul(M.T, inp.X))

@@ -9,8 +9,8 @@ import oracle.ref as ref
 import synth
 import vocab_lm_head_vp_b300 as vp
 from golden_io import read
-from gpu_util import (assert_grads_elementwise, assert_loss_close, assert_stats_close, dev_inputs, grad_tol,
-                      np64, rel_fro)
+from gpu_util import (assert_grads_elementwise, assert_loss_close, assert_lse_close, assert_stats_close, dev_inputs,
+                      grad_tol, np64, rel_fro)
 
 pytestmark = pytest.mark.gpu
 IGN = -100
@@ -103,7 +103,7 @@ def _run(inp, T, ignore_index=IGN, dloss=None, vocab_chunk=None, shard_stats=Tru
 def _check(inp, T, f, dX, dW, ignore_index=IGN, dloss=None, check_stats=True):
     wl = inp.wl
     o = ref.lmhead_ce_forward(inp.X, inp.W, inp.targets, wl.V, T, ignore_index)
-    assert_loss_close(np64(f["lse"]), o["lse"], wl.dtype, what="lse")
+    assert_lse_close(np64(f["lse"]), o["lse"], inp)
     assert_loss_close(np64(f["loss"]), o["loss"], wl.dtype, what="loss")
     assert_loss_close(np64(f["mean"]), [o["mean"]], wl.dtype, what="mean")
     assert int(f["n_bad"].item()) == o["n_bad"]

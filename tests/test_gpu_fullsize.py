@@ -23,7 +23,7 @@ import oracle.ref as ref
 import synth
 import vocab_lm_head_vp_b300 as vp
 from gpu_util import (abs_matmul, assert_loss_close, assert_stats_close, assert_within, dev_inputs, elementwise_u,
-                      np64, rel_fro, term_magnitudes)
+                      np64, rel_fro, term_magnitudes, with_p16_floor)
 
 pytestmark = pytest.mark.gpu
 IGN = -100
@@ -53,7 +53,7 @@ def _dense(name):
     dZ = ref.grad_logits(Z, inp.targets, fwd["lse"], g)
     del Z
     dX, dW = ref.lmhead_grads(inp.X, inp.W, dZ)
-    M = term_magnitudes(dZ, g, inp.targets)
+    M = with_p16_floor(term_magnitudes(dZ, g, inp.targets), g, "bf16")
     del dZ
     u = elementwise_u("bf16")
     bx, bw = u * abs_matmul(M, inp.W), u * abs_matmul(M.T, inp.X)
@@ -74,13 +74,13 @@ def _sampled(name):
     rows = np.sort(rng.choice(wl.N, 256, replace=False))
     o = ref.lmhead_ce_rows(inp.X, inp.W, inp.targets, rows, n_valid)
     u = elementwise_u("bf16")
-    Mx = term_magnitudes(o["dZ"], o["g"], inp.targets[rows])
+    Mx = with_p16_floor(term_magnitudes(o["dZ"], o["g"], inp.targets[rows]), o["g"], "bf16")
     counts = np.bincount(inp.targets[valid], minlength=wl.V)
     never = np.flatnonzero(counts == 0)
     vrows = np.unique(np.concatenate([np.argsort(-counts, kind="stable")[:8], rng.choice(wl.V, 32, replace=False),
                                       rng.choice(never, 8, replace=False)]))
     want_w, dZv, g = ref.lmhead_ce_dw_rows(inp.X, inp.W, inp.targets, lse, vrows, n_valid, return_dz=True)
-    Mw = term_magnitudes(dZv, g, inp.targets, cols=vrows)
+    Mw = with_p16_floor(term_magnitudes(dZv, g, inp.targets, cols=vrows), g, "bf16")
     return {"inp": inp, "lse": lse, "loss": loss, "mean": float(loss.sum()) / max(1, n_valid),
             "n_valid": n_valid, "rows": rows, "dX_rows": o["dX"], "bx": u * abs_matmul(Mx, inp.W),
             "vrows": vrows, "dW_rows": want_w, "bw": u * abs_matmul(Mw.T, inp.X), "top8": np.argsort(-counts)[:8]}

@@ -11,7 +11,7 @@ import torch
 import oracle.ref as ref
 import synth
 import vocab_lm_head_vp_b300 as vp
-from gpu_util import (assert_grads_elementwise, assert_loss_close, assert_stats_close, dev_inputs, grad_tol, np64,
+from gpu_util import (assert_grads_elementwise, assert_loss_close, assert_lse_close, assert_stats_close, dev_inputs, grad_tol, np64,
                       rel_fro)
 from test_gpu_ce import _argmax_case
 
@@ -57,7 +57,7 @@ def test_shards_match_the_oracle(N, H, V, T, dtype):
     st = np64(stats)
     st[:, 1] += 1.0                      # R_t -> S_t = 1 + R_t, the oracle's statistic
     assert_stats_close(st, o["shard_stats"], inp, T)
-    assert_loss_close(np64(fwd["lse"]), o["lse"], dtype, what="lse")
+    assert_lse_close(np64(fwd["lse"]), o["lse"], inp)
     assert_loss_close(np64(fwd["loss"]), o["loss"], dtype, what="loss")
     assert_loss_close(np64(fwd["mean"]), [o["mean"]], dtype, what="mean")
     assert int(fwd["n_bad"].item()) == o["n_bad"] == 3
