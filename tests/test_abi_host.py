@@ -117,8 +117,9 @@ def test_fused_workspace_sizes(lib):
     assert half - SK < (full - SK) / 2 + N * 8 and half - SK > (full - SK) / 2 - N * V - XT(N, H)
     assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 100) == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 128)
     # default: saved probabilities of at most 1.25 GiB, in the chunk that fills the dX GEMM's
-    # waves best (4736 token rows of V = 128256: 592 tiles of 128 x 256, four waves of 148)
-    assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 2) == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 4736)
+    # waves best by the dX cost model (4608 token rows of V = 128256: 288 tiles of 256 x 256, two waves
+    # of 148, three chunks and one of 2560 rows)
+    assert vp.workspace_size(N, H, V, T, vp.VP_BF16, 2) == vp.workspace_size(N, H, V, T, vp.VP_BF16, 2, 4608)
     # small problems fit in one chunk by default
     assert vp.workspace_size(4096, 512, 6400, 2, vp.VP_BF16, 2) == vp.workspace_size(4096, 512, 6400, 2,
                                                                                         vp.VP_BF16, 2, 4096)

@@ -463,7 +463,7 @@ namespace {
 // Token rows per tile group of a logits GEMM over N rows: all of them when
 // they are few enough that X stays in L2 beside the W tiles in use (W then
 // streams from DRAM once), else VP_GROUP_ROWS_LOGITS.  A token chunk of the
-// fused call (e.g. 4736 rows) would otherwise end in a small group that
+// fused call (e.g. 4608 rows) would otherwise end in a small group that
 // streams all of W again for a few rows.
 int logits_group_rows(int64_t N) {
   return N <= VP_GROUP_ROWS_LOGITS_MAX ? static_cast<int>(N) : VP_GROUP_ROWS_LOGITS;
@@ -795,14 +795,17 @@ bool dw_through_xt() { return g_variant != 2; }
 
 // Relative time of a dX launch over `rows` token rows in units of one wave of
 // 128 x 256 tiles: its waves on the persistent grid, a 256-row wave counting
-// twice, a 128-row wave 4% more than half of that (it streams W twice as
-// often per row).  The tile shape with the lower cost is taken.  (256 x 256
-// tiles on SM pairs, which fill waves of 74 pairs, were measured slower for
-// this contraction than either one-SM form at equal wave counts.)
+// twice, a 128-row wave 15% more than half of that.  Unthrottled a 128-row
+// wave costs about 4% more (it streams W twice as often per row); under the
+// GPU's power cap the fused step measured fastest with 15%, which also moves
+// its token chunks (V = 128256: 4608 rows, not 4736).  The tile shape with
+// the lower cost is taken.  (256 x 256 tiles on SM pairs, which fill waves of
+// 74 pairs, were measured slower for this contraction than either one-SM form
+// at equal wave counts.)
 DxPlan dx_plan(int64_t rows, int64_t H) {
   const int64_t G = sm_count(), cols = (H + kBN - 1) / kBN;
   const auto waves = [&](int64_t tile_rows) { return ((rows + tile_rows - 1) / tile_rows * cols + G - 1) / G; };
-  const double c1 = 1.04 * static_cast<double>(waves(kBM)), c2 = 2.0 * static_cast<double>(waves(2 * kBM));
+  const double c1 = 1.15 * static_cast<double>(waves(kBM)), c2 = 2.0 * static_cast<double>(waves(2 * kBM));
   DxPlan p;
   const bool two = g_variant != 2 && c2 <= c1;
   p.rows = two ? 2 * kBM : kBM;

@@ -96,7 +96,7 @@ constexpr int64_t kFusedRowAlign = 128;   // token chunks are whole 128-row GEMM
 // Budget of the fused call's saved probabilities when the caller names no
 // token chunk: N_c x round8(V) 2-byte values stay below it (the logits are
 // never held for all N tokens at once).  1.25 GiB: at V = 128256 the chunk
-// that fills the dX GEMM's waves best within it holds 4736 tokens (1.2 GB).
+// that balanced_token_chunk picks within it holds 4608 tokens (1.18 GB).
 constexpr size_t kFusedDefaultSavedBytes = size_t(5) << 28;
 
 int64_t fused_default_chunk(int64_t N, int64_t V) {
