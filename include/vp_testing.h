@@ -48,6 +48,22 @@ vp_status vp_test_gemm_bf16(const void* A, const void* B, float* D, int64_t M, i
 vp_status vp_test_set_gemm_variant(int variant);
 
 /*
+ * vp_test_dx_plan -- how a bf16 dX GEMM (dX = dZ W, `rows` token rows, H
+ * output columns) would run on a grid of `sms` persistent CTAs under the
+ * current GEMM form, without launching anything (host arithmetic only):
+ *   tile_rows: 256 (two 128-row A blocks per CTA sharing each W block) or 128;
+ *   streamk:   1 when the launch splits tiles x K-blocks evenly over the CTAs
+ *              (fewer 256-row tiles than CTAs, but at least a quarter as many,
+ *              and whole waves well over the work), else 0;
+ *   cost:      the relative time the plan is chosen by, in waves of 128 x 256
+ *              tiles (a 256-row wave counting 2, a 128-row wave 1.15; for
+ *              stream-K the 128-row tiles per CTA).
+ * The fused call's default token chunk is chosen with the same costs.
+ * rows, H or sms <= 0, or a null output: VP_ERR_INVALID_ARG.
+ */
+vp_status vp_test_dx_plan(int64_t rows, int64_t H, int sms, int32_t* tile_rows, int32_t* streamk, double* cost);
+
+/*
  * vp_test_set_wait_fault -- exercise the bounded waits of the tcgen05 GEMMs.
  * Applies to every later bf16 GEMM launch of this process (one-SM and SM-pair
  * forms; in a pair, both CTAs' producers, or the leader's MMA issuer):

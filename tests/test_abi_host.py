@@ -230,3 +230,45 @@ def test_suggested_workspaces_are_accepted(lib):
         nb = vp.workspace_size(N, H, V, T, vp.VP_BF16, 1, vc)
         code = lib.vp_lmhead_ce_bwd(X, W, y, lse, None, None, N, H, V, T, -100, vp.VP_BF16, dX, dW, ws, nb, None)
         assert code == 4, (N, H, V, T, vc, code)
+
+
+def test_dx_plan_choices(lib):
+    """The dX GEMM's tile choice, host arithmetic only (cost in waves of
+    128 x 256 tiles on the persistent grid: a 256-row wave counts 2, a 128-row
+    wave 1.15; the lower cost wins, 256 rows on a tie)."""
+    vp.set_gemm_variant(0)
+    cases = [
+        # rows, H, SMs -> tile rows, stream-K, cost
+        # a V = 128256 token chunk: 576 tiles of 128 rows = 4 waves (4.6) against 288 of 256 rows = 2 waves (4)
+        (4608, 4096, 148, 256, False, 4.0),
+        # its 2560-row tail chunk: 320 tiles = 3 waves (3.45) against 160 = 2 waves (4)
+        (2560, 4096, 148, 128, False, 3.45),
+        # N = 8192 (V32k): 1024 tiles = 7 waves (8.05) against 512 = 4 waves (8)
+        (8192, 4096, 148, 256, False, 8.0),
+        # N = 16384, the split path's dX: 2048 = 14 waves (16.1) against 1024 = 7 waves (14)
+        (16384, 4096, 148, 256, False, 14.0),
+        # N = 32768, H = 5120 (20 column tiles): 5120 = 35 waves (40.25) against 2560 = 18 waves (36)
+        (32768, 5120, 148, 256, False, 36.0),
+        # MiniMind (H = 512, 2 column tiles): 64 tiles in one wave (1.15) against 32 (2); 32 tiles of
+        # 256 rows are fewer than a quarter of the SMs, so no stream-K
+        (4096, 512, 148, 128, False, 1.15),
+        # 40 tiles of 256 rows (>= 148 / 4, < 148) and one wave (1.15) for 80 tiles' work (0.54):
+        # stream-K over 256-row tiles, cost the work per CTA
+        (2560, 1024, 148, 256, True, 80 / 148),
+        # the same token chunk on 132 SMs: 576 tiles = 5 waves (5.75) against 288 = 3 waves (6)
+        (4608, 4096, 132, 128, False, 5.75),
+    ]
+    for rows, H, sms, tile_rows, streamk, cost in cases:
+        p = vp.dx_plan(rows, H, sms)
+        assert (p["tile_rows"], p["streamk"]) == (tile_rows, streamk), (rows, H, sms, p)
+        assert abs(p["cost"] - cost) < 1e-9, (rows, H, sms, p)
+    # GEMM form 2 keeps 128-row tiles and no stream-K
+    vp.set_gemm_variant(2)
+    try:
+        assert vp.dx_plan(8192, 4096, 148) == {"tile_rows": 128, "streamk": False, "cost": 1.15 * 7}
+    finally:
+        vp.set_gemm_variant(0)
+    d, sk, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
+    for args in [(0, 4096, 148), (4096, 0, 148), (4096, 4096, 0)]:
+        assert lib.vp_test_dx_plan(*args, ctypes.byref(d), ctypes.byref(sk), ctypes.byref(c)) == 1
+    assert lib.vp_test_dx_plan(4096, 4096, 148, None, ctypes.byref(sk), ctypes.byref(c)) == 1

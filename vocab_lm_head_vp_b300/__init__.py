@@ -88,6 +88,9 @@ def _load():
     L.vp_test_gemm_bf16.argtypes = [P, P, P, I64, I64, I64, U, U, P, P]
     L.vp_test_set_gemm_variant.restype = I32
     L.vp_test_set_gemm_variant.argtypes = [I32]
+    L.vp_test_dx_plan.restype = I32
+    L.vp_test_dx_plan.argtypes = [I64, I64, I32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                  ctypes.POINTER(ctypes.c_double)]
     L.vp_test_set_wait_fault.restype = I32
     L.vp_test_set_wait_fault.argtypes = [I32, ctypes.c_uint64]
     L.vp_lmhead_ce_fwd_noalloc.restype = I32
@@ -475,6 +478,16 @@ def set_gemm_variant(variant) -> None:
     everywhere; 2 one SM per 128 x 256 tile everywhere, dW in the direct form;
     3 as 0 with the logits GEMMs in clusters that share W by TMA multicast."""
     _check("vp_test_set_gemm_variant", _load().vp_test_set_gemm_variant(int(variant)))
+
+
+def dx_plan(rows: int, H: int, sms: int) -> dict:
+    """How a bf16 dX GEMM over `rows` token rows and H columns would run on
+    `sms` persistent CTAs (host arithmetic, no launch): tile rows (256 or
+    128), whether stream-K, and the wave cost the choice is made by."""
+    r, sk, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
+    _check("vp_test_dx_plan", _load().vp_test_dx_plan(int(rows), int(H), int(sms), ctypes.byref(r),
+                                                      ctypes.byref(sk), ctypes.byref(c)))
+    return {"tile_rows": r.value, "streamk": bool(sk.value), "cost": c.value}
 
 
 def set_wait_fault(mode: int, wait_ns: int = 0) -> None:

@@ -802,8 +802,10 @@ bool dw_through_xt() { return g_variant != 2; }
 // the lower cost is taken.  (256 x 256 tiles on SM pairs, which fill waves of
 // 74 pairs, were measured slower for this contraction than either one-SM form
 // at equal wave counts.)
-DxPlan dx_plan(int64_t rows, int64_t H) {
-  const int64_t G = sm_count(), cols = (H + kBN - 1) / kBN;
+DxPlan dx_plan(int64_t rows, int64_t H) { return dx_plan_on(rows, H, sm_count()); }
+
+DxPlan dx_plan_on(int64_t rows, int64_t H, int64_t G) {
+  const int64_t cols = (H + kBN - 1) / kBN;
   const auto waves = [&](int64_t tile_rows) { return ((rows + tile_rows - 1) / tile_rows * cols + G - 1) / G; };
   const double c1 = 1.15 * static_cast<double>(waves(kBM)), c2 = 2.0 * static_cast<double>(waves(2 * kBM));
   DxPlan p;

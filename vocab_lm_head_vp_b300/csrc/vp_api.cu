@@ -776,6 +776,16 @@ VP_EXPORT vp_status vp_test_set_gemm_variant(int variant) {
   return VP_OK;
 }
 
+VP_EXPORT vp_status vp_test_dx_plan(int64_t rows, int64_t H, int sms, int32_t* tile_rows, int32_t* streamk,
+                                    double* cost) {
+  if (rows <= 0 || H <= 0 || sms <= 0 || !tile_rows || !streamk || !cost) return VP_ERR_INVALID_ARG;
+  const DxPlan p = dx_plan_on(rows, H, sms);
+  *tile_rows = p.rows;
+  *streamk = p.streamk ? 1 : 0;
+  *cost = p.cost;
+  return VP_OK;
+}
+
 VP_EXPORT vp_status vp_test_set_wait_fault(int mode, uint64_t wait_ns) {
   if (mode < 0 || mode > 2) return VP_ERR_INVALID_ARG;
   set_wait_fault(mode, wait_ns);

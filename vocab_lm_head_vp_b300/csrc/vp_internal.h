@@ -41,6 +41,8 @@ struct DxPlan {
   double cost;
 };
 DxPlan dx_plan(int64_t rows, int64_t H);
+// The same plan for a grid of G persistent CTAs (dx_plan: the device's SM count).
+DxPlan dx_plan_on(int64_t rows, int64_t H, int64_t G);
 // dW through X^T (A K-major): Xt = X^T [H][ldxt] bf16 (transpose_bf16 of X).
 // cudaErrorNotSupported under GEMM form 2 (callers then use bf16_dw_chunk).
 cudaError_t bf16_dwt_chunk(const void* Xt, int64_t ldxt, const void* dz, int64_t ldz, int64_t N, int64_t H,
