@@ -100,7 +100,7 @@ GEMM_TRAFFIC = {"workload": "v128k", "path": "fused", "gemm_variant": "single", 
                 "by_stage": {"lse_p_gemm": 9.06e9, "dw_gemm": 28.07e9, "dx_gemm": 14.63e9},
                 "sources": ("vocab_lm_head_vp_b300/csrc/ce_bf16.cu", "vocab_lm_head_vp_b300/csrc/ptx.cuh",
                             "vocab_lm_head_vp_b300/csrc/umma_gemm.cuh", "vocab_lm_head_vp_b300/csrc/umma_gemm_2sm.cuh"),
-                "sha256": "237b6cf423f2f21449d060e2032c86f270088532b01b09dcd4e96083fd63444c"}
+                "sha256": "df4529958c82f8e67c44fe513afdfe4a481f4678d5a030decd4806fe63e306d3"}
 
 
 def gemm_traffic(workload, path, variant, token_chunk):
