@@ -20,7 +20,7 @@ import torch
 
 __all__ = ["embed_fwd", "embed_fwd_sp", "embed_bwd", "embed_bwd_plan", "embed_bwd_planned", "lmhead_ce_fwd", "lmhead_ce_bwd", "lmhead_ce_fwd_bwd", "lmhead_ce",
            "lmhead_ce_shard_fwd", "lmhead_ce_merge_stats", "lmhead_ce_shard_bwd", "vocab_parallel_lmhead_ce", "workspace_size", "read_device_status",
-           "test_gemm_bf16", "set_gemm_variant", "set_wait_fault", "stage_timing_enable", "stage_timing_read", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
+           "test_gemm_bf16", "set_gemm_variant", "dx_plan", "set_wait_fault", "stage_timing_enable", "stage_timing_read", "VpError", "library_path", "VP_F32", "VP_BF16", "IGNORE_INDEX"]
 
 VP_F32, VP_BF16 = 0, 1
 IGNORE_INDEX = -100
