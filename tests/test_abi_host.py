@@ -262,6 +262,11 @@ def test_dx_plan_choices(lib):
         p = vp.dx_plan(rows, H, sms)
         assert (p["tile_rows"], p["streamk"]) == (tile_rows, streamk), (rows, H, sms, p)
         assert abs(p["cost"] - cost) < 1e-9, (rows, H, sms, p)
+    # the shapes of the GPU test of the dX tile forms (test_gpu_ce.py), on 148 SMs: stream-K where
+    # it expects the GEMM and its fix-up pass
+    for rows, H, streamk in [(300, 264, False), (1100, 512, False), (77, 64, False), (2600, 1032, True),
+                             (768, 4096, True), (700, 4104, True)]:
+        assert vp.dx_plan(rows, H, 148)["streamk"] == streamk, (rows, H)
     # GEMM form 2 keeps 128-row tiles and no stream-K
     vp.set_gemm_variant(2)
     try:
