@@ -65,8 +65,9 @@ vp_status vp_test_dx_plan(int64_t rows, int64_t H, int sms, int32_t* tile_rows, 
 
 /*
  * vp_test_set_wait_fault -- exercise the bounded waits of the tcgen05 GEMMs.
- * Applies to every later bf16 GEMM launch of this process (one-SM and SM-pair
- * forms; in a pair, both CTAs' producers, or the leader's MMA issuer):
+ * Applies to every later bf16 GEMM launch of this process (one-SM, SM-pair and
+ * multicast-cluster forms; in a pair, both CTAs' producers or the leader's MMA
+ * issuer; in a multicast cluster, both CTAs' producers or MMA issuers):
  *   mode 0: normal operation (the default);
  *   mode 1: the TMA producer issues no load, so the MMA issuer's wait for
  *           data runs out (VP_DEV_TIMEOUT_MMA) and the epilogue's wait for an
