@@ -118,10 +118,11 @@ def _check(inp, T, f, dX, dW, ignore_index=IGN, dloss=None, check_stats=True):
     return ex, ew
 
 
-def test_tiny_config_f32():
+@pytest.mark.parametrize("T", [1, 2, 4, 16])   # every T in {1, 2, the config's 4, 16}: all divide V = 16
+def test_tiny_config_f32(T):
     inp = synth.make_inputs("tiny")
-    f, dX, dW = _run(inp, inp.wl.T)
-    _check(inp, inp.wl.T, f, dX, dW)
+    f, dX, dW = _run(inp, T)
+    _check(inp, T, f, dX, dW)
 
 
 def test_page_t4_simulation_f32():

@@ -112,10 +112,14 @@ def test_fused_minimind_config():
     print(f"minimind fused rel Frobenius dX {ex:.3e} dW {ew:.3e}")
 
 
-def test_fused_tiny_config_and_repeatable():
+@pytest.mark.parametrize("T", [1, 2, 4, 16])   # every T in {1, 2, the config's 4, 16}: all divide V = 16
+def test_fused_tiny_config(T):
     inp = synth.make_inputs("tiny")
-    o, dX, dW = _fused(inp, inp.wl.T)
-    _check(inp, inp.wl.T, o, dX, dW)
+    o, dX, dW = _fused(inp, T)
+    _check(inp, T, o, dX, dW)
+
+
+def test_fused_repeatable():
     inp = synth.small_case(300, 256, 1500, 3, "bf16", seed=2)
     a = _fused(inp, 3)
     b = _fused(inp, 3)
