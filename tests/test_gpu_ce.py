@@ -138,6 +138,53 @@ def test_page_t4_simulation_f32():
     assert np.allclose(np64(f["loss"]), dense["loss"])          # the page's printed True
 
 
+@pytest.mark.parametrize("path", ["split", "fused"])
+@pytest.mark.parametrize("zero", ["W", "X"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_constant_logits_closed_form(dtype, zero, path):
+    """Every logit 0 (W = 0, or X = 0; several tiles, a ragged token tail,
+    shard edges inside tiles): the GPU path against the closed form rather
+    than the oracle.  Each valid token's loss and every lse are log V, each
+    shard reports m_t = 0, S_t = V/T, z_y^(t) = 0, and dZ = g (1/V - 1[j=y]):
+    with W = 0 dX is exactly 0 and dW = dZ^T X, with X = 0 dW is exactly 0 and
+    dX = dZ W ("Vocab Parallelism" sec. 5.3.1-5.3.2)."""
+    N, H, V, T = 300, 64, 1000, 8
+    inp = synth.small_case(N, H, V, T, dtype, seed=91, ignore_frac=0.1)
+    inp.targets[:2] = [V, -3]                      # out of range: ignored and counted
+    for a in ((inp.W, inp.W_bits) if zero == "W" else (inp.X, inp.X_bits)):
+        if a is not None:
+            a[...] = 0
+    if path == "split":
+        f, dX, dW = _run(inp, T)
+    else:
+        X, W, y = dev_inputs(inp)
+        f = vp.lmhead_ce_fwd_bwd(X, W, y, T, shard_stats=True)
+        torch.cuda.synchronize()
+        assert vp.read_device_status(f["workspace"]) == 0
+        dX, dW = f["dX"], f["dW"]
+    y = inp.targets
+    valid = (y >= 0) & (y < V)
+    logV = np.log(V)
+    loss, lse = np64(f["loss"]), np64(f["lse"])
+    assert np.all(np.abs(loss[valid] - logV) <= 1e-5 * logV) and np.all(loss[~valid] == 0.0)
+    assert np.all(np.abs(lse - logV) <= 1e-5 * logV)
+    assert abs(float(f["mean"].item()) - logV) <= 1e-5 * logV
+    assert int(f["n_bad"].item()) == 2
+    st = np64(f["shard_stats"])
+    assert np.all(st[:, 0] == 0.0) and np.all(st[:, 2] == 0.0)
+    assert np.all(np.abs(st[:, 1] - V / T) <= 1e-5 * V / T)
+    g = np.where(valid, 1.0 / valid.sum(), 0.0)
+    onehot = np.zeros((N, V))
+    onehot[np.nonzero(valid)[0], y[valid]] = 1.0
+    dZ = g[:, None] * (1.0 / V - onehot)
+    if zero == "W":
+        assert np.all(np64(dX) == 0.0)
+        assert rel_fro(np64(dW), dZ.T @ np.asarray(inp.X, np.float64)) <= grad_tol(dtype)
+    else:
+        assert np.all(np64(dW) == 0.0)
+        assert rel_fro(np64(dX), dZ @ np.asarray(inp.W, np.float64)) <= grad_tol(dtype)
+
+
 def _argmax_case(N, V, dtype, seed):
     """Logits chosen directly (X = Z, W = I, H = V, so the kernel's logits are
     exactly X): most targets are the row's maximum by a margin that puts the
