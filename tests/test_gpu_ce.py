@@ -103,6 +103,9 @@ def _run(inp, T, ignore_index=IGN, dloss=None, vocab_chunk=None, shard_stats=Tru
 def _check(inp, T, f, dX, dW, ignore_index=IGN, dloss=None, check_stats=True):
     wl = inp.wl
     o = ref.lmhead_ce_forward(inp.X, inp.W, inp.targets, wl.V, T, ignore_index)
+    # l_n = log1p(R) + (m - z_y): both terms are non-negative (z_y is one of the
+    # logits the maximum m is taken over), so no token's loss is below 0
+    assert (np64(f["loss"]) >= 0.0).all(), "negative per-token loss"
     assert_lse_close(np64(f["lse"]), o["lse"], inp)
     assert_loss_close(np64(f["loss"]), o["loss"], wl.dtype, what="loss")
     assert_loss_close(np64(f["mean"]), [o["mean"]], wl.dtype, what="mean")
