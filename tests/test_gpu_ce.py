@@ -44,15 +44,18 @@ def test_embed_worked_example(dtype):
         assert np.array_equal(out.float().cpu().numpy(), want)
 
 
-@pytest.mark.parametrize("name", ["tiny", "minimind"])
-def test_embed_workload_bit_exact(name):
+@pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 2), ("tiny", 4), ("tiny", 16),
+                                    ("minimind", 1), ("minimind", 2), ("minimind", 16)])
+def test_embed_workload_bit_exact(name, T):
+    """Each workload's ids gathered at every T in {1, 2, its own T, 16} that
+    divides V: bit-exact against the oracle's shard sum at that T."""
     inp = synth.make_inputs(name)
     wl = inp.wl
     X, W, y = dev_inputs(inp)
     ids = inp.targets
-    out = vp.embed_fwd(y, W, wl.T)
+    out = vp.embed_fwd(y, W, T)
     torch.cuda.synchronize()
-    assert np.array_equal(_bits(out), _oracle_embed_bits(ids, inp.W, wl.V, wl.T, wl.dtype))
+    assert np.array_equal(_bits(out), _oracle_embed_bits(ids, inp.W, wl.V, T, wl.dtype))
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
