@@ -111,6 +111,32 @@ def pin_ce_closed_form(o):
         np.testing.assert_allclose(st[:, 2], 0.0)
 
 
+def pin_ce_shift_invariance(o):
+    """Moving every logit of a row by the same constant c leaves the softmax,
+    the loss and the logit gradient unchanged and moves lse by c.  With logits
+    near +-1000, where e^z overflows or underflows in float64, only the
+    max-shifted forms ([VP-book] sec. 5.3.1 CE(x,k) = -x_k + m + log sum
+    e^(x_i - m); the interview note's key formulas) stay finite and agree with
+    the unshifted row: the dense form, its gradient and the shard merge."""
+    rng = np.random.default_rng(12)
+    n, V = 7, 20
+    Z = rng.standard_normal((n, V)) * 3
+    y = rng.integers(0, V, n)
+    y[4] = IGN
+    base = o.cross_entropy(Z, y, IGN)
+    g = o.upstream_scale(y, V, IGN)
+    dZ = o.grad_logits(Z, y, base["lse"], g)
+    for c in (1000.0, -1000.0):
+        r = o.cross_entropy(Z + c, y, IGN)
+        assert np.all(np.isfinite(r["lse"])) and np.all(np.isfinite(r["loss"])), c
+        np.testing.assert_allclose(r["loss"], base["loss"], rtol=1e-9, atol=1e-9)
+        np.testing.assert_allclose(r["lse"] - c, base["lse"], rtol=0, atol=1e-9)
+        np.testing.assert_allclose(o.grad_logits(Z + c, y, r["lse"], g), dZ, rtol=1e-9, atol=1e-15)
+        for T in (2, 4, 5):
+            mg = o.merge_local_stats(o.shard_local_stats(Z + c, y, V, T))
+            np.testing.assert_allclose(mg["lse"] - c, base["lse"], rtol=0, atol=1e-9)
+
+
 def pin_ce_ignore_and_bad(o):
     """Ignored and out-of-range targets: loss 0, excluded from the mean; all
     ignored gives mean 0; out-of-range non-ignored targets are counted."""
@@ -379,6 +405,6 @@ def pin_embed_bwd_finite_differences(o):
 ALL_PINS = [pin_embed_worked_table, pin_embed_figure1, pin_embed_brute_force,
             pin_embed_sp, pin_embed_bwd_worked_table, pin_embed_bwd_adjoint, pin_embed_bwd_library,
             pin_embed_bwd_finite_differences,
-            pin_ce_library, pin_ce_closed_form, pin_ce_ignore_and_bad,
+            pin_ce_library, pin_ce_closed_form, pin_ce_shift_invariance, pin_ce_ignore_and_bad,
             pin_shard_invariance, pin_page_t4_simulation,
             pin_grad_library, pin_grad_finite_differences, pin_rows_variant, pin_dw_rows_variant]

@@ -113,7 +113,24 @@ def _dw_rows_no_onehot(X, W, y, lse, vocab_rows, n_valid, ignore_index=-100):
     return (g[:, None] * np.exp(Zv - np.asarray(lse)[:, None])).T @ X64      # the -1[y = v] term dropped
 
 
-_ORIG = {k: getattr(ref, k) for k in ("cross_entropy", "merge_local_stats")}
+def _ce_lse_unshifted(Z, y, ignore_index=-100):
+    r = _ORIG["cross_entropy"](Z, y, ignore_index)
+    with np.errstate(over="ignore"):
+        r["lse"] = np.log(np.exp(np.asarray(Z, dtype=np.float64)).sum(axis=1))   # max shift dropped
+    return r
+
+
+def _shard_stats_unshifted(Z, y, V, T, ignore_index=-100):
+    out = _ORIG["shard_local_stats"](Z, y, V, T, ignore_index)
+    Z = np.asarray(Z, dtype=np.float64)
+    for t, (a, b) in enumerate(ref.shard_bounds(V, T)):
+        out[t, 0] = 0.0
+        with np.errstate(over="ignore"):
+            out[t, 1] = np.exp(Z[:, a:b]).sum(axis=1)                   # local max not subtracted
+    return out
+
+
+_ORIG = {k: getattr(ref, k) for k in ("cross_entropy", "merge_local_stats", "shard_local_stats")}
 
 MUTANTS = {
     "ce_drop_max_term": ("cross_entropy", _ce_drop_shift),
@@ -122,6 +139,8 @@ MUTANTS = {
     "shard_off_by_one": ("shard_bounds", _shard_off_by_one),
     "mean_scale_over_N": ("upstream_scale", _scale_by_n),
     "merge_no_rescale": ("merge_local_stats", _merge_no_rescale),
+    "ce_lse_unshifted": ("cross_entropy", _ce_lse_unshifted),
+    "shard_stats_unshifted": ("shard_local_stats", _shard_stats_unshifted),
     "embed_no_mask": ("embed_shard_partial", _embed_no_mask),
     "embed_bwd_keep_masked_rows": ("embed_shard_grad", _embed_bwd_keep_masked),
     "embed_bwd_assign_not_add": ("embed_shard_grad", _embed_bwd_assign),
