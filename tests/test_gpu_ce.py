@@ -191,6 +191,55 @@ def test_constant_logits_closed_form(dtype, zero, path):
         assert rel_fro(np64(dX), dZ @ np.asarray(inp.W, np.float64)) <= grad_tol(dtype)
 
 
+@pytest.mark.parametrize("path", ["split", "fused"])
+@pytest.mark.parametrize("c", [1000.0, -1000.0])
+def test_large_logits_bf16(c, path):
+    """Every logit of every row moved by c = +-1000 (X gets a column of ones,
+    W a column of c; exact in bf16): e^z would overflow or vanish without the
+    max shift, and softmax and loss are unchanged by it.  Both paths against
+    the oracle on the shifted inputs, statistics and gradients element by
+    element ("Vocab Parallelism" sec. 5.3.1, CE(x,k) = -x_k + m + log sum
+    e^(x_i - m))."""
+    N, H, V, T = 300, 64, 1000, 4
+    base = synth.small_case(N, H, V, T, "bf16", seed=93, ignore_frac=0.1)
+    pad = np.zeros((N, 8), np.float32)
+    pad[:, 0] = 1.0
+    wpad = np.zeros((V, 8), np.float32)
+    wpad[:, 0] = c
+    X = np.concatenate([base.X, pad], axis=1)
+    W = np.concatenate([base.W, wpad], axis=1)
+    bits = lambda a: torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    wl = synth.Workload("shifted", N, H + 8, V, T, "bf16", 0.0, "uniform")
+    inp = synth.Inputs(wl, X, W, base.targets, bits(X), bits(W))
+    assert np.array_equal(torch.from_numpy(bits(W).view(np.int16)).view(torch.bfloat16).float().numpy(), W)
+    if path == "split":
+        f, dX, dW = _run(inp, T)
+    else:
+        Xd, Wd, y = dev_inputs(inp)
+        f = vp.lmhead_ce_fwd_bwd(Xd, Wd, y, T, shard_stats=True)
+        torch.cuda.synchronize()
+        assert vp.read_device_status(f["workspace"]) == 0
+        dX, dW = f["dX"], f["dW"]
+    assert torch.isfinite(f["loss"]).all() and torch.isfinite(f["lse"]).all()
+    assert (np64(f["loss"]) >= 0.0).all()
+    o = ref.lmhead_ce_forward(inp.X, inp.W, inp.targets, V, T)
+    assert_lse_close(np64(f["lse"]), o["lse"], inp)
+    assert_loss_close(np64(f["loss"]), o["loss"], "bf16", what="loss")
+    assert_loss_close(np64(f["mean"]), [o["mean"]], "bf16", what="mean")
+    assert int(f["n_bad"].item()) == o["n_bad"]
+    assert_stats_close(np64(f["shard_stats"]), o["shard_stats"], inp, T)
+    b = ref.lmhead_ce_backward(inp.X, inp.W, inp.targets, V)
+    # dX's column of the constant feature is c * sum_v dZ[n, v], exactly 0 (the
+    # rows of dZ sum to 0) but made of terms up to c * g: the bf16 rounding of
+    # dZ leaves ~c * g * 2^-9 there, larger than the other columns' entries, so
+    # a per-tensor relative norm says nothing for it; the elementwise bound,
+    # which scales with each entry's terms, covers every column
+    dXn = np64(dX)
+    assert rel_fro(dXn[:, :H], b["dX"][:, :H]) <= grad_tol("bf16") and rel_fro(np64(dW), b["dW"]) <= grad_tol("bf16")
+    assert np.all(dXn[:, H + 1:] == 0.0)
+    assert_grads_elementwise(inp, dX, dW, b)
+
+
 def _argmax_case(N, V, dtype, seed):
     """Logits chosen directly (X = Z, W = I, H = V, so the kernel's logits are
     exactly X): most targets are the row's maximum by a margin that puts the
